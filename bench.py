@@ -1,0 +1,428 @@
+"""Benchmark of the TQ2_0_g128 ternary matmul library on GB300.
+
+Default workload (one JSON line on rank 0): the M=1 decode GEMV, K=4096,
+N=12288 (the fused gate/up shape), on seeded synthetic inputs.  One step is
+one tq2_gemv call through the C ABI; K steps are captured in a CUDA graph and
+replayed once inside the timed region, each step reading a different copy of
+the weight so that the copies together exceed twice the L2 size.  `value` is
+the weight bytes streamed per second (all ranks).  The same JSON line also
+carries the large-M GEMM numbers (M=1536, K=3072, N in {3072, 9216, 12288},
+TFLOP/s) measured the same way.
+
+`--impl reference` times the CPU oracle (test infrastructure, double
+precision) on the same workload and metric instead.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import tq2_synth  # noqa: E402
+
+METRIC = "TQ2 GEMM TFLOP/s @M=1536 and GEMV weight-GB/s @M=1, as % of GB300 roofline"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-gemm", action="store_true", help="skip the large-M GEMM section")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--gemm-steps", type=int, default=20)
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        hbm = float(d.get("hbm_gbs"))
+        bf16 = float(d.get("bf16_tflops"))
+        bf16s = float(d.get("bf16_tflops_sustained", bf16))
+        return hbm, bf16, bf16s, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def dist_setup(gpus):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    return world, rank, local, pg
+
+
+def max_over_ranks(value, pg, device):
+    if pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(pg):
+    if pg is not None:
+        pg.barrier()
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling while the GPU is busy."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def source_hash(*files):
+    h = hashlib.sha256()
+    for f in files:
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, src_files):
+    """Per-launch DRAM bytes from a committed ncu summary, if taken on the
+    current source of the kernel; else None."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[kernel_key]
+        if e.get("source_hash") != source_hash(*src_files):
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------
+# our arm
+
+
+def graph_of(fn, steps, torch):
+    """Capture `steps` calls fn(i) into one CUDA graph."""
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            for i in range(steps):
+                fn(i)
+    torch.cuda.current_stream().wait_stream(s)
+    return g
+
+
+def time_graph(g, torch, pg, device, reps=1):
+    """Device time (s) of one replay, CUDA events on the replay stream, max over ranks."""
+    best = []
+    for _ in range(reps):
+        barrier(pg)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        g.replay()
+        e1.record()
+        torch.cuda.synchronize()
+        barrier(pg)
+        best.append(e0.elapsed_time(e1) / 1e3)
+    t = statistics.median(best)
+    return max_over_ranks(t, pg, device)
+
+
+def run_ours(args, world, rank, local, pg):
+    import torch
+    import dit_tq2_g128_gb300 as tq2
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    hbm, bf16, bf16s, peak_src = peaks()
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
+
+    # ---- decode GEMV workload (per rank an independent problem: weak scaling)
+    p = tq2_synth.decode_gate_up(seed=rank)
+    wbytes = tq2.tq2_soa_bytes(p.n, p.k)
+    copies = max(2, -(-2 * l2 // wbytes) + 1)
+    w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
+    ws = [w0] + [w0.clone() for _ in range(copies - 1)]
+    x = torch.from_numpy(p.x[0]).to(device)
+    out = torch.empty(p.n, dtype=torch.float32, device=device)
+
+    def step(i):
+        tq2.tq2_gemv(ws[i % copies], x, None, out, p.n, p.k)
+
+    for i in range(max(3, args.warmup)):
+        step(i)
+    torch.cuda.synchronize()
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    gw = graph_of(step, max(3, args.warmup), torch)
+    gt = graph_of(step, args.steps, torch)
+    gw.replay()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        # sustained window for the clock record (same graph, >= 1 s of load)
+        t_end = time.time() + 1.0
+        while time.time() < t_end:
+            gt.replay()
+            torch.cuda.synchronize()
+        t_step = time_graph(gt, torch, pg, device, reps=1)
+    clocks = clk.summary()
+    per_launch = t_step / args.steps
+    value = world * wbytes * args.steps / t_step / 1e9
+    achieved = wbytes / per_launch / 1e9
+
+    # ---- end to end through the C ABI with host buffers
+    x_host = torch.from_numpy(p.x[0].copy()).pin_memory()
+    out_host = torch.empty(p.n, dtype=torch.float32).pin_memory()
+    xd = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def e2e_step(i):
+        xd.copy_(x_host, non_blocking=True)
+        tq2.tq2_gemv(ws[i % copies], xd, None, out, p.n, p.k)
+        out_host.copy_(out, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(pg)
+    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, pg, device)
+    e2e = {"value": world * wbytes * args.steps / t_e2e / 1e9, "unit": "GB/s",
+           "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(out_host.numel() * 4),
+           "note": "weights resident (uploaded once); x up and out down every step, pinned host buffers"}
+
+    gemv_src = ["dit_tq2_g128_gb300/csrc/gemv.cu"]
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s (TQ2 weight bytes, M=1 GEMV)",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(t_step / args.steps * 1e3, 6),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32 (exact f32 products, f32 accumulation)",
+        "data": "synthetic (seeded numpy: x~N(0,1), codes P(0)=0.4 P(+-1)=0.3, d=f16(|N(0,0.02)|+1e-4))",
+        "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288,
+                   "weight_bytes": wbytes, "kernel": "tq2_gemv",
+                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
+                         f"({copies * wbytes / 2**20:.0f} MiB > 2x L2 {l2 / 2**20:.0f} MiB)",
+                   "timing": "K steps captured in one CUDA graph, one replay timed with CUDA events",
+                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
+                     "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} (copy bandwidth)",
+                     "traffic": ncu_traffic("gemv_m1_k4096_n12288", gemv_src),
+                     "algorithmic_bytes_per_launch": wbytes,
+                     "note": "achieved = weight bytes / (graph time / launches); includes inter-kernel gaps"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "impl": "ours",
+    }
+
+    # ---- large-M GEMM (tensor cores)
+    if not args.no_gemm:
+        gemm = {}
+        launches = 0
+        for n in tq2_synth.DIT_NS:
+            q = tq2_synth.dit(n, seed=rank)
+            per = q.m * q.k * 4 + tq2.tq2_soa_bytes(q.n, q.k) + q.m * q.n * 4
+            c = max(2, -(-2 * l2 // per) + 1)
+            wq = tq2.upload_weight(q.w_aos, q.n, q.k)
+            wl = [wq] + [wq.clone() for _ in range(c - 1)]
+            xl = [torch.from_numpy(q.x).to(device) for _ in range(c)]
+            ol = [torch.empty((q.m, q.n), dtype=torch.float32, device=device) for _ in range(c)]
+
+            def gstep(i, q=q, wl=wl, xl=xl, ol=ol, c=c):
+                tq2.tq2_gemm(wl[i % c], xl[i % c], None, ol[i % c], q.m, q.n, q.k)
+
+            for i in range(3):
+                gstep(i)
+            torch.cuda.synchronize()
+            assert tq2.tq2_device_status() == tq2.TQ2_OK
+            gg = graph_of(gstep, args.gemm_steps, torch)
+            gg.replay()
+            torch.cuda.synchronize()
+            tg = time_graph(gg, torch, pg, device, reps=3) / args.gemm_steps
+            launches += args.gemm_steps
+            flops = 2.0 * q.m * q.n * q.k
+            tfl = flops / tg / 1e12
+            gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "us_per_call": round(tg * 1e6, 2),
+                             "tflops": round(tfl, 1), "frac_of_bf16_burst": round(tfl / bf16, 4),
+                             "frac_of_bf16_sustained": round(tfl / bf16s, 4),
+                             "l2": f"{c} rotating (x, w, out) copies"}
+            del wl, xl, ol, wq
+            torch.cuda.empty_cache()
+        line["gemm_m1536"] = {
+            "kernel": "tq2_gemm -> tcgen05 kind::f16 (f16 operands, f32 accumulation in TMEM)",
+            "per_n": gemm,
+            "roofline": {"bound": "tensor", "unit": "TFLOP/s",
+                         "achieved": gemm["n12288"]["tflops"], "peak": bf16,
+                         "frac": round(gemm["n12288"]["tflops"] / bf16, 4),
+                         "peak_source": f"{peak_src} dense bf16 burst (f16 runs at the bf16 rate)",
+                         "traffic": None},
+            "note": "timed separately from `value`; steps per N captured in a CUDA graph"}
+    return line
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg, and the --impl reference arm)
+
+
+def oracle_gemv_rate(p, seconds):
+    """Weight GB/s of the oracle on the decode GEMV; runs whole calls for about `seconds`."""
+    import oracle
+    wbytes = p.w_aos.size
+    oracle.matmul(p.w_aos[:64], p.x, n=64, k=p.k)  # build + warm
+    t0 = time.perf_counter()
+    calls = 0
+    while True:
+        oracle.matmul(p.w_aos, p.x, n=p.n, k=p.k)
+        calls += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return calls * wbytes / el / 1e9, calls, el, oracle.threads()
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return None
+    import oracle
+    p = tq2_synth.decode_gate_up()
+    wbytes = p.w_aos.size
+    for _ in range(args.warmup):
+        oracle.matmul(p.w_aos, p.x, n=p.n, k=p.k)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.matmul(p.w_aos, p.x, n=p.n, k=p.k)
+    el = time.perf_counter() - t0
+    v = args.steps * wbytes / el / 1e9
+    cores = oracle.threads()
+    return {
+        "metric": METRIC, "value": round(v, 4), "unit": "GB/s (TQ2 weight bytes, M=1 GEMV)",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
+        "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} full GEMV calls (12288x4096), double precision"},
+        "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world, rank, local, pg = dist_setup(args.gpus)
+    if args.impl == "reference":
+        line = run_reference(args, world, rank)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args, world, rank, local, pg)
+    if rank == 0:
+        if not args.no_cpu and world == 1:
+            p = tq2_synth.decode_gate_up()
+            v, calls, el, cores = oracle_gemv_rate(p, 10.0)
+            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
+                                    "kind": "oracle",
+                                    "sample": f"{calls} full decode GEMV calls in {el:.1f} s "
+                                              "(double precision, OpenMP over output rows)"}
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,203 @@
+// C-ABI entry points: host-side validation, kernel choice by shape, launch.
+//
+// The contract follows "oxibonsai-image 0.2.2 src/gpu.rs" (`ternary_matmul_gpu`
+// and its module doc "Correctness contract"): row-major f32 input[M,K],
+// out-major TQ2_0_g128 weight blocks [N, K/128], f32 out[M,N] written in full,
+// K a multiple of 128.  Unlike the page, every failure is a returned status
+// and there is no CPU fallback.
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "tq2_internal.cuh"
+
+namespace {
+
+// Device status word: kernels OR TQ2_ERR_TIMEOUT into it when a bounded wait
+// gives up.  Static device memory of this module (one word per device).
+__device__ unsigned int g_device_status;
+
+std::atomic<uint64_t> g_wait_ns{2000000000ull};
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+    int checked = 0;    // 0 = not yet, 1 = supported, -1 = unsupported
+    int num_sms = 0;
+    unsigned int *status = nullptr;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mu;
+
+// Looks up (once per device) whether the current device is sm_103 and where
+// its status word lives.
+int current_device(DeviceInfo *out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ2_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TQ2_ERR_UNSUPPORTED_DEVICE;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DeviceInfo &d = g_dev[dev];
+    if (d.checked == 0) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TQ2_ERR_CUDA;
+        if (major != 10 || minor != 3) {
+            d.checked = -1;
+        } else {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return TQ2_ERR_CUDA;
+            d.status = static_cast<unsigned int *>(p);
+            d.num_sms = sms;
+            d.checked = 1;
+        }
+    }
+    if (d.checked < 0) return TQ2_ERR_UNSUPPORTED_DEVICE;
+    *out = d;
+    return TQ2_OK;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+    uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return na && nb && x < y + nb && y < x + na;
+}
+
+// Shape checks shared by every matmul entry point.  Returns TQ2_OK and sets
+// *noop when there is nothing to compute.
+int check_matmul(const void *w, const float *x, const float *residual, const float *out,
+                 int64_t m, int64_t n, int64_t k, bool *noop) {
+    *noop = false;
+    if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
+    if (m < 0 || n < 0) return TQ2_ERR_INVALID_ARG;
+    const int64_t lim = int64_t(1) << 40;  // element counts beyond this are rejected
+    if (k > lim || m > lim || n > lim || (m && k > lim / m) || (n && k > lim / n) ||
+        (m && n > lim / m))
+        return TQ2_ERR_INVALID_ARG;
+    if (m == 0 || n == 0) {
+        *noop = true;
+        return TQ2_OK;
+    }
+    if (!w || !x || !out) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(x) || !aligned16(out) || (residual && !aligned16(residual)))
+        return TQ2_ERR_MISALIGNED;
+    const size_t wb = size_t(n) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
+    const size_t xb = size_t(m) * size_t(k) * 4, ob = size_t(m) * size_t(n) * 4;
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, w, wb)) return TQ2_ERR_INVALID_ARG;
+    if (residual && residual != out && overlaps(out, ob, residual, ob)) return TQ2_ERR_INVALID_ARG;
+    return TQ2_OK;
+}
+
+int make_ctx(cudaStream_t stream, tq2::LaunchCtx *ctx) {
+    DeviceInfo d;
+    int st = current_device(&d);
+    if (st != TQ2_OK) return st;
+    ctx->stream = stream;
+    ctx->status = d.status;
+    ctx->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
+    ctx->num_sms = d.num_sms;
+    return TQ2_OK;
+}
+
+int finish(cudaError_t e) { return e == cudaSuccess ? TQ2_OK : TQ2_ERR_CUDA; }
+
+// M at and above which the tcgen05 kernel beats the f32 CUDA-core small-M kernel.
+constexpr int64_t kTcMinM = 4;
+
+}  // namespace
+
+extern "C" {
+
+size_t tq2_soa_bytes(int64_t n, int64_t k) {
+    if (n < 0 || k <= 0 || k % tq2::kBlockW) return 0;
+    return size_t(n) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
+}
+
+const char *tq2_status_string(int status) {
+    switch (status) {
+        case TQ2_OK: return "TQ2_OK";
+        case TQ2_ERR_INVALID_ARG: return "TQ2_ERR_INVALID_ARG: null pointer, negative size, overlap or size overflow";
+        case TQ2_ERR_BAD_K: return "TQ2_ERR_BAD_K: k must be a positive multiple of 128";
+        case TQ2_ERR_MISALIGNED: return "TQ2_ERR_MISALIGNED: device pointers must be 16-byte aligned";
+        case TQ2_ERR_UNSUPPORTED_DEVICE: return "TQ2_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
+        case TQ2_ERR_CUDA: return "TQ2_ERR_CUDA: CUDA launch or runtime error";
+        case TQ2_ERR_TIMEOUT: return "TQ2_ERR_TIMEOUT: a bounded device-side wait expired";
+        default: return "unknown tq2 status";
+    }
+}
+
+int tq2_version(void) { return 0x000100; }
+
+uint64_t tq2_set_wait_timeout_ns(uint64_t ns) { return g_wait_ns.exchange(ns); }
+
+int tq2_device_status(void *stream) {
+    DeviceInfo d;
+    int st = current_device(&d);
+    if (st != TQ2_OK) return st;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return TQ2_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpy(&v, d.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ2_ERR_CUDA;
+    if (cudaMemcpy(d.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TQ2_ERR_CUDA;
+    return (v & TQ2_ERR_TIMEOUT) == TQ2_ERR_TIMEOUT ? TQ2_ERR_TIMEOUT : TQ2_OK;
+}
+
+int tq2_select_kernel(int64_t m, int64_t n, int64_t k) {
+    (void)n;
+    (void)k;
+    if (m == 1) return TQ2_KERNEL_GEMV;
+    if (m < kTcMinM && m <= tq2::kSkinnyMaxM) return TQ2_KERNEL_SKINNY;
+    return TQ2_KERNEL_TC;
+}
+
+int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k, void *stream) {
+    if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
+    if (n < 0 || n > (int64_t(1) << 40) / (k / tq2::kBlockW)) return TQ2_ERR_INVALID_ARG;
+    if (n == 0) return TQ2_OK;
+    if (!w_aos || !w_soa) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(w_soa)) return TQ2_ERR_MISALIGNED;
+    if (overlaps(w_aos, tq2_soa_bytes(n, k), w_soa, tq2_soa_bytes(n, k))) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_reformat(w_aos, w_soa, n, k, ctx));
+}
+
+int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *residual,
+                  float *out, int64_t m, int64_t n, int64_t k, void *stream) {
+    bool noop = false;
+    int st = check_matmul(w_soa, x, residual, out, m, n, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    if (kernel == TQ2_KERNEL_AUTO) kernel = tq2_select_kernel(m, n, k);
+    if (kernel == TQ2_KERNEL_GEMV && m != 1) return TQ2_ERR_INVALID_ARG;
+    if (kernel == TQ2_KERNEL_SKINNY && m > tq2::kSkinnyMaxM) return TQ2_ERR_INVALID_ARG;
+    if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_F32REF) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    switch (kernel) {
+        case TQ2_KERNEL_GEMV: return finish(tq2::launch_gemv(w_soa, x, residual, out, n, k, ctx));
+        case TQ2_KERNEL_SKINNY:
+            return finish(tq2::launch_skinny(w_soa, x, residual, out, m, n, k, ctx));
+        case TQ2_KERNEL_TC: return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
+        default: return finish(tq2::launch_f32ref(w_soa, x, residual, out, m, n, k, ctx));
+    }
+}
+
+int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,
+             int64_t n, int64_t k, void *stream) {
+    return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
+}
+
+int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out, int64_t n,
+             int64_t k, void *stream) {
+    return tq2_gemm_with(TQ2_KERNEL_GEMV, w_soa, x, residual, out, 1, n, k, stream);
+}
+
+int tq2_gemm_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
+                    int64_t m, int64_t n, int64_t k, void *stream) {
+    return tq2_gemm_with(TQ2_KERNEL_F32REF, w_soa, x, residual, out, m, n, k, stream);
+}
+
+}  // extern "C"

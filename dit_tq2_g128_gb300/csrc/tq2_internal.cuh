@@ -1,0 +1,202 @@
+// Internal declarations and device helpers of the TQ2_0_g128 CUDA library.
+// Everything here is sm_103a code written against the public PTX ISA
+// (mbarrier, tcgen05, fences); nothing is shared with the CPU oracle.
+#pragma once
+
+#include <cstdint>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "tq2.h"
+
+namespace tq2 {
+
+constexpr int kBlockW = 128;    // weights per block
+constexpr int kQsBytes = 32;    // code bytes per block
+constexpr int kBlockBytes = 34; // qs[32] + binary16 d
+
+// Per-launch context the API layer hands every kernel launcher.
+struct LaunchCtx {
+    cudaStream_t stream;
+    unsigned int *status;  // device status word (TQ2_ERR_TIMEOUT is OR-ed in)
+    uint64_t wait_ns;      // limit of every bounded device-side wait
+    int num_sms;
+};
+
+// Views of the SoA weight buffer.
+struct SoaView {
+    const uint8_t *qs;   // [N][K/4]
+    const __half *d;     // [N][K/128]
+};
+
+inline SoaView soa_view(const void *w_soa, int64_t n, int64_t k) {
+    const uint8_t *base = static_cast<const uint8_t *>(w_soa);
+    int64_t nblk = n * (k / kBlockW);
+    return SoaView{base, reinterpret_cast<const __half *>(base + nblk * kQsBytes)};
+}
+
+// ---------------------------------------------------------------------------
+// Kernel launchers (one per .cu file).  All return cudaError_t of the launch.
+cudaError_t launch_reformat(const void *w_aos, void *w_soa, int64_t n, int64_t k,
+                            const LaunchCtx &ctx);
+cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
+                        int64_t n, int64_t k, const LaunchCtx &ctx);
+cudaError_t launch_skinny(const void *w_soa, const float *x, const float *residual, float *out,
+                          int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
+cudaError_t launch_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
+                          int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
+cudaError_t launch_tc(const void *w_soa, const float *x, const float *residual, float *out,
+                      int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
+
+// Largest M the small-M CUDA-core kernel handles.
+constexpr int64_t kSkinnyMaxM = 16;
+
+// ---------------------------------------------------------------------------
+// Device helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_mbarrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("{\n\t.reg .b64 st;\n\tmbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(
+                     smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  Returns false (and records
+// TQ2_ERR_TIMEOUT in *status) if the phase did not complete within
+// `limit_ns` of %globaltimer time.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
+                                                  uint64_t limit_ns, unsigned int *status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 >= limit_ns) {
+            atomicOr(status, static_cast<unsigned int>(TQ2_ERR_TIMEOUT));
+            return false;
+        }
+    }
+}
+
+// Make generic-proxy shared-memory writes visible to the async proxy
+// (the tensor core reads operands through it).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// --- tcgen05 ---------------------------------------------------------------
+
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on an mbarrier when all previously issued tcgen05 ops of this
+// thread have completed.
+__device__ __forceinline__ void tc_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+}
+
+// --- streaming global loads -------------------------------------------------
+
+__device__ __forceinline__ uint2 ldg_stream_u2(const void *p) {
+    uint2 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
+                 : "=r"(v.x), "=r"(v.y)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint4 ldg_stream_u4(const void *p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ unsigned short ldg_u16(const void *p) {
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(p));
+    return v;
+}
+
+}  // namespace tq2

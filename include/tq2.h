@@ -1,0 +1,159 @@
+/*
+ * tq2.h -- C ABI of the GB300 (sm_103a) TQ2_0_g128 ternary matmul library.
+ *
+ * Operation ("oxibonsai-image 0.2.2 src/gpu.rs", module doc "Correctness
+ * contract", and the doc of `ternary_matmul_gpu`):
+ *
+ *     out[m, n] = sum_k input[m, k] * dequant(W)[n, k]   (+ residual[m, n])
+ *
+ * with row-major f32 input[M, K], out-major weight blocks [N, K/128] and
+ * row-major f32 out[M, N], written in full.  K must be a positive multiple of
+ * 128 (the page rejects `k % 128 != 0`).
+ *
+ * Weight block ("BlockTQ2_0_g128", same page, doc of `blocks_as_bytes` and
+ * test `block_is_thirty_four_bytes`): 34 bytes, no padding, little endian:
+ *
+ *     struct { uint8_t qs[32]; uint16_t d; }   // d: IEEE binary16 scale
+ *
+ * Code convention of this library (the pages do not print it): weight j
+ * (0..127) of a block has the 2-bit code c = (qs[j/4] >> 2*(j%4)) & 3, and
+ * its value is (c - 1) * d, i.e. c in {0,1,2} -> {-1, 0, +1} * d.  Code 3 is
+ * never produced by an encoder; every entry point decodes it arithmetically
+ * as c - 1 = +2.
+ *
+ * Device weight layout (SoA; the "SoA weight buffer" that the TQ2 kernels
+ * read, named on the "oxibonsai-kernels 0.1.5
+ * src/gpu_backend/metal_graph/pipelines.rs" page; the layout itself is this
+ * library's definition).  For B = N*(K/128) blocks in row-major (n, b) order:
+ *
+ *     bytes [0, 32*B)          qs plane: block (n,b)'s qs[32] at (n*(K/128)+b)*32
+ *     bytes [32*B, 34*B)       d plane : block (n,b)'s d (2 bytes) at 32*B + (n*(K/128)+b)*2
+ *
+ * The total size equals the AoS size, tq2_soa_bytes(n, k) = N*(K/128)*34.
+ *
+ * Conventions shared by every entry point below:
+ *  - Pointers are DEVICE pointers owned by the caller; the library allocates
+ *    nothing, frees nothing and keeps no cache of weights (the pages' pointer-
+ *    keyed upload cache is the caller's job here).
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    is asynchronous on it and never synchronises the host.
+ *  - Errors are returned as a tq2_status; nothing aborts and there is no CPU
+ *    fallback.  Argument errors are detected on the host before any launch.
+ *    TQ2_ERR_CUDA means a launch or runtime error (the CUDA error is left for
+ *    the caller to inspect with cudaGetLastError/cudaPeekAtLastError).
+ *  - m == 0 or n == 0 is a successful no-op (nothing is launched, nothing is
+ *    read).  m, n must be >= 0; k must be a positive multiple of 128.
+ *  - Alignment: w_soa, x, residual and out must be 16-byte aligned (128-bit
+ *    loads and stores).  w_aos needs no alignment.
+ *  - Aliasing: `residual` may equal `out` exactly (in-place out += x.W^T);
+ *    otherwise no output may overlap an input.
+ *  - Device: compute capability 10.3 (sm_103a) only; any other device gives
+ *    TQ2_ERR_UNSUPPORTED_DEVICE.
+ */
+#ifndef TQ2_H_
+#define TQ2_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TQ2_OK = 0,
+    TQ2_ERR_INVALID_ARG = 1,        /* null pointer, negative size, bad aliasing, size overflow */
+    TQ2_ERR_BAD_K = 2,              /* k <= 0 or k % 128 != 0 */
+    TQ2_ERR_MISALIGNED = 3,         /* a pointer that must be 16-byte aligned is not */
+    TQ2_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103 */
+    TQ2_ERR_CUDA = 5,               /* launch or runtime error */
+    TQ2_ERR_TIMEOUT = 6             /* a bounded device-side wait expired (see tq2_device_status) */
+} tq2_status;
+
+/* Kernel choice for tq2_gemm_with().  TQ2_KERNEL_AUTO is what tq2_gemm uses. */
+typedef enum {
+    TQ2_KERNEL_AUTO = 0,
+    TQ2_KERNEL_GEMV = 1,   /* M == 1 only: f32 CUDA-core decode GEMV */
+    TQ2_KERNEL_SKINNY = 2, /* small M: f32 CUDA-core kernel, weights decoded once per M rows */
+    TQ2_KERNEL_TC = 3,     /* tcgen05 tensor-core kernel: f16 operands, f32 accumulation in TMEM */
+    TQ2_KERNEL_F32REF = 4  /* exact-f32 CUDA-core tiled kernel */
+} tq2_kernel;
+
+/* Bytes of a weight of n rows and k columns in either layout: n*(k/128)*34.
+ * Returns 0 for n < 0 or a k that is not a positive multiple of 128. */
+size_t tq2_soa_bytes(int64_t n, int64_t k);
+
+/* Human-readable name of a tq2_status value (static string, never NULL). */
+const char *tq2_status_string(int status);
+
+/* Relayout AoS weight blocks into the SoA layout above, bit-exactly.
+ * The pages convert the uploaded AoS bytes with a `reformat_tq2_aos_to_soa`
+ * kernel ("oxibonsai-image 0.2.2 src/gpu.rs", doc of `blocks_as_bytes`).
+ *   w_aos : device, n*(k/128)*34 bytes, AoS [N][K/128] blocks, any alignment
+ *   w_soa : device, same size, 16-byte aligned, must not overlap w_aos
+ */
+int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k, void *stream);
+
+/* M = 1 decode GEMV: out[n] = sum_k x[k] * dequant(W)[n,k] (+ residual[n]).
+ * The decode-path GEMV `gemv_tq2_g128_v1` of the "oxibonsai-kernels 0.1.5 ...
+ * pipelines.rs" page; the operation is the contract above with M = 1.
+ *   w_soa    : device SoA weight (tq2_soa_bytes(n,k) bytes)
+ *   x        : device f32 [k]
+ *   residual : device f32 [n], or NULL
+ *   out      : device f32 [n]
+ * Arithmetic: exact f32 products, f32 accumulation. */
+int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out,
+             int64_t n, int64_t k, void *stream);
+
+/* Any-M matmul with optional residual epilogue, dispatching on M (and N, K)
+ * between the GEMV, the small-M CUDA-core kernel and the tcgen05 tensor-core
+ * kernel ("oxibonsai-image 0.2.2 src/gpu.rs", `ternary_matmul_gpu`;
+ * the batched TQ2 GEMMs of the "oxibonsai-kernels 0.1.5 ... pipelines.rs"
+ * page).
+ *   w_soa    : device SoA weight
+ *   x        : device f32 [m, k] row-major
+ *   residual : device f32 [m, n] row-major, or NULL
+ *   out      : device f32 [m, n] row-major
+ * Arithmetic: the tensor-core kernel rounds x to binary16 (round to nearest
+ * even; |x| must stay below 65504) and multiplies by the exactly representable
+ * binary16 weights (c-1)*d with f32 accumulation; the CUDA-core kernels use
+ * exact f32 products and f32 accumulation. */
+int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out,
+             int64_t m, int64_t n, int64_t k, void *stream);
+
+/* Same operation as tq2_gemm, computed by the exact-f32 CUDA-core tiled
+ * kernel (the role of the pages' non-matrix-unit `gemm_tq2_g128_v8_tiled`,
+ * kept for tolerance checks). */
+int tq2_gemm_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
+                    int64_t m, int64_t n, int64_t k, void *stream);
+
+/* tq2_gemm with an explicit kernel choice (a tq2_kernel value), for
+ * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 (else
+ * TQ2_ERR_INVALID_ARG). */
+int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *residual,
+                  float *out, int64_t m, int64_t n, int64_t k, void *stream);
+
+/* The kernel that tq2_gemm picks for this shape (a tq2_kernel value).  Host
+ * only; needs no device. */
+int tq2_select_kernel(int64_t m, int64_t n, int64_t k);
+
+/* Bounded device-side waits.  Every spin-wait inside a kernel (on an mbarrier)
+ * gives up after `ns` nanoseconds of %globaltimer time, records
+ * TQ2_ERR_TIMEOUT in a device status word and lets the kernel exit cleanly
+ * (draining its own in-flight work first).  Default 2e9 (2 s).  Applies to
+ * launches issued after the call.  Returns the previous value. */
+uint64_t tq2_set_wait_timeout_ns(uint64_t ns);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device: TQ2_OK, or TQ2_ERR_TIMEOUT if any kernel since the last
+ * check gave up on a wait; TQ2_ERR_CUDA if the synchronisation itself failed. */
+int tq2_device_status(void *stream);
+
+/* Library version, e.g. 0x000100 for 0.1.0. */
+int tq2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ2_H_ */

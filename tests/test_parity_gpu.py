@@ -1,0 +1,275 @@
+"""GPU parity: every CUDA entry point against the CPU oracle, through the C ABI.
+
+Bars (per element, Sigma|xw| computed by the oracle in f64):
+  * reformat: bit-exact;
+  * f32 kernels (GEMV, small-M, f32ref): |out - ref| <= 1e-5 * Sigma|xw| + 2^-23 |residual|;
+  * tensor-core kernel: |out - ref| <= 4e-3 * Sigma|xw| + 2^-23 |residual|, and the
+    cosine between each output row and the oracle's row >= 0.9999.
+Large problems run in full on the GPU and are checked on sampled rows (all N
+columns of each sampled row) that the oracle computes one by one.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import tq2_synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+TOL_F32 = 1e-5
+TOL_TC = 4e-3
+COS_MIN = 0.9999
+
+
+@pytest.fixture(scope="module")
+def tq2():
+    import dit_tq2_g128_gb300 as m
+    return m
+
+
+def tol_for(tq2, kernel):
+    return TOL_TC if kernel == tq2.TQ2_KERNEL_TC else TOL_F32
+
+
+def upload(tq2, p):
+    return tq2.upload_weight(p.w_aos, p.n, p.k)
+
+
+def sample_rows(m, extra=12, seed=0):
+    base = {0, 1, m - 1, m // 2}
+    for r in (127, 128, 129, 255, 256, m - 128, m - 129):
+        if 0 <= r < m:
+            base.add(r)
+    rng = np.random.default_rng(seed)
+    base.update(rng.integers(0, m, size=min(extra, m)).tolist())
+    return np.array(sorted(base), dtype=np.int64)
+
+
+def check(out, p, kernel_tol, *, rows=None, cos=False, what=""):
+    out = np.asarray(out, dtype=np.float64).reshape(-1, p.n)
+    ref, scale = oracle.matmul(p.w_aos, p.x, p.residual, n=p.n, k=p.k, rows=rows)
+    got = out if rows is None else out[rows]
+    res = 0.0 if p.residual is None else np.abs(p.residual.reshape(-1, p.n)[
+        slice(None) if rows is None else rows].astype(np.float64))
+    bound = kernel_tol * scale + 2.0 ** -23 * res + 1e-30
+    err = np.abs(got - ref)
+    worst = float(np.max(err / bound)) if err.size else 0.0
+    assert np.all(err <= bound), f"{what}: max err/bound {worst:.3g}"
+    if cos:
+        num = np.sum(got * ref, axis=1)
+        den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+        c = np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)
+        assert np.all(c >= COS_MIN), f"{what}: min row cosine {c.min()}"
+    return worst
+
+
+def run(tq2, kernel, w, p, *, out=None, inplace=False):
+    x = torch.from_numpy(p.x).cuda()
+    r = None if p.residual is None else torch.from_numpy(p.residual).cuda()
+    if inplace:
+        out = r.clone()
+        r = out
+    elif out is None:
+        out = torch.full((p.m, p.n), float("nan"), dtype=torch.float32, device="cuda")
+    tq2.tq2_gemm_with(kernel, w, x, r, out, p.m, p.n, p.k)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# AoS -> SoA
+
+
+@pytest.mark.parametrize("n,k", [(1, 128), (3, 384), (17, 1024), (257, 256), (1000, 1152),
+                                 (12288, 4096)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_reformat_bit_exact(tq2, n, k, offset):
+    p = tq2_synth.make_problem(1, n, k, seed=n + k)
+    nbytes = tq2.tq2_soa_bytes(n, k)
+    raw = torch.zeros(nbytes + 64, dtype=torch.uint8, device="cuda")
+    raw[offset:offset + nbytes] = torch.from_numpy(p.w_aos.reshape(-1)).cuda()
+    soa = torch.full((nbytes + 32,), 0xA5, dtype=torch.uint8, device="cuda")
+    tq2.tq2_reformat_aos_to_soa(raw[offset:].data_ptr(), soa, n, k)
+    torch.cuda.synchronize()
+    got = soa.cpu().numpy()
+    assert np.array_equal(got[:nbytes], oracle.aos_to_soa(p.w_aos, n, k))
+    assert np.all(got[nbytes:] == 0xA5)  # nothing written past the end
+
+
+# ---------------------------------------------------------------------------
+# M = 1 decode GEMV
+
+
+def test_gemv_gate_up_full(tq2):
+    p = tq2_synth.decode_gate_up()
+    w = upload(tq2, p)
+    x = torch.from_numpy(p.x[0]).cuda()
+    out = torch.full((p.n,), float("nan"), device="cuda")
+    tq2.tq2_gemv(w, x, None, out, p.n, p.k)
+    torch.cuda.synchronize()
+    check(out.cpu().numpy(), p, TOL_F32, what="gemv gate/up")
+
+
+def test_gemv_down_residual_full(tq2):
+    p = tq2_synth.decode_down()
+    w = upload(tq2, p)
+    x = torch.from_numpy(p.x[0]).cuda()
+    r = torch.from_numpy(p.residual[0]).cuda()
+    out = torch.full((p.n,), float("nan"), device="cuda")
+    tq2.tq2_gemv(w, x, r, out, p.n, p.k)
+    torch.cuda.synchronize()
+    check(out.cpu().numpy(), p, TOL_F32, what="gemv down+res")
+    # in place: residual and out are the same buffer
+    tq2.tq2_gemv(w, x, r, r, p.n, p.k)
+    torch.cuda.synchronize()
+    check(r.cpu().numpy(), p, TOL_F32, what="gemv in-place")
+
+
+@pytest.mark.parametrize("n,k", [(1, 128), (129, 128), (7, 1152), (300, 3072), (33, 20480),
+                                 (5, 65536)])
+def test_gemv_edge_shapes(tq2, n, k):
+    p = tq2_synth.make_problem(1, n, k, seed=n * 7 + k, residual=(n % 2 == 1))
+    w = upload(tq2, p)
+    check(run(tq2, tq2.TQ2_KERNEL_GEMV, w, p), p, TOL_F32, what=f"gemv n={n} k={k}")
+
+
+# ---------------------------------------------------------------------------
+# all kernels on the small configuration and on ragged shapes
+
+KERNELS = ["TQ2_KERNEL_TC", "TQ2_KERNEL_F32REF", "TQ2_KERNEL_SKINNY"]
+
+
+@pytest.mark.parametrize("kname", KERNELS)
+@pytest.mark.parametrize("residual", [False, True])
+def test_small_config_each_kernel(tq2, kname, residual):
+    p = tq2_synth.make_problem(8, 1024, 1024, seed=0, residual=residual)
+    w = upload(tq2, p)
+    kernel = getattr(tq2, kname)
+    check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), cos=kernel == tq2.TQ2_KERNEL_TC,
+          what=kname)
+
+
+@pytest.mark.parametrize("m,n,k", [(1, 1, 128), (2, 129, 256), (3, 7, 128), (17, 257, 384),
+                                   (129, 300, 640), (130, 255, 128), (5, 1000, 1024),
+                                   (256, 512, 256), (200, 33, 1280)])
+@pytest.mark.parametrize("kname", KERNELS + ["TQ2_KERNEL_AUTO"])
+def test_ragged_shapes(tq2, m, n, k, kname):
+    kernel = getattr(tq2, kname)
+    if kernel == tq2.TQ2_KERNEL_SKINNY and m > 16:
+        pytest.skip("small-M kernel is limited to M <= 16")
+    p = tq2_synth.make_problem(m, n, k, seed=m * 1000 + n + k, residual=(m + n) % 2 == 0,
+                               outlier_frac=0.01)
+    w = upload(tq2, p)
+    eff = tq2.tq2_select_kernel(m, n, k) if kernel == tq2.TQ2_KERNEL_AUTO else kernel
+    out = run(tq2, kernel, w, p)
+    check(out, p, tol_for(tq2, eff), cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16),
+          what=f"{kname} {m}x{n}x{k}")
+
+
+@pytest.mark.parametrize("kname", KERNELS)
+def test_inplace_residual(tq2, kname):
+    kernel = getattr(tq2, kname)
+    p = tq2_synth.make_problem(9, 300, 512, seed=5, residual=True)
+    w = upload(tq2, p)
+    check(run(tq2, kernel, w, p, inplace=True), p, tol_for(tq2, kernel), what=f"{kname} in-place")
+
+
+def test_code3_decodes_to_plus_two_everywhere(tq2):
+    # code 3 is never generated; every kernel still decodes it as c - 1 = +2
+    m, n, k = 4, 64, 256
+    p = tq2_synth.make_problem(m, n, k, seed=3)
+    p.w_aos[:, :, :32] = 0xFF
+    w = upload(tq2, p)
+    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_F32REF, tq2.TQ2_KERNEL_SKINNY):
+        check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), what=f"code3 {kernel}")
+    p1 = tq2_synth.make_problem(1, n, k, seed=3)
+    p1.w_aos[:] = p.w_aos
+    check(run(tq2, tq2.TQ2_KERNEL_GEMV, w, p1), p1, TOL_F32, what="code3 gemv")
+
+
+def test_zero_weights_give_residual(tq2):
+    m, n, k = 130, 260, 384
+    p = tq2_synth.make_problem(m, n, k, seed=9, residual=True)
+    p.w_aos[:, :, :32] = 0x55
+    w = upload(tq2, p)
+    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_F32REF):
+        out = run(tq2, kernel, w, p)
+        assert np.array_equal(out, p.residual), kernel
+
+
+def test_empty_problems_are_noops(tq2):
+    w = torch.zeros(34, dtype=torch.uint8, device="cuda")
+    x = torch.zeros(128, device="cuda")
+    out = torch.full((4,), 7.0, device="cuda")
+    for kernel in (0, 1, 2, 3, 4):
+        tq2.tq2_gemm_with(kernel, w, x, None, out, 0, 1, 128)
+        tq2.tq2_gemm_with(kernel, w, x, None, out, 1, 0, 128)
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+
+
+# ---------------------------------------------------------------------------
+# the benchmark configurations
+
+
+@pytest.mark.parametrize("m", tq2_synth.SKINNY_MS)
+def test_skinny_sweep_auto(tq2, m):
+    p = tq2_synth.skinny(m)
+    w = upload(tq2, p)
+    kernel = tq2.tq2_select_kernel(m, p.n, p.k)
+    out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
+    check(out, p, tol_for(tq2, kernel), cos=kernel == tq2.TQ2_KERNEL_TC, what=f"skinny m={m}")
+
+
+@pytest.mark.parametrize("m", [7, 8, 9, 16])
+def test_skinny_sweep_tc(tq2, m):
+    p = tq2_synth.skinny(m)
+    w = upload(tq2, p)
+    check(run(tq2, tq2.TQ2_KERNEL_TC, w, p), p, TOL_TC, cos=True, what=f"tc m={m}")
+
+
+@pytest.mark.parametrize("n", tq2_synth.DIT_NS)
+def test_dit_large_m_tc(tq2, n):
+    p = tq2_synth.dit(n)
+    w = upload(tq2, p)
+    out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
+    assert tq2.tq2_select_kernel(p.m, p.n, p.k) == tq2.TQ2_KERNEL_TC
+    check(out, p, TOL_TC, rows=sample_rows(p.m), cos=True, what=f"dit n={n}")
+
+
+def test_dit_large_m_f32ref(tq2):
+    p = tq2_synth.dit(3072)
+    w = upload(tq2, p)
+    check(run(tq2, tq2.TQ2_KERNEL_F32REF, w, p), p, TOL_F32, rows=sample_rows(p.m, extra=6),
+          what="f32ref dit")
+
+
+@pytest.mark.parametrize("layer", [0, 1, 40, 41, 60, 61, 80, 81])
+def test_dit_forward_layers(tq2, layer):
+    p = tq2_synth.dit_forward_layer(layer)
+    w = upload(tq2, p)
+    out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
+    check(out, p, TOL_TC, rows=sample_rows(p.m, extra=4, seed=layer), cos=True,
+          what=f"dit forward layer {layer}")
+
+
+# ---------------------------------------------------------------------------
+# bounded device waits
+
+
+def test_wait_timeout_is_reported_and_context_survives(tq2):
+    p = tq2_synth.make_problem(128, 256, 2048, seed=1)
+    w = upload(tq2, p)
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    old = tq2.tq2_set_wait_timeout_ns(0)
+    try:
+        run(tq2, tq2.TQ2_KERNEL_TC, w, p)
+        st = tq2.tq2_device_status()
+    finally:
+        tq2.tq2_set_wait_timeout_ns(old)
+    assert st == tq2.TQ2_ERR_TIMEOUT
+    assert tq2.tq2_device_status() == tq2.TQ2_OK  # cleared by the read
+    check(run(tq2, tq2.TQ2_KERNEL_TC, w, p), p, TOL_TC, cos=True, what="after timeout")
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
