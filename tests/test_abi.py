@@ -12,8 +12,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def tq2():
-    from dit_tq2_g128_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     import dit_tq2_g128_gb300 as m
     return m
 
