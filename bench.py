@@ -328,29 +328,42 @@ def run_ours(args, world, rank, local, pg):
             xl = [torch.from_numpy(q.x).to(device) for _ in range(c)]
             ol = [torch.empty((q.m, q.n), dtype=torch.float32, device=device) for _ in range(c)]
 
+            wsl = [tq2.workspace(q.m, q.n, q.k, device=device) for _ in range(c)]
+
             def gstep(i, q=q, wl=wl, xl=xl, ol=ol, c=c):
                 tq2.tq2_gemm(wl[i % c], xl[i % c], None, ol[i % c], q.m, q.n, q.k)
 
-            for i in range(3):
-                gstep(i)
-            torch.cuda.synchronize()
-            assert tq2.tq2_device_status() == tq2.TQ2_OK
-            gg = graph_of(gstep, args.gemm_steps, torch)
-            gg.replay()
-            torch.cuda.synchronize()
-            tg = time_graph(gg, torch, pg, device, reps=3) / args.gemm_steps
-            launches += args.gemm_steps
+            def gstep_ws(i, q=q, wl=wl, xl=xl, ol=ol, c=c, wsl=wsl):
+                tq2.tq2_gemm_ws(wl[i % c], xl[i % c], None, ol[i % c], q.m, q.n, q.k, wsl[i % c],
+                                wsl[i % c].numel())
+
             flops = 2.0 * q.m * q.n * q.k
-            tfl = flops / tg / 1e12
-            gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "us_per_call": round(tg * 1e6, 2),
+            res = {}
+            for name, fn in (("tq2_gemm", gstep), ("tq2_gemm_ws", gstep_ws)):
+                for i in range(3):
+                    fn(i)
+                torch.cuda.synchronize()
+                assert tq2.tq2_device_status() == tq2.TQ2_OK
+                gg = graph_of(fn, args.gemm_steps, torch)
+                gg.replay()
+                torch.cuda.synchronize()
+                tg = time_graph(gg, torch, pg, device, reps=3) / args.gemm_steps
+                launches += args.gemm_steps * (1 if name == "tq2_gemm" else 2)
+                res[name] = (tg, flops / tg / 1e12)
+            tg, tfl = res["tq2_gemm_ws"]
+            gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "entry": "tq2_gemm_ws",
+                             "us_per_call": round(tg * 1e6, 2),
                              "tflops": round(tfl, 1), "frac_of_bf16_burst": round(tfl / bf16, 4),
                              "frac_of_bf16_sustained": round(tfl / bf16s, 4),
+                             "tq2_gemm_no_workspace": {"us_per_call": round(res["tq2_gemm"][0] * 1e6, 2),
+                                                       "tflops": round(res["tq2_gemm"][1], 1)},
                              "l2": f"{c} rotating (x, w, out) copies"}
-            del wl, xl, ol, wq
+            del wl, xl, ol, wq, wsl
             torch.cuda.empty_cache()
         top = gemm[f"n{max(int(k[1:]) for k in gemm)}"]
         line["gemm_m1536"] = {
-            "kernel": "tq2_gemm -> tcgen05 kind::f16 (f16 operands, f32 accumulation in TMEM)",
+            "kernel": "tq2_gemm_ws -> x f16-tile pre-pass + persistent tcgen05 kind::f16 kernel "
+                      "(f16 operands, f32 accumulation in TMEM); tq2_gemm (in-kernel conversion) alongside",
             "per_n": gemm,
             "roofline": {"bound": "tensor", "unit": "TFLOP/s",
                          "achieved": top["tflops"], "peak": bf16,

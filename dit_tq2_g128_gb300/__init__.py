@@ -40,7 +40,7 @@ KERNEL_NAMES = {0: "auto", 1: "gemv", 2: "skinny", 3: "tc", 4: "f32ref"}
 EXPORTS = (
     "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
-    "tq2_device_status", "tq2_version",
+    "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
 )
 
 
@@ -79,6 +79,10 @@ def _load():
     L.tq2_device_status.argtypes = [vp]
     L.tq2_version.restype = i32
     L.tq2_version.argtypes = []
+    L.tq2_gemm_workspace_bytes.restype = ctypes.c_size_t
+    L.tq2_gemm_workspace_bytes.argtypes = [i64, i64, i64]
+    L.tq2_gemm_ws.restype = i32
+    L.tq2_gemm_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
     return L
 
 
@@ -160,6 +164,16 @@ def tq2_gemm_f32ref(w_soa, x, residual, out, m: int, n: int, k: int, stream=None
                                _stream(stream)), "tq2_gemm_f32ref")
 
 
+def tq2_gemm_workspace_bytes(m: int, n: int, k: int) -> int:
+    return int(lib.tq2_gemm_workspace_bytes(m, n, k))
+
+
+def tq2_gemm_ws(w_soa, x, residual, out, m: int, n: int, k: int, workspace, workspace_bytes: int,
+                stream=None) -> None:
+    _check(lib.tq2_gemm_ws(_ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), m, n, k,
+                           _ptr(workspace), int(workspace_bytes), _stream(stream)), "tq2_gemm_ws")
+
+
 def tq2_gemm_with(kernel: int, w_soa, x, residual, out, m: int, n: int, k: int,
                   stream=None) -> None:
     _check(lib.tq2_gemm_with(int(kernel), _ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), m, n,
@@ -199,9 +213,18 @@ def upload_weight(w_aos_host, n: int, k: int, stream=None):
     return soa
 
 
+def workspace(m: int, n: int, k: int, device="cuda"):
+    """A device workspace for tq2_gemm_ws (torch uint8 tensor; None if not needed)."""
+    import torch
+    nbytes = tq2_gemm_workspace_bytes(m, n, k)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device) if nbytes else None
+
+
 def matmul(w_soa, x, residual=None, *, n: int, k: int, out=None, kernel: int = TQ2_KERNEL_AUTO,
-           stream=None):
-    """out[M, N] = x[M, K] . dequant(W)^T (+ residual) on torch CUDA tensors."""
+           workspace=None, stream=None):
+    """out[M, N] = x[M, K] . dequant(W)^T (+ residual) on torch CUDA tensors.
+
+    With ``workspace`` (see ``workspace()``) and kernel AUTO, runs tq2_gemm_ws."""
     import torch
     m = x.numel() // k if k else 0
     _check_tensor(w_soa, "w_soa", "torch.uint8", tq2_soa_bytes(n, k))
@@ -211,5 +234,8 @@ def matmul(w_soa, x, residual=None, *, n: int, k: int, out=None, kernel: int = T
     if out is None:
         out = torch.empty((m, n), dtype=torch.float32, device=x.device)
     _check_tensor(out, "out", "torch.float32", m * n)
-    tq2_gemm_with(kernel, w_soa, x, residual, out, m, n, k, stream)
+    if workspace is not None and kernel == TQ2_KERNEL_AUTO:
+        tq2_gemm_ws(w_soa, x, residual, out, m, n, k, workspace, workspace.numel(), stream)
+    else:
+        tq2_gemm_with(kernel, w_soa, x, residual, out, m, n, k, stream)
     return out

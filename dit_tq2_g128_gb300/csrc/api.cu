@@ -65,10 +65,9 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     return na && nb && x < y + nb && y < x + na;
 }
 
-// Shape checks shared by every matmul entry point.  Returns TQ2_OK and sets
-// *noop when there is nothing to compute.
-int check_matmul(const void *w, const float *x, const float *residual, const float *out,
-                 int64_t m, int64_t n, int64_t k, bool *noop) {
+// Shape-only checks.  Returns TQ2_OK and sets *noop when there is nothing
+// to compute.
+int check_shape(int64_t m, int64_t n, int64_t k, bool *noop) {
     *noop = false;
     if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
     if (m < 0 || n < 0) return TQ2_ERR_INVALID_ARG;
@@ -76,10 +75,15 @@ int check_matmul(const void *w, const float *x, const float *residual, const flo
     if (k > lim || m > lim || n > lim || (m && k > lim / m) || (n && k > lim / n) ||
         (m && n > lim / m))
         return TQ2_ERR_INVALID_ARG;
-    if (m == 0 || n == 0) {
-        *noop = true;
-        return TQ2_OK;
-    }
+    if (m == 0 || n == 0) *noop = true;
+    return TQ2_OK;
+}
+
+// Shape and pointer checks shared by every matmul entry point.
+int check_matmul(const void *w, const float *x, const float *residual, const float *out,
+                 int64_t m, int64_t n, int64_t k, bool *noop) {
+    int st = check_shape(m, n, k, noop);
+    if (st != TQ2_OK || *noop) return st;
     if (!w || !x || !out) return TQ2_ERR_INVALID_ARG;
     if (!aligned16(w) || !aligned16(x) || !aligned16(out) || (residual && !aligned16(residual)))
         return TQ2_ERR_MISALIGNED;
@@ -183,6 +187,34 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
         case TQ2_KERNEL_TC: return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
         default: return finish(tq2::launch_f32ref(w_soa, x, residual, out, m, n, k, ctx));
     }
+}
+
+size_t tq2_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
+    bool noop = false;
+    if (check_shape(m, n, k, &noop) != TQ2_OK || noop) return 0;
+    if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC) return 0;
+    return tq2::tc_ws_bytes(m, k);
+}
+
+int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,
+                int64_t n, int64_t k, void *workspace, size_t workspace_bytes, void *stream) {
+    bool noop = false;
+    int st = check_matmul(w_soa, x, residual, out, m, n, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC)
+        return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
+    const size_t need = tq2::tc_ws_bytes(m, k);
+    if (!workspace || workspace_bytes < need) return TQ2_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 127u) != 0) return TQ2_ERR_MISALIGNED;
+    const size_t wb = size_t(n) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
+    const size_t xb = size_t(m) * size_t(k) * 4, ob = size_t(m) * size_t(n) * 4;
+    if (overlaps(workspace, need, x, xb) || overlaps(workspace, need, w_soa, wb) ||
+        overlaps(workspace, need, out, ob) || (residual && overlaps(workspace, need, residual, ob)))
+        return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, workspace, ctx));
 }
 
 int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,

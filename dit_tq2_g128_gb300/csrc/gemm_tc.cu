@@ -204,19 +204,16 @@ tc_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
                 }
             }
         };
-        ProdRegs nxt;
-        if (KT > 0) load(0, nxt);
-        for (int it = 0; it < KT; ++it) {
-            const ProdRegs cur = nxt;
-            if (it + 1 < KT) load(it + 1, nxt);
+        // Returns false when the pipeline was aborted.
+        auto produce = [&](int it, const ProdRegs &cur) -> bool {
             const int s = it % STAGES;
             if (it >= STAGES) {
                 if (!mbar_wait_bounded(&ctl->empty[s], ((it / STAGES) - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
-                    break;
+                    return false;
                 }
             }
-            if (*abort_flag) break;
+            if (*abort_flag) return false;
             const uint32_t a_base = smem_base + s * STAGE_BYTES;
             const uint32_t b_base = a_base + A_BYTES;
             // activations: f32 -> f16 (RNE), pairs (i, i+8)
@@ -242,6 +239,19 @@ tc_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
             }
             fence_proxy_async_smem();
             mbar_arrive(&ctl->full[s]);
+            return true;
+        };
+        // Two register stages in flight: the loads of stage it+2 are issued as
+        // soon as stage it has been written.
+        ProdRegs ra, rb;
+        if (KT > 0) load(0, ra);
+        if (KT > 1) load(1, rb);
+        for (int it = 0; it < KT; it += 2) {
+            if (!produce(it, ra)) break;
+            if (it + 2 < KT) load(it + 2, ra);
+            if (it + 1 >= KT) break;
+            if (!produce(it + 1, rb)) break;
+            if (it + 3 < KT) load(it + 3, rb);
         }
     } else if (warp == MMA_WARP) {
         // ---------------- MMA issuer ----------------

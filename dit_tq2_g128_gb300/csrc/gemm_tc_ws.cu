@@ -1,0 +1,521 @@
+// Large-M tensor-core kernel, workspace variant: the activations are
+// converted once to binary16 tiles in a caller-provided workspace, then the
+// persistent tcgen05 kernel streams them with bulk copies.
+//
+// Same contraction as the in-kernel-conversion kernel (the role of the
+// pages' `gemm_tq2_g128_v10_simdgroup`: weights dequantised into shared
+// memory as half, f16 operands, f32 accumulation, staging overlapped with the
+// matrix units; "oxibonsai-kernels 0.1.5 src/gpu_backend/metal_graph/
+// pipelines.rs").  What changes on sm_103a:
+//
+//  * Pre-pass: x f32 [M,K] -> f16 tiles of 128 rows x 64 k (16 KB each), laid
+//    out exactly as the MMA's K-major SWIZZLE_128B shared-memory image, with
+//    the K permutation that matches the weight decode (pairs (i, i+8) of every
+//    16-wide group).  Rows past M are zero.  One tile then moves with a single
+//    cp.async.bulk; the activation path costs the SM no load instructions.
+//  * Weight codes: a 2-D TMA load of the qs plane (256 rows x 16 bytes per
+//    stage) into shared memory; 8 decoder warps read their row's 16 bytes,
+//    decode to f16 (c - 1) * d and write the B tile.  The scales come with
+//    one 16-byte load per 8 blocks per row.
+//  * Persistent CTAs (one per SM) walk the 128 x 256 output tiles; the f32
+//    accumulator is double-buffered in TMEM (2 x 256 columns), so the
+//    epilogue of one tile overlaps the main loop of the next.
+//  * Roles: warp 0 issues the bulk/TMA copies, warp 1 the MMAs (and owns
+//    TMEM), warps 4-7 run the epilogue (TMEM lanes 0-127), warps 8-15 decode.
+//  * All mbarrier waits are bounded; on a timeout the roles stop, the issued
+//    copies and MMAs drain, and TMEM is freed before exit.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <climits>
+#include <mutex>
+
+#include "tq2_internal.cuh"
+
+namespace tq2 {
+namespace {
+
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, CSTAGES = 8;
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB (one pre-converted tile)
+constexpr int B_BYTES = BN * BK * 2;     // 32 KB
+constexpr int C_BYTES = BN * BK / 4;     // 4 KB of raw codes
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int NUM_THREADS = 512;
+// warp 0: code TMA issuer, warp 1: MMA issuer + TMEM owner, warp 2: A-tile
+// issuer, warps 4-7: epilogue, warps 8-15: decoders
+constexpr int TMA_WARP = 0, MMA_WARP = 1, A_WARP = 2, EPI_WARP0 = 4, DEC_WARP0 = 8;
+constexpr int NUM_DEC = 256;             // one weight row per decoder thread
+constexpr int NUM_EPI = 128;
+constexpr uint32_t TMEM_COLS = 512;      // two 128 x 256 f32 accumulators
+constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+
+struct Ctl {
+    uint64_t full_a[STAGES];
+    uint64_t full_b[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t codes_full[CSTAGES];
+    uint64_t codes_empty[CSTAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+constexpr size_t SMEM_BYTES =
+    size_t(STAGES) * STAGE_BYTES + size_t(CSTAGES) * C_BYTES + sizeof(Ctl) + 1024;
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+__device__ __forceinline__ uint32_t sw128_off(int r, int j) {
+    return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ uint32_t h2u(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 u2h(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                       uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                             uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+// Decode one 16-weight code word into 8 half2 (weights (i, i+8)), each (c-1)*d.
+__device__ __forceinline__ void decode_word(uint32_t w, __half2 d2, uint32_t (&o)[8]) {
+    const uint32_t w6 = w >> 6;
+    const uint32_t base = 0x64006400u;
+    const uint32_t v0 = (w & 0x00030003u) | base;
+    const uint32_t v1 = (w & 0x000C000Cu) | base;
+    const uint32_t v2 = (w & 0x00300030u) | base;
+    const uint32_t v3 = (w & 0x00C000C0u) | base;
+    const uint32_t v4 = (w & 0x03000300u) | base;
+    const uint32_t v5 = (w6 & 0x00300030u) | base;
+    const uint32_t v6 = (w6 & 0x00C000C0u) | base;
+    const uint32_t v7 = (w6 & 0x03000300u) | base;
+    const __half2 s0 = __float2half2_rn(1.0f), b0 = __float2half2_rn(-1025.0f);
+    const __half2 s2 = __float2half2_rn(0.25f), b2 = __float2half2_rn(-257.0f);
+    const __half2 s4 = __float2half2_rn(0.0625f), b4 = __float2half2_rn(-65.0f);
+    const __half2 s6 = __float2half2_rn(0.015625f), b6 = __float2half2_rn(-17.0f);
+    const __half2 s8 = __float2half2_rn(0.00390625f), b8 = __float2half2_rn(-5.0f);
+    o[0] = h2u(__hmul2(__hfma2(u2h(v0), s0, b0), d2));
+    o[1] = h2u(__hmul2(__hfma2(u2h(v1), s2, b2), d2));
+    o[2] = h2u(__hmul2(__hfma2(u2h(v2), s4, b4), d2));
+    o[3] = h2u(__hmul2(__hfma2(u2h(v3), s6, b6), d2));
+    o[4] = h2u(__hmul2(__hfma2(u2h(v4), s8, b8), d2));
+    o[5] = h2u(__hmul2(__hfma2(u2h(v5), s4, b4), d2));
+    o[6] = h2u(__hmul2(__hfma2(u2h(v6), s6, b6), d2));
+    o[7] = h2u(__hmul2(__hfma2(u2h(v7), s8, b8), d2));
+}
+
+// --------------------------------------------------------------------------
+// Pre-pass: x f32 [M,K] -> f16 MMA tiles.  Item = (row, 16-float group).
+
+__global__ void __launch_bounds__(256)
+x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, int K, int MT) {
+    const int groups = K / 16;                 // 16-float groups per row
+    const int KT = K / BK;
+    const int64_t items = int64_t(MT) * BM * groups;
+    for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
+         it += int64_t(gridDim.x) * blockDim.x) {
+        const int row = int(it / groups), g = int(it % groups);
+        float f[16];
+        if (row < M) {
+            const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(row) * K + 16 * g);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = __ldg(src + q);
+                f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = 0.f;
+        }
+        const int mt = row / BM, r = row % BM, kt = g / 4, q = g % 4;
+        uint8_t *tile = ws + (int64_t(mt) * KT + kt) * A_BYTES;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint4 v;
+            v.x = h2u(__floats2half2_rn(f[4 * h + 0], f[8 + 4 * h + 0]));
+            v.y = h2u(__floats2half2_rn(f[4 * h + 1], f[8 + 4 * h + 1]));
+            v.z = h2u(__floats2half2_rn(f[4 * h + 2], f[8 + 4 * h + 2]));
+            v.w = h2u(__floats2half2_rn(f[4 * h + 3], f[8 + 4 * h + 3]));
+            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 2 * q + h)) = v;
+        }
+    }
+}
+
+// --------------------------------------------------------------------------
+// Main kernel.
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict__ dpl,
+             const uint8_t *__restrict__ xtiles, const float *residual, float *out, int M, int N,
+             int K, unsigned int *status, uint64_t wait_ns) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw_addr = smem_u32(smem_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    const uint32_t sbase = raw_addr + pad;
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * STAGE_BYTES +
+                                       size_t(CSTAGES) * C_BYTES);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int KT = K / BK;
+    const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
+    const int ntiles = MT * NT;
+    const int64_t kb = K / kBlockW;
+
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&ctl->full_a[s], 1);
+            mbar_init(&ctl->full_b[s], NUM_DEC);
+            mbar_init(&ctl->empty[s], 1);
+        }
+        for (int s = 0; s < CSTAGES; ++s) {
+            mbar_init(&ctl->codes_full[s], 1);
+            mbar_init(&ctl->codes_empty[s], NUM_DEC);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->tmem_full[b], 1);
+            mbar_init(&ctl->tmem_empty[b], NUM_EPI);
+        }
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        fence_mbarrier_init();
+    }
+    if (warp == MMA_WARP) {
+        tmem_alloc(&ctl->tmem_base, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort;
+
+    auto stage_a = [&](int s) { return sbase + uint32_t(s) * STAGE_BYTES; };
+    auto stage_b = [&](int s) { return sbase + uint32_t(s) * STAGE_BYTES + A_BYTES; };
+    auto stage_c = [&](int s) {
+        return sbase + uint32_t(STAGES) * STAGE_BYTES + uint32_t(s) * C_BYTES;
+    };
+
+    if (warp == TMA_WARP || warp == A_WARP) {
+        // Two independent copy streams: weight codes into their own deep ring
+        // (warp 0), pre-converted activation tiles into the A/B ring (warp 2).
+        const bool codes = warp == TMA_WARP;
+        const int depth = codes ? CSTAGES : STAGES;
+        if (lane == 0) {
+            if (codes)
+                asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+            int64_t g = 0;
+            int last_round[CSTAGES];
+            for (int s = 0; s < CSTAGES; ++s) last_round[s] = -1;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
+                const int mt = t % MT, nt = t / MT;
+                const uint8_t *atile = xtiles + int64_t(mt) * KT * A_BYTES;
+                for (int kt = 0; kt < KT; ++kt, ++g) {
+                    const int s = int(g % depth);
+                    const int u = int(g / depth);
+                    uint64_t *freed = codes ? &ctl->codes_empty[s] : &ctl->empty[s];
+                    if (u > 0 && !mbar_wait_bounded(freed, (u - 1) & 1, wait_ns, status)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    if (codes) {
+                        mbar_expect_tx(&ctl->codes_full[s], C_BYTES);
+                        tma_2d(stage_c(s), &qmap, kt * (BK / 4), nt * BN, &ctl->codes_full[s]);
+                    } else {
+                        mbar_expect_tx(&ctl->full_a[s], A_BYTES);
+                        bulk_g2s(stage_a(s), atile + int64_t(kt) * A_BYTES, A_BYTES, &ctl->full_a[s]);
+                    }
+                    last_round[s] = u;
+                }
+            }
+            // Drain: every copy this thread issued must land before the CTA exits.
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            for (int s = 0; s < depth; ++s) {
+                if (last_round[s] < 0) continue;
+                mbar_wait_bounded(codes ? &ctl->codes_full[s] : &ctl->full_a[s], last_round[s] & 1,
+                                  drain, status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == MMA_WARP) {
+        if (lane == 0) {
+            int64_t g = 0;
+            int i = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+                const int ab = i & 1, ur = i >> 1;
+                if (ur > 0 && !mbar_wait_bounded(&ctl->tmem_empty[ab], (ur - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t dt = tmem + uint32_t(ab * BN);
+                for (int kt = 0; kt < KT; ++kt, ++g) {
+                    const int s = int(g % STAGES);
+                    const uint32_t par = uint32_t(g / STAGES) & 1;
+                    if (!mbar_wait_bounded(&ctl->full_a[s], par, wait_ns, status) ||
+                        !mbar_wait_bounded(&ctl->full_b[s], par, wait_ns, status)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    if (*abort_flag) { ok = false; break; }
+                    tc_fence_after();
+                    const uint64_t adesc = sw128_desc(stage_a(s));
+                    const uint64_t bdesc = sw128_desc(stage_b(s));
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk)
+                        tc_mma_f16(dt, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kt | kk) != 0);
+                    tc_commit(&ctl->empty[s]);
+                }
+                if (ok) tc_commit(&ctl->tmem_full[ab]);
+            }
+        }
+        __syncwarp();
+    } else if (warp >= DEC_WARP0) {
+        const int pt = tid - DEC_WARP0 * 32;
+        int64_t g = 0;
+        const bool dvec = (kb % 8) == 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+            const int nt = t / MT;
+            const int row = nt * BN + pt;
+            const bool rvalid = row < N;
+            const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
+            // scales: 8 blocks (16 stages) per 16-byte load, one group ahead
+            uint4 dv = make_uint4(0, 0, 0, 0), dv_next = make_uint4(0, 0, 0, 0);
+            if (dvec && rvalid) dv_next = __ldg(reinterpret_cast<const uint4 *>(drow));
+            uint32_t dscalar = 0;
+            bool stop = false;
+            for (int kt = 0; kt < KT; ++kt, ++g) {
+                const int cs = int(g % CSTAGES);
+                const int s = int(g % STAGES);
+                const int blk = kt >> 1;
+                if (dvec) {
+                    if ((kt & 15) == 0) {
+                        dv = dv_next;
+                        if (rvalid && blk + 8 < kb)
+                            dv_next = __ldg(reinterpret_cast<const uint4 *>(drow + blk + 8));
+                    }
+                } else if ((kt & 1) == 0 && rvalid) {
+                    dscalar = ldg_u16(drow + blk);
+                }
+                if (!mbar_wait_bounded(&ctl->codes_full[cs], uint32_t(g / CSTAGES) & 1, wait_ns,
+                                       status)) {
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                const uint4 code = ld_shared_v4(stage_c(cs) + uint32_t(pt) * 16);
+                mbar_arrive(&ctl->codes_empty[cs]);
+                // the B slot is free once the MMAs of its previous round completed
+                const int u = int(g / STAGES);
+                if (u > 0 && !mbar_wait_bounded(&ctl->empty[s], (u - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    stop = true;
+                    break;
+                }
+                if (*abort_flag) { stop = true; break; }
+                uint32_t dbits;
+                if (dvec) {
+                    const int e = blk & 7;
+                    const uint32_t wv = (e >> 1) == 0 ? dv.x : (e >> 1) == 1 ? dv.y : (e >> 1) == 2 ? dv.z : dv.w;
+                    dbits = (e & 1) ? (wv >> 16) : (wv & 0xFFFFu);
+                } else {
+                    dbits = dscalar;
+                }
+                if (!rvalid) dbits = 0;
+                const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(dbits)));
+                const uint32_t words[4] = {code.x, code.y, code.z, code.w};
+                const uint32_t bb = stage_b(s);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    uint32_t o[8];
+                    decode_word(words[q], d2, o);
+                    st_shared_v4(bb + sw128_off(pt, 2 * q), o[0], o[1], o[2], o[3]);
+                    st_shared_v4(bb + sw128_off(pt, 2 * q + 1), o[4], o[5], o[6], o[7]);
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&ctl->full_b[s]);
+            }
+            if (stop) break;
+        }
+    } else if (warp >= EPI_WARP0) {
+        const int ew = warp - EPI_WARP0;  // TMEM lanes 32*ew .. 32*ew+31
+        int i = 0;
+        const bool vec = (N % 4) == 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int ab = i & 1, ur = i >> 1;
+            const int mt = t % MT, nt = t / MT;
+            if (!mbar_wait_bounded(&ctl->tmem_full[ab], ur & 1, wait_ns, status)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            tc_fence_after();
+            const int row = mt * BM + ew * 32 + lane;
+            const bool rvalid = row < M;
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + (uint32_t(ew * 32) << 16) + uint32_t(ab * BN + c * 32), r);
+                tc_wait_ld();
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(&ctl->tmem_empty[ab]);
+                }
+                const int col0 = nt * BN + c * 32;
+                if (!rvalid || col0 >= N) continue;
+                float *op = out + int64_t(row) * N + col0;
+                const float *rp = residual ? residual + int64_t(row) * N + col0 : nullptr;
+                if (vec && col0 + 32 <= N) {
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
+                                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
+                        if (rp) {
+                            const float4 rr = *reinterpret_cast<const float4 *>(rp + 4 * q);
+                            v.x += rr.x; v.y += rr.y; v.z += rr.z; v.w += rr.w;
+                        }
+                        *reinterpret_cast<float4 *>(op + 4 * q) = v;
+                    }
+                } else {
+                    for (int j = 0; j < 32 && col0 + j < N; ++j) {
+                        float v = __uint_as_float(r[j]);
+                        if (rp) v += rp[j];
+                        op[j] = v;
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == MMA_WARP) {
+        if (lane == 0) {
+            // Every issued MMA must be complete before TMEM is released: one
+            // more commit arrives once all of them have finished.
+            tc_commit(&ctl->drain);
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            mbar_wait_bounded(&ctl->drain, 0, drain, status);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+}  // namespace
+
+size_t tc_ws_bytes(int64_t m, int64_t k) {
+    const int64_t mt = (m + BM - 1) / BM;
+    return size_t(mt) * BM * size_t(k) * 2;
+}
+
+cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
+                         int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx) {
+    if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return cudaErrorInvalidValue;
+    const SoaView v = soa_view(w_soa, n, k);
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap qmap;
+    const cuuint64_t gdim[2] = {cuuint64_t(k / 4), cuuint64_t(n)};
+    const cuuint64_t gstride[1] = {cuuint64_t(k / 4)};
+    const cuuint32_t box[2] = {BK / 4, BN};
+    const cuuint32_t estride[2] = {1, 1};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(v.qs), gdim, gstride, box,
+            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    // pre-pass
+    const int MT = int((m + BM - 1) / BM);
+    const int64_t items = int64_t(MT) * BM * (k / 16);
+    const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
+    x_to_tiles_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(x, static_cast<uint8_t *>(ws), int(m),
+                                                               int(k), MT);
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(tc_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(SMEM_BYTES));
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = int64_t(MT) * ((n + BN - 1) / BN);
+    const int64_t grid = std::min<int64_t>(ntiles, ctx.num_sms);
+    tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
+        qmap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
+        ctx.status, ctx.wait_ns);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace tq2

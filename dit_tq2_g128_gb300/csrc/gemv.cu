@@ -228,11 +228,226 @@ cudaError_t launch_tpl(const void *w_soa, const float *x, const float *residual,
     return cudaPeekAtLastError();
 }
 
+
+// ---------------------------------------------------------------------------
+// M = 1 decode GEMV.
+//
+// Lane l of a warp owns 64 consecutive weights (one 16-byte code load, half
+// a block) of a 2048-weight chunk; a CTA holds C chunk-warps per row stream
+// (C = ceil(K / 2048)) and S = max(1, 8 / C) row streams.  Rows are split
+// into contiguous, near-equal ranges over all streams of the grid.  Per
+// batch of kP rows a warp issues all code and scale loads before decoding
+// (the next batch's loads are issued before the current batch is decoded),
+// so that a large part of the weight is in flight from the start.  x is
+// copied once per CTA into shared memory, pre-scaled per code position, in
+// 64-float segments padded to 68 floats (conflict-free 16-byte reads, zeros
+// past K).  The inner loop is branch-free: rows past a stream's range and
+// lanes past K read clamped, valid addresses and contribute zero.  The kP
+// row partials are reduced across the warp with one halving butterfly; the
+// per-(row, chunk) partials meet in shared memory.
+constexpr int kP = 4;           // rows per load batch
+constexpr int kGvChunk = 2048;  // weights per warp-chunk (32 lanes x 64)
+constexpr int kSeg = 68;        // padded floats per 64-weight segment
+
+// (w & MASK) | magic in one LOP3, the magic constant in a register.
+template <uint32_t MASK>
+__device__ __forceinline__ float mag(uint32_t w, uint32_t magic) {
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(MASK), "r"(magic));
+    return __uint_as_float(r);
+}
+
+// Loop-invariant constants kept in registers (pinned through an opaque move
+// so the compiler does not rematerialise them at every use).
+struct GvConst {
+    uint32_t magic;
+    float2 nb[8];  // -(2^23 + 4^pos) for positions (2p, 2p+1)
+};
+
+__device__ __forceinline__ float pin(float v) {
+    float r;
+    asm volatile("mov.b32 %0, %1;" : "=f"(r) : "f"(v));
+    return r;
+}
+
+__device__ __forceinline__ void gv_const_init(GvConst &c) {
+    uint32_t m;
+    asm volatile("mov.b32 %0, 0x4B000000;" : "=r"(m));
+    c.magic = m;
+#pragma unroll
+    for (int p = 0; p < 8; ++p) c.nb[p] = make_float2(pin(-pos_bias(2 * p)), pin(-pos_bias(2 * p + 1)));
+}
+
+// acc += sum_i (c_i - 1) * x_i over one 16-weight code word; xs pre-scaled.
+__device__ __forceinline__ float2 dot16c(uint32_t w, const float4 (&xs)[4], const GvConst &k,
+                                         float2 acc) {
+    const uint32_t w2 = w >> 22;
+    const uint32_t mg = k.magic;
+    float2 t;
+#define TQ2_STEP(P, A, B, XA, XB)                                              \
+    t = __fadd2_rn(make_float2(A, B), k.nb[P]);                                \
+    acc = __ffma2_rn(t, make_float2(XA, XB), acc);
+    TQ2_STEP(0, mag<0x3u>(w, mg), mag<0xCu>(w, mg), xs[0].x, xs[0].y)
+    TQ2_STEP(1, mag<0x30u>(w, mg), mag<0xC0u>(w, mg), xs[0].z, xs[0].w)
+    TQ2_STEP(2, mag<0x300u>(w, mg), mag<0xC00u>(w, mg), xs[1].x, xs[1].y)
+    TQ2_STEP(3, mag<0x3000u>(w, mg), mag<0xC000u>(w, mg), xs[1].z, xs[1].w)
+    TQ2_STEP(4, mag<0x30000u>(w, mg), mag<0xC0000u>(w, mg), xs[2].x, xs[2].y)
+    TQ2_STEP(5, mag<0x300000u>(w, mg), mag<0x3u>(w2, mg), xs[2].z, xs[2].w)
+    TQ2_STEP(6, mag<0xCu>(w2, mg), mag<0x30u>(w2, mg), xs[3].x, xs[3].y)
+    TQ2_STEP(7, mag<0xC0u>(w2, mg), mag<0x300u>(w2, mg), xs[3].z, xs[3].w)
+#undef TQ2_STEP
+    return acc;
+}
+
+struct GvBatch {
+    uint4 w[kP];
+    unsigned short d[kP];
+};
+
+__global__ void __launch_bounds__(768, 1)
+gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
+            const float *__restrict__ x, const float *residual, float *out, int n, int k, int C,
+            int S) {
+    extern __shared__ float4 gv_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = warp % C, s = warp / C;
+    // contiguous row range of this CTA, then of this stream inside it
+    const int R0 = int(int64_t(n) * blockIdx.x / gridDim.x);
+    const int R1 = int(int64_t(n) * (blockIdx.x + 1) / gridDim.x);
+    const int ra = R0 + (R1 - R0) * s / S, rb = R0 + (R1 - R0) * (s + 1) / S;
+    const int kw0 = c * kGvChunk + lane * 64;
+    const bool active = kw0 < k;
+    const int64_t kq = k / 4, kb = k / kBlockW;
+    const int nseg = C * 32;                       // 64-weight segments incl. padding past K
+    float *xsm = reinterpret_cast<float *>(gv_smem);
+    float *partial = xsm + nseg * kSeg;            // [R1 - R0][C]
+
+    const int kw_ld = active ? kw0 : 0;           // inactive lanes read a valid address
+    const uint8_t *qbase = qs + kw_ld / 4;
+    const __half *dbase = dpl + kw_ld / kBlockW;
+    // Loads of a batch of kP rows from row r; rows at or past rb re-read row rb-1.
+    auto load = [&](int r, GvBatch &b) {
+        const uint8_t *q = qbase + int64_t(r) * kq;
+        const __half *dd = dbase + int64_t(r) * kb;
+        if (r + kP <= rb) {
+#pragma unroll
+            for (int u = 0; u < kP; ++u) {
+                b.w[u] = ldg_stream_u4(q + u * kq);
+                b.d[u] = ldg_u16(dd + u * kb);
+            }
+        } else {
+            const int last = rb - 1 - r;
+#pragma unroll
+            for (int u = 0; u < kP; ++u) {
+                const int uu = u < last ? u : last;
+                b.w[u] = ldg_stream_u4(q + uu * kq);
+                b.d[u] = ldg_u16(dd + uu * kb);
+            }
+        }
+    };
+    GvBatch bA, bB;
+    const bool has_rows = ra < rb;
+    if (has_rows) load(ra, bA);
+
+    // x -> shared memory, pre-scaled per code position, zero past K.
+    for (int i = threadIdx.x; i < nseg * 16; i += blockDim.x) {
+        const int seg = i >> 4, q = i & 15;
+        const int kk = seg * 64 + 4 * q;
+        float4 v = kk < k ? __ldg(reinterpret_cast<const float4 *>(x + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        v.x *= pos_scale((4 * q + 0) & 15);
+        v.y *= pos_scale((4 * q + 1) & 15);
+        v.z *= pos_scale((4 * q + 2) & 15);
+        v.w *= pos_scale((4 * q + 3) & 15);
+        *reinterpret_cast<float4 *>(xsm + seg * kSeg + 4 * q) = v;
+    }
+    GvConst kc;
+    gv_const_init(kc);
+    __syncthreads();
+
+    const float4 *xl = reinterpret_cast<const float4 *>(xsm + (c * 32 + lane) * kSeg);
+    // Decode and reduce one batch; rows r.. (nv of them valid) of this stream.
+    auto compute = [&](const GvBatch &b, int r) {
+        const int nv = min(kP, rb - r);
+        float2 acc[kP];
+#pragma unroll
+        for (int u = 0; u < kP; ++u) acc[u] = make_float2(0.f, 0.f);
+        if (nv == kP) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 xs[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xs[j] = xl[4 * q + j];
+#pragma unroll
+                for (int u = 0; u < kP; ++u) {
+                    const uint32_t wq = q == 0 ? b.w[u].x : q == 1 ? b.w[u].y : q == 2 ? b.w[u].z : b.w[u].w;
+                    acc[u] = dot16c(wq, xs, kc, acc[u]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float4 xs[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) xs[j] = xl[4 * q + j];
+#pragma unroll
+                for (int u = 0; u < kP; ++u) {
+                    if (u < nv) {
+                        const uint32_t wq = q == 0 ? b.w[u].x : q == 1 ? b.w[u].y : q == 2 ? b.w[u].z : b.w[u].w;
+                        acc[u] = dot16c(wq, xs, kc, acc[u]);
+                    }
+                }
+            }
+        }
+        float v[kP];
+#pragma unroll
+        for (int u = 0; u < kP; ++u)
+            v[u] = (acc[u].x + acc[u].y) * (active ? __half2float(__ushort_as_half(b.d[u])) : 0.f);
+        butterfly<kP>(v, lane);
+        constexpr int G = 32 / kP;
+        if (lane % G == 0) {
+            const int u = lane / G;
+            if (u < nv) partial[(r + u - R0) * C + c] = v[0];
+        }
+    };
+    if (has_rows) {
+        for (int r = ra; r < rb; r += 2 * kP) {
+            if (r + kP < rb) load(r + kP, bB);
+            compute(bA, r);
+            if (r + kP >= rb) break;
+            if (r + 2 * kP < rb) load(r + 2 * kP, bA);
+            compute(bB, r + kP);
+        }
+    }
+    __syncthreads();
+    for (int i = R0 + threadIdx.x; i < R1; i += blockDim.x) {
+        float sum = 0.f;
+        for (int cc = 0; cc < C; ++cc) sum += partial[(i - R0) * C + cc];
+        if (residual) sum += residual[i];
+        out[i] = sum;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
                         int64_t n, int64_t k, const LaunchCtx &ctx) {
-    return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
+    const int64_t C = (k + kGvChunk - 1) / kGvChunk;
+    if (C > 16 || n > INT32_MAX)  // K > 32768: the chunk-looping small-M kernel
+        return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
+    // One CTA per SM, up to 18 warps: C chunk-warps per row stream, S streams.
+    const int S = std::max<int>(1, 18 / int(C));
+    const int threads = 32 * int(C) * S;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + kP - 1) / kP));
+    const int64_t rows_cta = (n + grid - 1) / grid;
+    const size_t smem = size_t(C) * 32 * kSeg * 4 + size_t(rows_cta) * size_t(C) * 4;
+    if (smem > 200 * 1024) return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
+    cudaError_t e = cudaFuncSetAttribute(gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(std::max<size_t>(smem, 48 * 1024)));
+    if (e != cudaSuccess) return e;
+    const SoaView v = soa_view(w_soa, n, k);
+    gemv_kernel<<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(
+        v.qs, v.d, x, residual, out, int(n), int(k), int(C), S);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_skinny(const void *w_soa, const float *x, const float *residual, float *out,

@@ -127,6 +127,27 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
 int tq2_gemm_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
                     int64_t m, int64_t n, int64_t k, void *stream);
 
+/* Workspace bytes that tq2_gemm_ws needs for this shape: the binary16 copy of
+ * x, padded to a multiple of 128 rows (ceil(m/128)*128*k*2 bytes) when the
+ * shape selects the tensor-core kernel, else 0.  Host only.  Returns 0 for
+ * invalid shapes. */
+size_t tq2_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
+
+/* tq2_gemm with a caller-owned device workspace (the library still
+ * allocates nothing).  When the shape selects the tensor-core kernel, x is
+ * first converted to binary16 MMA tiles in the workspace by a pre-pass and the
+ * tensor-core kernel streams those tiles with bulk copies instead of
+ * converting x itself; results are those of the tensor-core kernel.  Other
+ * shapes ignore the workspace and behave exactly like tq2_gemm.
+ *   workspace       : device, >= tq2_gemm_workspace_bytes(m,n,k) bytes,
+ *                     128-byte aligned, overlapping no other argument; may be
+ *                     NULL when that size is 0.  Its contents on return are
+ *                     unspecified; the call only reads what it wrote.
+ *   workspace_bytes : its size; a smaller size gives TQ2_ERR_INVALID_ARG.
+ * Two calls that share a workspace must be ordered (same stream). */
+int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,
+                int64_t n, int64_t k, void *workspace, size_t workspace_bytes, void *stream);
+
 /* tq2_gemm with an explicit kernel choice (a tq2_kernel value), for
  * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 (else
  * TQ2_ERR_INVALID_ARG). */

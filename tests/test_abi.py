@@ -102,6 +102,26 @@ def test_argument_errors_are_returned_before_any_launch(tq2):
     assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 9) == tq2.TQ2_ERR_INVALID_ARG
 
 
+def test_workspace_size_and_errors(tq2):
+    # binary16 copy of x padded to 128 rows, only for tensor-core shapes
+    assert tq2.tq2_gemm_workspace_bytes(1536, 3072, 3072) == 1536 * 3072 * 2
+    assert tq2.tq2_gemm_workspace_bytes(130, 64, 256) == 256 * 256 * 2
+    assert tq2.tq2_gemm_workspace_bytes(1, 4096, 4096) == 0
+    assert tq2.tq2_gemm_workspace_bytes(0, 4096, 4096) == 0
+    assert tq2.tq2_gemm_workspace_bytes(64, 64, 100) == 0
+    assert tq2.tq2_gemm_workspace_bytes(4096, 3072, 12288) == 4096 * 12288 * 2
+    A = 1 << 20
+    W, X, O, WS = A, 64 * A, 128 * A, 256 * A
+    need = tq2.tq2_gemm_workspace_bytes(128, 256, 1024)
+    f = tq2.lib.tq2_gemm_ws
+    assert f(W, X, None, O, 128, 256, 1024, None, 0, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, None, O, 128, 256, 1024, WS, need - 1, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, None, O, 128, 256, 1024, WS + 16, need, None) == tq2.TQ2_ERR_MISALIGNED
+    assert f(W, X, None, O, 128, 256, 1024, X, need, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, None, O, 128, 256, 1000, WS, need, None) == tq2.TQ2_ERR_BAD_K
+    assert f(None, None, None, None, 0, 256, 1024, None, 0, None) == tq2.TQ2_OK
+
+
 def test_python_wrapper_raises(tq2):
     with pytest.raises(tq2.TQ2Error) as e:
         tq2.tq2_gemm(1 << 20, 2 << 20, None, 3 << 20, 4, 4, 100)

@@ -256,6 +256,66 @@ def test_dit_forward_layers(tq2, layer):
 
 
 # ---------------------------------------------------------------------------
+# tensor-core kernel fed from the workspace (tq2_gemm_ws)
+
+
+def run_ws(tq2, w, p, *, inplace=False):
+    x = torch.from_numpy(p.x).cuda()
+    r = None if p.residual is None else torch.from_numpy(p.residual).cuda()
+    out = r.clone() if inplace else torch.full((p.m, p.n), float("nan"), device="cuda")
+    if inplace:
+        r = out
+    ws = tq2.workspace(p.m, p.n, p.k)
+    nbytes = 0 if ws is None else ws.numel()
+    tq2.tq2_gemm_ws(w, x, r, out, p.m, p.n, p.k, ws, nbytes)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+@pytest.mark.parametrize("m,n,k", [(8, 1024, 1024), (4, 7, 128), (17, 257, 384), (129, 300, 640),
+                                   (130, 255, 128), (256, 512, 256), (200, 33, 1280),
+                                   (300, 700, 4096), (5, 1000, 1152)])
+@pytest.mark.parametrize("residual", [False, True])
+def test_ws_ragged(tq2, m, n, k, residual):
+    p = tq2_synth.make_problem(m, n, k, seed=m + n + k, residual=residual, outlier_frac=0.01)
+    w = upload(tq2, p)
+    eff = tq2.tq2_select_kernel(m, n, k)
+    check(run_ws(tq2, w, p), p, tol_for(tq2, eff), cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16),
+          what=f"ws {m}x{n}x{k}")
+
+
+def test_ws_inplace_and_repeat(tq2):
+    p = tq2_synth.make_problem(260, 520, 768, seed=7, residual=True)
+    w = upload(tq2, p)
+    a = run_ws(tq2, w, p, inplace=True)
+    check(a, p, TOL_TC, cos=True, what="ws in-place")
+    b = run_ws(tq2, w, p, inplace=True)
+    assert np.array_equal(a, b)  # deterministic
+
+
+@pytest.mark.parametrize("n", tq2_synth.DIT_NS)
+def test_ws_dit_large_m(tq2, n):
+    p = tq2_synth.dit(n)
+    w = upload(tq2, p)
+    check(run_ws(tq2, w, p), p, TOL_TC, rows=sample_rows(p.m), cos=True, what=f"ws dit n={n}")
+
+
+@pytest.mark.parametrize("layer", [0, 41, 60, 81])
+def test_ws_dit_forward_layers(tq2, layer):
+    p = tq2_synth.dit_forward_layer(layer)
+    w = upload(tq2, p)
+    check(run_ws(tq2, w, p), p, TOL_TC, rows=sample_rows(p.m, extra=4, seed=layer), cos=True,
+          what=f"ws dit forward layer {layer}")
+
+
+@pytest.mark.parametrize("m", [7, 8, 9, 16, 64, 100])
+def test_ws_skinny(tq2, m):
+    p = tq2_synth.skinny(m)
+    w = upload(tq2, p)
+    check(run_ws(tq2, w, p), p, TOL_TC, cos=True, what=f"ws skinny m={m}")
+
+
+# ---------------------------------------------------------------------------
 # bounded device waits
 
 
@@ -272,4 +332,19 @@ def test_wait_timeout_is_reported_and_context_survives(tq2):
     assert st == tq2.TQ2_ERR_TIMEOUT
     assert tq2.tq2_device_status() == tq2.TQ2_OK  # cleared by the read
     check(run(tq2, tq2.TQ2_KERNEL_TC, w, p), p, TOL_TC, cos=True, what="after timeout")
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+
+
+def test_wait_timeout_ws_kernel(tq2):
+    p = tq2_synth.make_problem(256, 512, 2048, seed=2)
+    w = upload(tq2, p)
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    old = tq2.tq2_set_wait_timeout_ns(0)
+    try:
+        run_ws(tq2, w, p)
+        st = tq2.tq2_device_status()
+    finally:
+        tq2.tq2_set_wait_timeout_ns(old)
+    assert st == tq2.TQ2_ERR_TIMEOUT
+    check(run_ws(tq2, w, p), p, TOL_TC, cos=True, what="ws after timeout")
     assert tq2.tq2_device_status() == tq2.TQ2_OK
