@@ -36,17 +36,19 @@
 namespace tq2 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, CSTAGES = 8;
+constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, CSTAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB (one pre-converted tile)
 constexpr int B_BYTES = BN * BK * 2;     // 32 KB
 constexpr int C_BYTES = BN * BK / 4;     // 4 KB of raw codes
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 512;
+constexpr int NUM_THREADS = 768;
 // warp 0: code TMA issuer, warp 1: MMA issuer + TMEM owner, warp 2: A-tile
-// issuer, warps 4-7: epilogue, warps 8-15: decoders
+// issuer, warps 4-7: epilogue, warps 8-23: decoders
 constexpr int TMA_WARP = 0, MMA_WARP = 1, A_WARP = 2, EPI_WARP0 = 4, DEC_WARP0 = 8;
-constexpr int NUM_DEC = 256;             // one weight row per decoder thread
+constexpr int NUM_DEC = 512;             // two decoder threads per weight row (32 codes each)
 constexpr int NUM_EPI = 128;
+constexpr int EPI_LD = 33;               // padded row of the epilogue staging buffer (floats)
+constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;  // one 32 x 32 f32 block per epilogue warp
 constexpr uint32_t TMEM_COLS = 512;      // two 128 x 256 f32 accumulators
 constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
 
@@ -63,8 +65,8 @@ struct Ctl {
     int abort;
 };
 
-constexpr size_t SMEM_BYTES =
-    size_t(STAGES) * STAGE_BYTES + size_t(CSTAGES) * C_BYTES + sizeof(Ctl) + 1024;
+constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_BYTES + size_t(CSTAGES) * C_BYTES +
+                              size_t(EPI_BYTES) + sizeof(Ctl) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -209,8 +211,10 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     const uint32_t sbase = raw_addr + pad;
+    float *epi_stage = reinterpret_cast<float *>(smem_raw + pad + size_t(STAGES) * STAGE_BYTES +
+                                                 size_t(CSTAGES) * C_BYTES);
     Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * STAGE_BYTES +
-                                       size_t(CSTAGES) * C_BYTES);
+                                       size_t(CSTAGES) * C_BYTES + EPI_BYTES);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KT = K / BK;
@@ -332,7 +336,9 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
         }
         __syncwarp();
     } else if (warp >= DEC_WARP0) {
-        const int pt = tid - DEC_WARP0 * 32;
+        const int dt = tid - DEC_WARP0 * 32;
+        const int pt = dt & (BN - 1);    // weight row in the tile
+        const int hw = dt >> 8;          // which 32 codes of the row's 64 (words 2hw, 2hw+1)
         int64_t g = 0;
         const bool dvec = (kb % 8) == 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
@@ -364,7 +370,11 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                     stop = true;
                     break;
                 }
-                const uint4 code = ld_shared_v4(stage_c(cs) + uint32_t(pt) * 16);
+                uint2 code;
+                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                             : "=r"(code.x), "=r"(code.y)
+                             : "r"(stage_c(cs) + uint32_t(pt) * 16 + uint32_t(hw) * 8)
+                             : "memory");
                 mbar_arrive(&ctl->codes_empty[cs]);
                 // the B slot is free once the MMAs of its previous round completed
                 const int u = int(g / STAGES);
@@ -384,14 +394,14 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                 }
                 if (!rvalid) dbits = 0;
                 const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(dbits)));
-                const uint32_t words[4] = {code.x, code.y, code.z, code.w};
                 const uint32_t bb = stage_b(s);
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
+                for (int q = 0; q < 2; ++q) {
                     uint32_t o[8];
-                    decode_word(words[q], d2, o);
-                    st_shared_v4(bb + sw128_off(pt, 2 * q), o[0], o[1], o[2], o[3]);
-                    st_shared_v4(bb + sw128_off(pt, 2 * q + 1), o[4], o[5], o[6], o[7]);
+                    decode_word(q == 0 ? code.x : code.y, d2, o);
+                    const int j = 4 * hw + 2 * q;
+                    st_shared_v4(bb + sw128_off(pt, j), o[0], o[1], o[2], o[3]);
+                    st_shared_v4(bb + sw128_off(pt, j + 1), o[4], o[5], o[6], o[7]);
                 }
                 fence_proxy_async_smem();
                 mbar_arrive(&ctl->full_b[s]);
@@ -411,8 +421,10 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
             }
             if (*abort_flag) break;
             tc_fence_after();
-            const int row = mt * BM + ew * 32 + lane;
-            const bool rvalid = row < M;
+            // Each 32 x 32 f32 block: TMEM -> registers (thread = row) -> padded
+            // shared memory -> coalesced rows (8 lanes per 128-byte row segment).
+            float *st = epi_stage + ew * 32 * EPI_LD;
+            const int rsub = lane >> 3, csub = (lane & 7) * 4;
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + (uint32_t(ew * 32) << 16) + uint32_t(ab * BN + c * 32), r);
@@ -421,28 +433,32 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                     tc_fence_before();
                     mbar_arrive(&ctl->tmem_empty[ab]);
                 }
-                const int col0 = nt * BN + c * 32;
-                if (!rvalid || col0 >= N) continue;
-                float *op = out + int64_t(row) * N + col0;
-                const float *rp = residual ? residual + int64_t(row) * N + col0 : nullptr;
-                if (vec && col0 + 32 <= N) {
 #pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        float4 v = make_float4(__uint_as_float(r[4 * q]), __uint_as_float(r[4 * q + 1]),
-                                               __uint_as_float(r[4 * q + 2]), __uint_as_float(r[4 * q + 3]));
-                        if (rp) {
-                            const float4 rr = *reinterpret_cast<const float4 *>(rp + 4 * q);
-                            v.x += rr.x; v.y += rr.y; v.z += rr.z; v.w += rr.w;
+                for (int j = 0; j < 32; ++j) st[lane * EPI_LD + j] = __uint_as_float(r[j]);
+                __syncwarp();
+                const int col = nt * BN + c * 32 + csub;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int rl = 4 * i + rsub;
+                    const int row = mt * BM + ew * 32 + rl;
+                    const float *sp = st + rl * EPI_LD + csub;
+                    float4 v = make_float4(sp[0], sp[1], sp[2], sp[3]);
+                    if (row < M) {
+                        const int64_t o = int64_t(row) * N + col;
+                        if (vec && col + 4 <= N) {
+                            if (residual) {
+                                const float4 rr = *reinterpret_cast<const float4 *>(residual + o);
+                                v.x += rr.x; v.y += rr.y; v.z += rr.z; v.w += rr.w;
+                            }
+                            *reinterpret_cast<float4 *>(out + o) = v;
+                        } else {
+                            const float vv[4] = {v.x, v.y, v.z, v.w};
+                            for (int e = 0; e < 4 && col + e < N; ++e)
+                                out[o + e] = vv[e] + (residual ? residual[o + e] : 0.f);
                         }
-                        *reinterpret_cast<float4 *>(op + 4 * q) = v;
-                    }
-                } else {
-                    for (int j = 0; j < 32 && col0 + j < N; ++j) {
-                        float v = __uint_as_float(r[j]);
-                        if (rp) v += rp[j];
-                        op[j] = v;
                     }
                 }
+                __syncwarp();
             }
         }
     }

@@ -299,12 +299,10 @@ __device__ __forceinline__ float2 dot16c(uint32_t w, const float4 (&xs)[4], cons
     return acc;
 }
 
-struct GvBatch {
-    uint4 w[kP];
-    unsigned short d[kP];
-};
-
-__global__ void __launch_bounds__(768, 1)
+// Up to kR rows of one warp's stream are loaded at once (all of them, for
+// the row counts the launcher picks), then decoded in groups of kP.
+template <int kR, int kMaxThreads>
+__global__ void __launch_bounds__(kMaxThreads, 1)
 gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
             const float *__restrict__ x, const float *residual, float *out, int n, int k, int C,
             int S) {
@@ -325,29 +323,21 @@ gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
     const int kw_ld = active ? kw0 : 0;           // inactive lanes read a valid address
     const uint8_t *qbase = qs + kw_ld / 4;
     const __half *dbase = dpl + kw_ld / kBlockW;
-    // Loads of a batch of kP rows from row r; rows at or past rb re-read row rb-1.
-    auto load = [&](int r, GvBatch &b) {
+    uint4 w[kR];
+    unsigned short dh[kR];
+    // rows r .. r+kR-1; rows at or past rb re-read row rb-1 (never used)
+    auto load = [&](int r) {
         const uint8_t *q = qbase + int64_t(r) * kq;
         const __half *dd = dbase + int64_t(r) * kb;
-        if (r + kP <= rb) {
+        const int last = rb - 1 - r;
 #pragma unroll
-            for (int u = 0; u < kP; ++u) {
-                b.w[u] = ldg_stream_u4(q + u * kq);
-                b.d[u] = ldg_u16(dd + u * kb);
-            }
-        } else {
-            const int last = rb - 1 - r;
-#pragma unroll
-            for (int u = 0; u < kP; ++u) {
-                const int uu = u < last ? u : last;
-                b.w[u] = ldg_stream_u4(q + uu * kq);
-                b.d[u] = ldg_u16(dd + uu * kb);
-            }
+        for (int u = 0; u < kR; ++u) {
+            const int uu = u < last ? u : last;
+            w[u] = ldg_stream_u4(q + uu * kq);
+            dh[u] = ldg_u16(dd + uu * kb);
         }
     };
-    GvBatch bA, bB;
-    const bool has_rows = ra < rb;
-    if (has_rows) load(ra, bA);
+    if (ra < rb) load(ra);
 
     // x -> shared memory, pre-scaled per code position, zero past K.
     for (int i = threadIdx.x; i < nseg * 16; i += blockDim.x) {
@@ -365,25 +355,15 @@ gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
     __syncthreads();
 
     const float4 *xl = reinterpret_cast<const float4 *>(xsm + (c * 32 + lane) * kSeg);
-    // Decode and reduce one batch; rows r.. (nv of them valid) of this stream.
-    auto compute = [&](const GvBatch &b, int r) {
-        const int nv = min(kP, rb - r);
-        float2 acc[kP];
+    for (int r = ra; r < rb; r += kR) {
+        if (r != ra) load(r);
 #pragma unroll
-        for (int u = 0; u < kP; ++u) acc[u] = make_float2(0.f, 0.f);
-        if (nv == kP) {
+        for (int g0 = 0; g0 < kR; g0 += kP) {
+            const int nv = min(kP, rb - (r + g0));  // warp-uniform
+            if (nv <= 0) break;
+            float2 acc[kP];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float4 xs[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) xs[j] = xl[4 * q + j];
-#pragma unroll
-                for (int u = 0; u < kP; ++u) {
-                    const uint32_t wq = q == 0 ? b.w[u].x : q == 1 ? b.w[u].y : q == 2 ? b.w[u].z : b.w[u].w;
-                    acc[u] = dot16c(wq, xs, kc, acc[u]);
-                }
-            }
-        } else {
+            for (int u = 0; u < kP; ++u) acc[u] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 float4 xs[4];
@@ -391,31 +371,22 @@ gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
                 for (int j = 0; j < 4; ++j) xs[j] = xl[4 * q + j];
 #pragma unroll
                 for (int u = 0; u < kP; ++u) {
-                    if (u < nv) {
-                        const uint32_t wq = q == 0 ? b.w[u].x : q == 1 ? b.w[u].y : q == 2 ? b.w[u].z : b.w[u].w;
-                        acc[u] = dot16c(wq, xs, kc, acc[u]);
-                    }
+                    const uint4 &wu = w[g0 + u];
+                    const uint32_t wq = q == 0 ? wu.x : q == 1 ? wu.y : q == 2 ? wu.z : wu.w;
+                    if (u < nv) acc[u] = dot16c(wq, xs, kc, acc[u]);
                 }
             }
-        }
-        float v[kP];
+            float v[kP];
 #pragma unroll
-        for (int u = 0; u < kP; ++u)
-            v[u] = (acc[u].x + acc[u].y) * (active ? __half2float(__ushort_as_half(b.d[u])) : 0.f);
-        butterfly<kP>(v, lane);
-        constexpr int G = 32 / kP;
-        if (lane % G == 0) {
-            const int u = lane / G;
-            if (u < nv) partial[(r + u - R0) * C + c] = v[0];
-        }
-    };
-    if (has_rows) {
-        for (int r = ra; r < rb; r += 2 * kP) {
-            if (r + kP < rb) load(r + kP, bB);
-            compute(bA, r);
-            if (r + kP >= rb) break;
-            if (r + 2 * kP < rb) load(r + 2 * kP, bA);
-            compute(bB, r + kP);
+            for (int u = 0; u < kP; ++u)
+                v[u] = (acc[u].x + acc[u].y) *
+                       (active ? __half2float(__ushort_as_half(dh[g0 + u])) : 0.f);
+            butterfly<kP>(v, lane);
+            constexpr int G = 32 / kP;
+            if (lane % G == 0) {
+                const int u = lane / G;
+                if (u < nv) partial[(r + g0 + u - R0) * C + c] = v[0];
+            }
         }
     }
     __syncthreads();
@@ -434,19 +405,22 @@ cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual
     const int64_t C = (k + kGvChunk - 1) / kGvChunk;
     if (C > 16 || n > INT32_MAX)  // K > 32768: the chunk-looping small-M kernel
         return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
-    // One CTA per SM, up to 18 warps: C chunk-warps per row stream, S streams.
-    const int S = std::max<int>(1, 18 / int(C));
+    // One CTA per SM, up to 16 warps: C chunk-warps per row stream, S streams.
+    const int S = std::max<int>(1, 16 / int(C));
     const int threads = 32 * int(C) * S;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + kP - 1) / kP));
     const int64_t rows_cta = (n + grid - 1) / grid;
     const size_t smem = size_t(C) * 32 * kSeg * 4 + size_t(rows_cta) * size_t(C) * 4;
     if (smem > 200 * 1024) return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
-    cudaError_t e = cudaFuncSetAttribute(gemv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const int64_t rows_stream = (rows_cta + S - 1) / S;
+    // deeper register batches when the CTA is small enough to afford them
+    auto kern = (threads <= 384 && rows_stream > 12) ? gemv_kernel<16, 384> : gemv_kernel<12, 512>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(std::max<size_t>(smem, 48 * 1024)));
     if (e != cudaSuccess) return e;
     const SoaView v = soa_view(w_soa, n, k);
-    gemv_kernel<<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(
-        v.qs, v.d, x, residual, out, int(n), int(k), int(C), S);
+    kern<<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(v.qs, v.d, x, residual, out,
+                                                                     int(n), int(k), int(C), S);
     return cudaPeekAtLastError();
 }
 
