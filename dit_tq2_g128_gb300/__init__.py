@@ -28,6 +28,8 @@ TQ2_ERR_MISALIGNED = 3
 TQ2_ERR_UNSUPPORTED_DEVICE = 4
 TQ2_ERR_CUDA = 5
 TQ2_ERR_TIMEOUT = 6
+TQ2_ERR_TOO_LARGE = 7
+TQ2_NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 TQ2_KERNEL_AUTO = 0
 TQ2_KERNEL_GEMV = 1
@@ -41,6 +43,7 @@ EXPORTS = (
     "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
+    "tq2_gemm_noalloc",
 )
 
 
@@ -83,6 +86,8 @@ def _load():
     L.tq2_gemm_workspace_bytes.argtypes = [i64, i64, i64]
     L.tq2_gemm_ws.restype = i32
     L.tq2_gemm_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
+    L.tq2_gemm_noalloc.restype = i32
+    L.tq2_gemm_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     return L
 
 
@@ -172,6 +177,12 @@ def tq2_gemm_ws(w_soa, x, residual, out, m: int, n: int, k: int, workspace, work
                 stream=None) -> None:
     _check(lib.tq2_gemm_ws(_ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), m, n, k,
                            _ptr(workspace), int(workspace_bytes), _stream(stream)), "tq2_gemm_ws")
+
+
+def tq2_gemm_noalloc(w_soa, x, residual, out, m: int, n: int, k: int, stream=None) -> None:
+    """tq2_gemm without any device allocation (fixed library scratch; see include/tq2.h)."""
+    _check(lib.tq2_gemm_noalloc(_ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), m, n, k,
+                                _stream(stream)), "tq2_gemm_noalloc")
 
 
 def tq2_gemm_with(kernel: int, w_soa, x, residual, out, m: int, n: int, k: int,

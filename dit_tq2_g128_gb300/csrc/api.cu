@@ -128,6 +128,7 @@ const char *tq2_status_string(int status) {
         case TQ2_ERR_UNSUPPORTED_DEVICE: return "TQ2_ERR_UNSUPPORTED_DEVICE: needs compute capability 10.3 (sm_103a)";
         case TQ2_ERR_CUDA: return "TQ2_ERR_CUDA: CUDA launch or runtime error";
         case TQ2_ERR_TIMEOUT: return "TQ2_ERR_TIMEOUT: a bounded device-side wait expired";
+        case TQ2_ERR_TOO_LARGE: return "TQ2_ERR_TOO_LARGE: the shape needs more scratch than tq2_gemm_noalloc has";
         default: return "unknown tq2 status";
     }
 }
@@ -215,6 +216,20 @@ int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float 
     st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, workspace, ctx));
+}
+
+int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
+                     int64_t m, int64_t n, int64_t k, void *stream) {
+    bool noop = false;
+    int st = check_matmul(w_soa, x, residual, out, m, n, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC)  // these kernels use no scratch
+        return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
+    if (tq2::tc_ws_bytes(m, k) > tq2::kNoAllocScratchBytes) return TQ2_ERR_TOO_LARGE;
+    tq2::LaunchCtx ctx;
+    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_tc_noalloc(w_soa, x, residual, out, m, n, k, ctx));
 }
 
 int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,

@@ -493,7 +493,39 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
+std::mutex g_noalloc_mu;
+uint8_t *g_noalloc_ptr[64];  // device address of the scratch array, per device
+
 }  // namespace
+
+// Fixed scratch of the allocation-free entry point (tq2_gemm_noalloc): the
+// binary16 activation tiles live here instead of in a caller workspace.  Being
+// a file-scope device array, it is reserved on every device that loads this
+// library and stays reserved until the process exits.  All calls share it.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
+                              int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx) {
+    if (tc_ws_bytes(m, k) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    uint8_t *scratch = nullptr;
+    {
+        // One-time set-up per device, with that device current: the host-side
+        // name of the array is not a device address, so ask the runtime for it.
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_ptr[dev]) {
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess) return e;
+            g_noalloc_ptr[dev] = static_cast<uint8_t *>(p);
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    return launch_tc_ws(w_soa, x, residual, out, m, n, k, scratch, ctx);
+}
 
 size_t tc_ws_bytes(int64_t m, int64_t k) {
     const int64_t mt = (m + BM - 1) / BM;

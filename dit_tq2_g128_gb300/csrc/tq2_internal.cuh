@@ -51,6 +51,10 @@ cudaError_t launch_tc(const void *w_soa, const float *x, const float *residual, 
 size_t tc_ws_bytes(int64_t m, int64_t k);
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx);
+// Same kernel pair with the library's fixed device scratch (no allocation).
+constexpr size_t kNoAllocScratchBytes = size_t(TQ2_NOALLOC_SCRATCH_BYTES);
+cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
+                              int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
 
 // Largest M the small-M CUDA-core kernel handles.
 constexpr int64_t kSkinnyMaxM = 16;

@@ -67,8 +67,12 @@ typedef enum {
     TQ2_ERR_MISALIGNED = 3,         /* a pointer that must be 16-byte aligned is not */
     TQ2_ERR_UNSUPPORTED_DEVICE = 4, /* current device is not sm_103 */
     TQ2_ERR_CUDA = 5,               /* launch or runtime error */
-    TQ2_ERR_TIMEOUT = 6             /* a bounded device-side wait expired (see tq2_device_status) */
+    TQ2_ERR_TIMEOUT = 6,            /* a bounded device-side wait expired (see tq2_device_status) */
+    TQ2_ERR_TOO_LARGE = 7           /* tq2_gemm_noalloc: the shape needs more than its fixed scratch */
 } tq2_status;
+
+/* Size of the fixed device scratch behind tq2_gemm_noalloc (32 MiB). */
+#define TQ2_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
 /* Kernel choice for tq2_gemm_with().  TQ2_KERNEL_AUTO is what tq2_gemm uses. */
 typedef enum {
@@ -147,6 +151,34 @@ size_t tq2_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
  * Two calls that share a workspace must be ordered (same stream). */
 int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,
                 int64_t n, int64_t k, void *workspace, size_t workspace_bytes, void *stream);
+
+/* tq2_gemm for callers that cannot allocate device memory.  (No counterpart
+ * on the pages; this is an addition of this library.)
+ *
+ * Some callers may not call cudaMalloc or any allocating routine at all: a
+ * host application that owns every byte of device memory and gives its
+ * plugins no allocator, a real-time loop that must never allocate after
+ * start-up, or code that runs where an allocation could fail or block.
+ * tq2_gemm_ws needs such a caller to provide a workspace; this entry point
+ * needs none.  For shapes that select the tensor-core kernel it converts x
+ * into a fixed scratch array that is part of the library's device image
+ * (TQ2_NOALLOC_SCRATCH_BYTES, reserved on every device that loads the library
+ * until the process exits) and then runs the same kernel as tq2_gemm_ws, with
+ * the same results.  Other shapes use no scratch and behave like tq2_gemm.
+ *   - Limit: shapes with ceil(m/128)*128*k*2 > TQ2_NOALLOC_SCRATCH_BYTES
+ *     return TQ2_ERR_TOO_LARGE before any work (e.g. m = 4096 with k up to
+ *     4096 fits; k = 12288 does not).
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - The first call on a device looks up the scratch array's device address
+ *     (one-time set-up, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the one scratch array, which keeps the last call's
+ *     contents (each call writes all of the scratch it reads, so nothing needs
+ *     clearing).  Calls whose GPU work overlaps in time race on it: issue them
+ *     on one stream or otherwise order them.
+ * Arguments, layouts and other errors as tq2_gemm. */
+int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
+                     int64_t m, int64_t n, int64_t k, void *stream);
 
 /* tq2_gemm with an explicit kernel choice (a tq2_kernel value), for
  * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 (else

@@ -44,7 +44,7 @@ def test_soa_bytes(tq2):
 
 
 def test_status_strings(tq2):
-    for s in range(7):
+    for s in range(8):
         assert tq2.status_string(s).startswith("TQ2_")
     assert "unknown" in tq2.status_string(99)
 
