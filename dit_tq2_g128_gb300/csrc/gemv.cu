@@ -229,199 +229,357 @@ cudaError_t launch_tpl(const void *w_soa, const float *x, const float *residual,
 }
 
 
-// ---------------------------------------------------------------------------
-// M = 1 decode GEMV.
-//
-// Lane l of a warp owns 64 consecutive weights (one 16-byte code load, half
-// a block) of a 2048-weight chunk; a CTA holds C chunk-warps per row stream
-// (C = ceil(K / 2048)) and S = max(1, 8 / C) row streams.  Rows are split
-// into contiguous, near-equal ranges over all streams of the grid.  Per
-// batch of kP rows a warp issues all code and scale loads before decoding
-// (the next batch's loads are issued before the current batch is decoded),
-// so that a large part of the weight is in flight from the start.  x is
-// copied once per CTA into shared memory, pre-scaled per code position, in
-// 64-float segments padded to 68 floats (conflict-free 16-byte reads, zeros
-// past K).  The inner loop is branch-free: rows past a stream's range and
-// lanes past K read clamped, valid addresses and contribute zero.  The kP
-// row partials are reduced across the warp with one halving butterfly; the
-// per-(row, chunk) partials meet in shared memory.
-constexpr int kP = 4;           // rows per load batch
 constexpr int kGvChunk = 2048;  // weights per warp-chunk (32 lanes x 64)
-constexpr int kSeg = 68;        // padded floats per 64-weight segment
 
-// (w & MASK) | magic in one LOP3, the magic constant in a register.
-template <uint32_t MASK>
-__device__ __forceinline__ float mag(uint32_t w, uint32_t magic) {
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(w), "n"(MASK), "r"(magic));
-    return __uint_as_float(r);
+// ---------------------------------------------------------------------------
+// M = 1 decode GEMV (K <= 16384): bulk-copy streaming + integer dot products.
+//
+// Memory side.  One CTA per SM owns a contiguous row range, i.e. a contiguous
+// range of the qs plane.  One producer thread streams it into a shared-memory
+// ring with cp.async.bulk (four rows per stage, completion counted on an
+// mbarrier), so the bytes in flight do not depend on per-thread load slots.
+//
+// Arithmetic.  x is quantised once per CTA, per 64-weight segment, to a signed
+// fixed-point integer X = rint(x * 2^22 / s) with s = max |x| of the segment
+// (|X| <= 2^22), held as three 8-bit limbs (top limb signed).  For one 32-bit
+// code word (16 weights, code i at bits 2i), (w >> 2t) & 0x03030303 gathers
+// the codes of weights t, t+4, t+8, t+12 into four bytes, and dp4a multiplies
+// them with the matching limb bytes and accumulates exactly in int32.  Per row
+// and segment, sum_i (c_i - 1) X_i = sum c*X - sum X is exact; one conversion
+// to f32 and one multiply by s * 2^-22 * d finish the segment.  Per weight this
+// is 3/4 dp4a + 7/16 shift/logic operations instead of the 2 operations of an
+// exact-f32 decode.  The only error is the quantisation of x: per element at
+// most 2^-22 * s (s the segment's max |x|: half a step of 2^-22 * s plus the
+// rounding of the reciprocal); all sums are exact until the final f32 sum over
+// segments.
+// Consumer warps take (row, 2048-weight chunk) items round-robin: each lane
+// owns one 64-weight segment of the chunk, reads its 16 code bytes from the
+// ring and its segment's limbs from shared memory, and the row's 32 lane
+// partials are reduced with shuffles.  Per-(row, chunk) partials meet in
+// shared memory and are summed per row at the end (plus the residual).
+
+constexpr int kSegWords = 52;  // 48 limb words per segment, padded (conflict-free 16-byte reads)
+
+__device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint32_t bytes,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
 }
 
-// Loop-invariant constants kept in registers (pinned through an opaque move
-// so the compiler does not rematerialise them at every use).
-struct GvConst {
-    uint32_t magic;
-    float2 nb[8];  // -(2^23 + 4^pos) for positions (2p, 2p+1)
+__device__ __forceinline__ void mbar_expect_tx_gv(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ int dp4a_uu(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.u32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+struct GvsParams {
+    int n, k, C;       // rows, K, 2048-weight chunks per row
+    int rbase, rextra; // CTA b owns rbase (+1 if b < rextra) rows starting at b*rbase + min(b, rextra)
+    // shared-memory offsets (bytes), computed on the host
+    uint32_t off_x, off_limbs, off_scale, off_sum, off_d, off_partial, off_bar;
+    int rs;            // rows per stage
+    int ns;            // ring slots
+    int consumers;     // consumer warps = groups * C
+    int groups;        // consumer warp groups; group g owns the ring slots s with s % groups == g
+    int rows_cta;      // max rows of a CTA (partial buffer size)
 };
 
-__device__ __forceinline__ float pin(float v) {
-    float r;
-    asm volatile("mov.b32 %0, %1;" : "=f"(r) : "f"(v));
-    return r;
-}
-
-__device__ __forceinline__ void gv_const_init(GvConst &c) {
-    uint32_t m;
-    asm volatile("mov.b32 %0, 0x4B000000;" : "=r"(m));
-    c.magic = m;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) c.nb[p] = make_float2(pin(-pos_bias(2 * p)), pin(-pos_bias(2 * p + 1)));
-}
-
-// acc += sum_i (c_i - 1) * x_i over one 16-weight code word; xs pre-scaled.
-__device__ __forceinline__ float2 dot16c(uint32_t w, const float4 (&xs)[4], const GvConst &k,
-                                         float2 acc) {
-    const uint32_t w2 = w >> 22;
-    const uint32_t mg = k.magic;
-    float2 t;
-#define TQ2_STEP(P, A, B, XA, XB)                                              \
-    t = __fadd2_rn(make_float2(A, B), k.nb[P]);                                \
-    acc = __ffma2_rn(t, make_float2(XA, XB), acc);
-    TQ2_STEP(0, mag<0x3u>(w, mg), mag<0xCu>(w, mg), xs[0].x, xs[0].y)
-    TQ2_STEP(1, mag<0x30u>(w, mg), mag<0xC0u>(w, mg), xs[0].z, xs[0].w)
-    TQ2_STEP(2, mag<0x300u>(w, mg), mag<0xC00u>(w, mg), xs[1].x, xs[1].y)
-    TQ2_STEP(3, mag<0x3000u>(w, mg), mag<0xC000u>(w, mg), xs[1].z, xs[1].w)
-    TQ2_STEP(4, mag<0x30000u>(w, mg), mag<0xC0000u>(w, mg), xs[2].x, xs[2].y)
-    TQ2_STEP(5, mag<0x300000u>(w, mg), mag<0x3u>(w2, mg), xs[2].z, xs[2].w)
-    TQ2_STEP(6, mag<0xCu>(w2, mg), mag<0x30u>(w2, mg), xs[3].x, xs[3].y)
-    TQ2_STEP(7, mag<0xC0u>(w2, mg), mag<0x300u>(w2, mg), xs[3].z, xs[3].w)
-#undef TQ2_STEP
-    return acc;
-}
-
-// Up to kR rows of one warp's stream are loaded at once (all of them, for
-// the row counts the launcher picks), then decoded in groups of kP.
-template <int kR, int kMaxThreads>
-__global__ void __launch_bounds__(kMaxThreads, 1)
-gemv_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
-            const float *__restrict__ x, const float *residual, float *out, int n, int k, int C,
-            int S) {
-    extern __shared__ float4 gv_smem[];
+template <int RS>  // rows per stage
+__global__ void __launch_bounds__(1024, 1)
+gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
+                   const float *__restrict__ x, const float *residual, float *out, GvsParams P,
+                   unsigned int *status, uint64_t wait_ns) {
+    extern __shared__ __align__(128) uint8_t gvs_smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int c = warp % C, s = warp / C;
-    // contiguous row range of this CTA, then of this stream inside it
-    const int R0 = int(int64_t(n) * blockIdx.x / gridDim.x);
-    const int R1 = int(int64_t(n) * (blockIdx.x + 1) / gridDim.x);
-    const int ra = R0 + (R1 - R0) * s / S, rb = R0 + (R1 - R0) * (s + 1) / S;
-    const int kw0 = c * kGvChunk + lane * 64;
-    const bool active = kw0 < k;
+    const int k = P.k, C = P.C;
     const int64_t kq = k / 4, kb = k / kBlockW;
-    const int nseg = C * 32;                       // 64-weight segments incl. padding past K
-    float *xsm = reinterpret_cast<float *>(gv_smem);
-    float *partial = xsm + nseg * kSeg;            // [R1 - R0][C]
+    const int nseg = C * 32;                 // 64-weight segments incl. padding past K
+    const int consumers = P.consumers;       // warp `consumers` is the producer
+    const int b = int(blockIdx.x);
+    const int R0 = b * P.rbase + min(b, P.rextra);
+    const int rows = P.rbase + (b < P.rextra ? 1 : 0);
+    const int nstages = (rows + P.rs - 1) / P.rs;
+    const uint32_t stage_bytes = uint32_t(P.rs * kq);
 
-    const int kw_ld = active ? kw0 : 0;           // inactive lanes read a valid address
-    const uint8_t *qbase = qs + kw_ld / 4;
-    const __half *dbase = dpl + kw_ld / kBlockW;
-    uint4 w[kR];
-    unsigned short dh[kR];
-    // rows r .. r+kR-1; rows at or past rb re-read row rb-1 (never used)
-    auto load = [&](int r) {
-        const uint8_t *q = qbase + int64_t(r) * kq;
-        const __half *dd = dbase + int64_t(r) * kb;
-        const int last = rb - 1 - r;
-#pragma unroll
-        for (int u = 0; u < kR; ++u) {
-            const int uu = u < last ? u : last;
-            w[u] = ldg_stream_u4(q + uu * kq);
-            dh[u] = ldg_u16(dd + uu * kb);
+    // shared memory: [ring][raw x][limbs][seg scale][seg sum X][d rows][partials][barriers]
+    uint8_t *ring = gvs_smem;
+    uint32_t *limbs = reinterpret_cast<uint32_t *>(gvs_smem + P.off_limbs);
+    float *sscale = reinterpret_cast<float *>(gvs_smem + P.off_scale);
+    int *ssum = reinterpret_cast<int *>(gvs_smem + P.off_sum);
+    __half *dsm = reinterpret_cast<__half *>(gvs_smem + P.off_d);
+    float *partial = reinterpret_cast<float *>(gvs_smem + P.off_partial);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gvs_smem + P.off_bar);
+    uint64_t *empty = full + P.ns + 2;  // full[P.ns]: the x copy, full[P.ns + 1]: the scale copy
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + P.ns);
+    const uint32_t ring_addr = smem_u32(ring);
+    float *xraw = reinterpret_cast<float *>(gvs_smem + P.off_x);
+
+    // barriers: the lanes of warp 0 initialise them in parallel
+    if (warp == 0) {
+        for (int i = lane; i < P.ns; i += 32) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 32 * C);
         }
-    };
-    if (ra < rb) load(ra);
-
-    // x -> shared memory, pre-scaled per code position, zero past K.
-    for (int i = threadIdx.x; i < nseg * 16; i += blockDim.x) {
-        const int seg = i >> 4, q = i & 15;
-        const int kk = seg * 64 + 4 * q;
-        float4 v = kk < k ? __ldg(reinterpret_cast<const float4 *>(x + kk)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        v.x *= pos_scale((4 * q + 0) & 15);
-        v.y *= pos_scale((4 * q + 1) & 15);
-        v.z *= pos_scale((4 * q + 2) & 15);
-        v.w *= pos_scale((4 * q + 3) & 15);
-        *reinterpret_cast<float4 *>(xsm + seg * kSeg + 4 * q) = v;
+        if (lane == 0) {
+            mbar_init(&full[P.ns], 1);
+            mbar_init(&full[P.ns + 1], 1);
+            *abort_flag = 0;
+        }
+        fence_proxy_async_smem();   // the inits are visible to the copy engine
     }
-    GvConst kc;
-    gv_const_init(kc);
+    __syncthreads();
+    const bool dbulk = (kb % 8) == 0;
+    if (threadIdx.x == 0) {
+        const uint32_t xbytes = uint32_t(k) * 4;
+        const uint32_t dbytes = (dbulk && rows > 0) ? uint32_t(int64_t(rows) * kb * 2) : 0u;
+        mbar_expect_tx_gv(&full[P.ns], xbytes);
+        bulk_g2s_gv(smem_u32(xraw), x, xbytes, &full[P.ns]);
+        if (dbytes) {
+            mbar_expect_tx_gv(&full[P.ns + 1], dbytes);
+            bulk_g2s_gv(smem_u32(dsm), dpl + int64_t(R0) * kb, dbytes, &full[P.ns + 1]);
+        }
+    }
+    // ---- producer warp, part 1: the first ring-full of stages needs no slot to
+    // free up; its 32 lanes issue those copies in parallel
+    const bool producer = warp == consumers && lane == 0;
+    const uint8_t *src = qs + int64_t(R0) * kq;
+    auto issue = [&](int st) {
+        const int slot = st % P.ns;
+        const int r = min(P.rs, rows - st * P.rs);
+        const uint32_t bytes = uint32_t(r * kq);
+        mbar_expect_tx_gv(&full[slot], bytes);
+        bulk_g2s_gv(ring_addr + uint32_t(slot) * stage_bytes, src + int64_t(st) * stage_bytes, bytes,
+                    &full[slot]);
+    };
+    const int first = min(nstages, P.ns);
+    if (warp == consumers)
+        for (int st = lane; st < first; st += 32) issue(st);
+    // ---- everyone: quantise x per 64-weight segment.  Thread (segment, word q,
+    // group t) owns the four weights 16q + 4m + t (m = 0..3) of its segment --
+    // exactly the bytes of its three limb words -- so it writes whole words.
+    // (Rolled loops throughout: this code runs once per launch, so a small
+    // instruction footprint matters more than unrolling.)
+    if (!mbar_wait_bounded(&full[P.ns], 0, wait_ns, status)) *abort_flag = 1;
+    const int nthr = nseg * 16;  // 16 threads per segment; blockDim.x is a multiple of 16
+#pragma unroll 1
+    for (int i0 = 0; i0 < nthr; i0 += blockDim.x) {
+        const int i = i0 + threadIdx.x;
+        const int seg = i >> 4, q = (i >> 2) & 3, t = i & 3;
+        float xe[4];
+        float m = 0.f;
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int kk = seg * 64 + 16 * q + 4 * mm + t;
+            xe[mm] = (i < nthr && kk < k) ? xraw[kk] : 0.f;
+            m = fmaxf(m, fabsf(xe[mm]));
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float inv = m > 0.f ? 4194304.0f / m : 0.f;  // 2^22 / s, correctly rounded
+        // |X| <= 2^22 (the rounded reciprocal may overshoot by half an ulp)
+        uint32_t l0 = 0, l1 = 0, l2 = 0;
+        int sx = 0;
+#pragma unroll
+        for (int mm = 0; mm < 4; ++mm) {
+            const int X = max(-4194304, min(4194304, __float2int_rn(xe[mm] * inv)));
+            sx += X;
+            l0 |= uint32_t(X & 0xFF) << (8 * mm);
+            l1 |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
+            l2 |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
+        }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+        if (i < nthr) {
+            uint32_t *lw = limbs + seg * kSegWords + (q * 4 + t) * 3;
+            lw[0] = l0;
+            lw[1] = l1;
+            lw[2] = l2;
+            if ((i & 15) == 0) {
+                sscale[seg] = m * (1.0f / 4194304.0f);  // s * 2^-22
+                ssum[seg] = sx;
+            }
+        }
+    }
+    if (!dbulk) {
+        const unsigned short *dsrc = reinterpret_cast<const unsigned short *>(dpl + int64_t(R0) * kb);
+        unsigned short *ddst = reinterpret_cast<unsigned short *>(dsm);
+        for (int64_t i = threadIdx.x; i < int64_t(rows) * kb; i += blockDim.x) ddst[i] = dsrc[i];
+    }
     __syncthreads();
 
-    const float4 *xl = reinterpret_cast<const float4 *>(xsm + (c * 32 + lane) * kSeg);
-    for (int r = ra; r < rb; r += kR) {
-        if (r != ra) load(r);
+    if (producer) {
+        // ---- producer, part 2: refill slots as the consumers release them
+        for (int st = P.ns; st < nstages; ++st) {
+            const int slot = st % P.ns, u = st / P.ns;
+            if (!mbar_wait_bounded(&empty[slot], (u - 1) & 1, wait_ns, status)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            issue(st);
+        }
+        // every copy issued must land before the CTA exits: the last round of each slot
+        const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+        for (int st = max(0, nstages - P.ns); st < nstages; ++st)
+            mbar_wait_bounded(&full[st % P.ns], (st / P.ns) & 1, drain, status);
+    }
+    if (warp < consumers) {
+        // Warp w takes chunk w % C of the stages st = g, g + groups, ... (g = w / C).
+        // The ring size is a multiple of `groups`, so every slot is only ever
+        // touched by one group, in stage order: no warp can wait on a slot's
+        // next round before the group released the current one.
+        const int g = warp / C, c = warp % C;
+        if (dbulk && rows > 0 && !mbar_wait_bounded(&full[P.ns + 1], 0, wait_ns, status))
+            *abort_flag = 1;
+        const int seg = c * 32 + lane;
+        const int kw0 = seg * 64;
+        const bool active = kw0 < k;
+        const int kw_rd = active ? kw0 : 0;
+        for (int st = g; st < nstages; st += P.groups) {
+            const int slot = st % P.ns, u = st / P.ns;
+            if (!mbar_wait_bounded(&full[slot], u & 1, wait_ns, status)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            const int r0 = st * P.rs;                 // first row (CTA-relative) of the stage
+            const int nv = min(P.rs, rows - r0);      // warp-uniform, >= 1
+            const uint8_t *base = ring + size_t(slot) * stage_bytes + kw_rd / 4;
+            // codes are read straight from the ring, word by word
+            const uint8_t *rowp[RS];
 #pragma unroll
-        for (int g0 = 0; g0 < kR; g0 += kP) {
-            const int nv = min(kP, rb - (r + g0));  // warp-uniform
-            if (nv <= 0) break;
-            float2 acc[kP];
+            for (int uu = 0; uu < RS; ++uu) rowp[uu] = base + size_t(uu < nv ? uu : nv - 1) * kq;
+            int a0[RS], a1[RS], a2[RS];
 #pragma unroll
-            for (int u = 0; u < kP; ++u) acc[u] = make_float2(0.f, 0.f);
-#pragma unroll
+            for (int uu = 0; uu < RS; ++uu) a0[uu] = a1[uu] = a2[uu] = 0;
+            const uint4 *lw = reinterpret_cast<const uint4 *>(limbs + seg * kSegWords);
+#pragma unroll 1
             for (int q = 0; q < 4; ++q) {
-                float4 xs[4];
+                // limb words (q, t, l) for t = 0..3, l = 0..2: 12 words
+                const uint4 L0 = lw[3 * q + 0], L1 = lw[3 * q + 1], L2 = lw[3 * q + 2];
+                const uint32_t lv[12] = {L0.x, L0.y, L0.z, L0.w, L1.x, L1.y, L1.z, L1.w,
+                                         L2.x, L2.y, L2.z, L2.w};
 #pragma unroll
-                for (int j = 0; j < 4; ++j) xs[j] = xl[4 * q + j];
+                for (int uu = 0; uu < RS; ++uu) {
+                    const uint32_t wq = *reinterpret_cast<const uint32_t *>(rowp[uu] + 4 * q);
 #pragma unroll
-                for (int u = 0; u < kP; ++u) {
-                    const uint4 &wu = w[g0 + u];
-                    const uint32_t wq = q == 0 ? wu.x : q == 1 ? wu.y : q == 2 ? wu.z : wu.w;
-                    if (u < nv) acc[u] = dot16c(wq, xs, kc, acc[u]);
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t v = (wq >> (2 * t)) & 0x03030303u;
+                        a0[uu] = dp4a_uu(v, lv[3 * t + 0], a0[uu]);
+                        a1[uu] = dp4a_uu(v, lv[3 * t + 1], a1[uu]);
+                        a2[uu] = dp4a_us(v, lv[3 * t + 2], a2[uu]);
+                    }
                 }
             }
-            float v[kP];
+            // every lane has read its codes: release this chunk's share of the slot
+            mbar_arrive(&empty[slot]);
+            const float sc = active ? sscale[seg] : 0.f;
+            const int sx = active ? ssum[seg] : 0;
+            float v[RS];
 #pragma unroll
-            for (int u = 0; u < kP; ++u)
-                v[u] = (acc[u].x + acc[u].y) *
-                       (active ? __half2float(__ushort_as_half(dh[g0 + u])) : 0.f);
-            butterfly<kP>(v, lane);
-            constexpr int G = 32 / kP;
+            for (int uu = 0; uu < RS; ++uu) {
+                const int ur = uu < nv ? uu : nv - 1;
+                const int tot = a2[uu] * 65536 + a1[uu] * 256 + a0[uu] - sx;
+                const float d = __half2float(dsm[int64_t(r0 + ur) * kb + kw_rd / kBlockW]);
+                v[uu] = float(tot) * (sc * d);
+            }
+            butterfly<RS>(v, lane);
+            constexpr int G = 32 / RS;
             if (lane % G == 0) {
-                const int u = lane / G;
-                if (u < nv) partial[(r + g0 + u - R0) * C + c] = v[0];
+                const int uu = lane / G;
+                if (uu < nv) partial[(r0 + uu) * C + c] = v[0];
             }
         }
     }
     __syncthreads();
-    for (int i = R0 + threadIdx.x; i < R1; i += blockDim.x) {
+    if (*abort_flag) return;
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
         float sum = 0.f;
-        for (int cc = 0; cc < C; ++cc) sum += partial[(i - R0) * C + cc];
-        if (residual) sum += residual[i];
-        out[i] = sum;
+        for (int cc = 0; cc < C; ++cc) sum += partial[i * C + cc];
+        if (residual) sum += residual[R0 + i];
+        out[R0 + i] = sum;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
-                        int64_t n, int64_t k, const LaunchCtx &ctx) {
-    const int64_t C = (k + kGvChunk - 1) / kGvChunk;
-    if (C > 16 || n > INT32_MAX)  // K > 32768: the chunk-looping small-M kernel
-        return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
-    // One CTA per SM, up to 16 warps: C chunk-warps per row stream, S streams.
-    const int S = std::max<int>(1, 16 / int(C));
-    const int threads = 32 * int(C) * S;
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + kP - 1) / kP));
-    const int64_t rows_cta = (n + grid - 1) / grid;
-    const size_t smem = size_t(C) * 32 * kSeg * 4 + size_t(rows_cta) * size_t(C) * 4;
-    if (smem > 200 * 1024) return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
-    const int64_t rows_stream = (rows_cta + S - 1) / S;
-    // deeper register batches when the CTA is small enough to afford them
-    auto kern = (threads <= 384 && rows_stream > 12) ? gemv_kernel<16, 384> : gemv_kernel<12, 512>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(std::max<size_t>(smem, 48 * 1024)));
+cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *residual,
+                               float *out, int64_t n, int64_t k, const LaunchCtx &ctx) {
+    const int C = int((k + kGvChunk - 1) / kGvChunk);
+    const int64_t kq = k / 4, kb = k / kBlockW;
+    if (C > 30) return cudaErrorNotSupported;
+    GvsParams P;
+    P.n = int(n);
+    P.k = int(k);
+    P.C = C;
+    P.rs = 4;
+    P.groups = 30 / C;  // consumer warp groups of C warps (one per chunk)
+    const int threads = 1024;  // 30 consumer warps at most, the producer warp, one helper
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + P.rs - 1) / P.rs));
+    P.rbase = int(n / grid);
+    P.rextra = int(n % grid);
+    P.rows_cta = P.rbase + (P.rextra ? 1 : 0);
+    const int nseg = C * 32;
+    const size_t stage_bytes = size_t(P.rs) * kq;
+    const size_t lwords = size_t(nseg) * kSegWords;
+    const size_t fixed = size_t(k) * 4 + lwords * 4 + size_t(nseg) * 8 +
+                         size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2 +
+                         size_t((P.rows_cta * C + 1) & ~1) * 4;
+    const size_t budget = 220 * 1024;
+    if (fixed + stage_bytes + 64 * 16 + 32 > budget) return cudaErrorNotSupported;
+    // ring: enough slots for all of a CTA's stages if shared memory allows (no
+    // refill round trips), as a multiple of the group count
+    const int nst = (P.rows_cta + P.rs - 1) / P.rs;
+    const int max_slots = int(std::min<size_t>(64, (budget - fixed - 64 * 16 - 32) / stage_bytes));
+    int ns = std::min(max_slots, ((nst + P.groups - 1) / P.groups) * P.groups);
+    ns = (ns / P.groups) * P.groups;
+    if (ns < P.groups) {  // fewer slots than groups: shrink the groups
+        P.groups = std::max(1, max_slots);
+        ns = P.groups;
+    }
+    P.ns = ns;
+    P.consumers = P.groups * C;
+    P.off_x = uint32_t(size_t(ns) * stage_bytes);
+    P.off_limbs = uint32_t(P.off_x + size_t(k) * 4);
+    P.off_scale = uint32_t(P.off_limbs + lwords * 4);
+    P.off_sum = uint32_t(P.off_scale + size_t(nseg) * 4);
+    P.off_d = uint32_t(P.off_sum + size_t(nseg) * 4);
+    P.off_partial = uint32_t(P.off_d + size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2);
+    P.off_bar = uint32_t(P.off_partial + size_t((P.rows_cta * C + 1) & ~1) * 4);
+    const size_t smem = size_t(P.off_bar) + size_t(2 * ns + 2) * 8 + 16;
+    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const SoaView v = soa_view(w_soa, n, k);
-    kern<<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(v.qs, v.d, x, residual, out,
-                                                                     int(n), int(k), int(C), S);
+    gemv_stream_kernel<4><<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(
+        v.qs, v.d, x, residual, out, P, ctx.status, ctx.wait_ns);
     return cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
+                        int64_t n, int64_t k, const LaunchCtx &ctx) {
+    if (k <= 16384 && n <= INT32_MAX) {
+        cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, ctx);
+        if (e != cudaErrorNotSupported) return e;
+        (void)cudaGetLastError();
+    }
+    // very long rows: the chunk-looping small-M kernel (exact f32)
+    return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
 }
 
 cudaError_t launch_skinny(const void *w_soa, const float *x, const float *residual, float *out,

@@ -87,14 +87,17 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// One try_wait: the thread may sleep (without using issue slots) until the
+// phase completes or about `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity,
+                                              uint32_t hint_ns = 1000000u) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -104,10 +107,11 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
 // `limit_ns` of %globaltimer time.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity,
                                                   uint64_t limit_ns, unsigned int *status) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const uint32_t hint = limit_ns < 1000000ull ? uint32_t(limit_ns) : 1000000u;
+    if (mbar_try_wait(bar, parity, hint)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity, hint)) return true;
         if (globaltimer_ns() - t0 >= limit_ns) {
             atomicOr(status, static_cast<unsigned int>(TQ2_ERR_TIMEOUT));
             return false;

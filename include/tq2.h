@@ -102,10 +102,16 @@ int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k
  * The decode-path GEMV `gemv_tq2_g128_v1` of the "oxibonsai-kernels 0.1.5 ...
  * pipelines.rs" page; the operation is the contract above with M = 1.
  *   w_soa    : device SoA weight (tq2_soa_bytes(n,k) bytes)
- *   x        : device f32 [k]
+ *   x        : device f32 [k], finite
  *   residual : device f32 [n], or NULL
  *   out      : device f32 [n]
- * Arithmetic: exact f32 products, f32 accumulation. */
+ * Arithmetic (k <= 16384): x is quantised per 64-weight segment to a signed
+ * fixed-point integer relative to the segment's largest |x| (23 bits:
+ * |x - xq| <= 2^-22 * max|x_segment|); the ternary dot products are then
+ * exact integer sums, scaled by max|x_segment| * 2^-22 * d and summed in f32.
+ * Per element: |error| <= sum over segments of 2^-22 * max|x_seg| * sum_seg |w|
+ * plus f32 rounding of the final sum.  For k > 16384: exact f32 products and
+ * f32 accumulation. */
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t n, int64_t k, void *stream);
 

@@ -128,11 +128,30 @@ def test_gemv_down_residual_full(tq2):
 
 
 @pytest.mark.parametrize("n,k", [(1, 128), (129, 128), (7, 1152), (300, 3072), (33, 20480),
-                                 (5, 65536)])
+                                 (5, 65536), (30400, 4096), (250000, 512), (2000, 16384)])
 def test_gemv_edge_shapes(tq2, n, k):
     p = tq2_synth.make_problem(1, n, k, seed=n * 7 + k, residual=(n % 2 == 1))
     w = upload(tq2, p)
     check(run(tq2, tq2.TQ2_KERNEL_GEMV, w, p), p, TOL_F32, what=f"gemv n={n} k={k}")
+
+
+def test_gemv_quantisation_bound_with_wide_dynamic_range(tq2):
+    # one huge activation per 64-weight segment next to tiny ones: the GEMV's
+    # documented bound (2^-22 * max|x_seg| * sum_seg |w| per segment) must hold
+    n, k = 512, 4096
+    p = tq2_synth.make_problem(1, n, k, seed=17)
+    rng = np.random.default_rng(5)
+    x = (rng.standard_normal(k) * 1e-3).astype(np.float32)
+    x[::64] = 1e3 * np.sign(rng.standard_normal(k // 64)).astype(np.float32)
+    p.x = x[None, :]
+    w = upload(tq2, p)
+    out = run(tq2, tq2.TQ2_KERNEL_GEMV, w, p)[0].astype(np.float64)
+    ref, scale = oracle.matmul(p.w_aos, p.x, n=n, k=k)
+    W = np.abs(oracle.dequant(p.w_aos, n, k))
+    smax = np.abs(x.astype(np.float64)).reshape(-1, 64).max(axis=1)
+    bound = (W.reshape(n, -1, 64).sum(axis=2) * smax[None, :]).sum(axis=1) * 2.0 ** -22
+    bound += 1e-6 * scale[0]
+    assert np.all(np.abs(out - ref[0]) <= bound)
 
 
 # ---------------------------------------------------------------------------
