@@ -3,27 +3,32 @@
 // persistent tcgen05 kernel streams them with bulk copies.
 //
 // Same contraction as the in-kernel-conversion kernel (the role of the
-// pages' `gemm_tq2_g128_v10_simdgroup`: weights dequantised into shared
-// memory as half, f16 operands, f32 accumulation, staging overlapped with the
-// matrix units; "oxibonsai-kernels 0.1.5 src/gpu_backend/metal_graph/
-// pipelines.rs").  What changes on sm_103a:
+// pages' `gemm_tq2_g128_v10_simdgroup`: weights dequantised on chip as half,
+// f16 operands, f32 accumulation, staging overlapped with the matrix units;
+// "oxibonsai-kernels 0.1.5 src/gpu_backend/metal_graph/pipelines.rs").  On
+// sm_103a it is computed transposed, out^T = W . x^T, so that the decoded
+// weights can be the MMA's A operand in tensor memory:
 //
 //  * Pre-pass: x f32 [M,K] -> f16 tiles of 128 rows x 64 k (16 KB each), laid
 //    out exactly as the MMA's K-major SWIZZLE_128B shared-memory image, with
 //    the K permutation that matches the weight decode (pairs (i, i+8) of every
-//    16-wide group).  Rows past M are zero.  One tile then moves with a single
-//    cp.async.bulk; the activation path costs the SM no load instructions.
-//  * Weight codes: a 2-D TMA load of the qs plane (256 rows x 16 bytes per
-//    stage) into shared memory; 8 decoder warps read their row's 16 bytes,
-//    decode to f16 (c - 1) * d and write the B tile.  The scales come with
-//    one 16-byte load per 8 blocks per row.
-//  * Persistent CTAs (one per SM) walk the 128 x 256 output tiles; the f32
-//    accumulator is double-buffered in TMEM (2 x 256 columns), so the
-//    epilogue of one tile overlaps the main loop of the next.
-//  * Roles: warp 0 issues the bulk/TMA copies, warp 1 the MMAs (and owns
-//    TMEM), warps 4-7 run the epilogue (TMEM lanes 0-127), warps 8-15 decode.
-//  * All mbarrier waits are bounded; on a timeout the roles stop, the issued
-//    copies and MMAs drain, and TMEM is freed before exit.
+//    16-wide group).  Rows past M are zero.  Two tiles (256 x rows) move per
+//    pipeline stage with cp.async.bulk: the B operand.
+//  * Weight codes: a 2-D TMA load of the qs plane (128 rows x 16 bytes per
+//    stage).  8 decoder warps decode (c - 1) * d to f16 in registers and write
+//    the 128 x 64 A tile straight into tensor memory with tcgen05.st, so the
+//    decoded weights never touch shared memory (the shared-memory traffic per
+//    stage is the 32 KB x tile in and out of the tensor core only).
+//  * tcgen05.mma kind::f16, M = 128 weight rows, N = 256 x rows, K = 16,
+//    f32 accumulation in TMEM.  Output tile 256 (x rows) x 128 (weight rows);
+//    persistent CTAs walk the tiles.
+//  * Epilogue: TMEM lane = output column, so each tcgen05.ld gives a warp 32
+//    consecutive output columns of one output row: stores (and the residual
+//    loads) are 128-byte coalesced without staging.
+//  * Roles: warp 0 issues the code TMA loads, warp 1 the MMAs (and owns TMEM),
+//    warp 2 the x-tile bulk copies, warps 4-7 run the epilogue, warps 8-15
+//    decode.  All mbarrier waits are bounded; on a timeout the roles stop, the
+//    issued copies and MMAs drain, and TMEM is freed before exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,37 +41,40 @@
 namespace tq2 {
 namespace {
 
-constexpr int BM = 128, BN = 256, BK = 64, STAGES = 4, CSTAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;     // 16 KB (one pre-converted tile)
-constexpr int B_BYTES = BN * BK * 2;     // 32 KB
-constexpr int C_BYTES = BN * BK / 4;     // 4 KB of raw codes
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 768;
-// warp 0: code TMA issuer, warp 1: MMA issuer + TMEM owner, warp 2: A-tile
-// issuer, warps 4-7: epilogue, warps 8-23: decoders
-constexpr int TMA_WARP = 0, MMA_WARP = 1, A_WARP = 2, EPI_WARP0 = 4, DEC_WARP0 = 8;
-constexpr int NUM_DEC = 512;             // two decoder threads per weight row (32 codes each)
+constexpr int BM = 128;                  // pre-converted x tile height (rows)
+constexpr int BX = 256;                  // x rows per output tile (MMA N)
+constexpr int BW = 128;                  // weight rows per output tile (MMA M)
+constexpr int BK = 64, STAGES = 4, CSTAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;     // 16 KB: one pre-converted x tile
+constexpr int X_BYTES = BX * BK * 2;     // 32 KB: the B operand of one stage
+constexpr int C_BYTES = BW * BK / 4;     // 2 KB of raw codes
+constexpr int NUM_THREADS = 512;
+// warp 0: code TMA issuer, warp 1: MMA issuer + TMEM owner, warp 2: x-tile
+// issuer, warps 4-7: epilogue, warps 8-15: decoders
+constexpr int TMA_WARP = 0, MMA_WARP = 1, X_WARP = 2, EPI_WARP0 = 4, DEC_WARP0 = 8;
+constexpr int NUM_DEC = 256;             // two decoder threads per weight row (32 codes each)
 constexpr int NUM_EPI = 128;
-constexpr int EPI_LD = 33;               // padded row of the epilogue staging buffer (floats)
-constexpr int EPI_BYTES = 4 * 32 * EPI_LD * 4;  // one 32 x 32 f32 block per epilogue warp
-constexpr uint32_t TMEM_COLS = 512;      // two 128 x 256 f32 accumulators
-constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BN >> 3) << 17) | (uint32_t(BM >> 4) << 24);
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t ACC_COL = 0;          // f32 accumulator: 256 columns
+constexpr uint32_t A_COL0 = 256;         // decoded weights: STAGES x 32 columns
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16, both
+// K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BX >> 3) << 17) | (uint32_t(BW >> 4) << 24);
 
 struct Ctl {
-    uint64_t full_a[STAGES];
-    uint64_t full_b[STAGES];
+    uint64_t x_full[STAGES];
+    uint64_t a_full[STAGES];
     uint64_t empty[STAGES];
     uint64_t codes_full[CSTAGES];
     uint64_t codes_empty[CSTAGES];
-    uint64_t tmem_full[2];
-    uint64_t tmem_empty[2];
+    uint64_t tmem_full;
+    uint64_t tmem_empty;
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = size_t(STAGES) * STAGE_BYTES + size_t(CSTAGES) * C_BYTES +
-                              size_t(EPI_BYTES) + sizeof(Ctl) + 1024;
+constexpr size_t SMEM_BYTES = size_t(STAGES) * X_BYTES + size_t(CSTAGES) * C_BYTES + sizeof(Ctl) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
@@ -105,22 +113,6 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
-                                             uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
-}
-
-__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
-    uint4 v;
-    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "r"(addr)
-                 : "memory");
-    return v;
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -133,6 +125,30 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, one CTA.
+__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -211,34 +227,32 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     const uint32_t sbase = raw_addr + pad;
-    float *epi_stage = reinterpret_cast<float *>(smem_raw + pad + size_t(STAGES) * STAGE_BYTES +
-                                                 size_t(CSTAGES) * C_BYTES);
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * STAGE_BYTES +
-                                       size_t(CSTAGES) * C_BYTES + EPI_BYTES);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * X_BYTES +
+                                       size_t(CSTAGES) * C_BYTES);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KT = K / BK;
-    const int MT = (M + BM - 1) / BM, NT = (N + BN - 1) / BN;
-    const int ntiles = MT * NT;
+    const int MT = (M + BM - 1) / BM;           // 128-row x tiles in the workspace
+    const int MX = (M + BX - 1) / BX;           // 256-row output tiles
+    const int NW = (N + BW - 1) / BW;
+    const int ntiles = MX * NW;
     const int64_t kb = K / kBlockW;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->full_a[s], 1);
-            mbar_init(&ctl->full_b[s], NUM_DEC);
+            mbar_init(&ctl->x_full[s], 1);
+            mbar_init(&ctl->a_full[s], NUM_DEC);
             mbar_init(&ctl->empty[s], 1);
         }
         for (int s = 0; s < CSTAGES; ++s) {
             mbar_init(&ctl->codes_full[s], 1);
             mbar_init(&ctl->codes_empty[s], NUM_DEC);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&ctl->tmem_full[b], 1);
-            mbar_init(&ctl->tmem_empty[b], NUM_EPI);
-        }
+        mbar_init(&ctl->tmem_full, 1);
+        mbar_init(&ctl->tmem_empty, NUM_EPI);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
-        fence_mbarrier_init();
+        fence_proxy_async_smem();
     }
     if (warp == MMA_WARP) {
         tmem_alloc(&ctl->tmem_base, TMEM_COLS);
@@ -250,27 +264,26 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort;
 
-    auto stage_a = [&](int s) { return sbase + uint32_t(s) * STAGE_BYTES; };
-    auto stage_b = [&](int s) { return sbase + uint32_t(s) * STAGE_BYTES + A_BYTES; };
+    auto stage_x = [&](int s) { return sbase + uint32_t(s) * X_BYTES; };
     auto stage_c = [&](int s) {
-        return sbase + uint32_t(STAGES) * STAGE_BYTES + uint32_t(s) * C_BYTES;
+        return sbase + uint32_t(STAGES) * X_BYTES + uint32_t(s) * C_BYTES;
     };
 
-    if (warp == TMA_WARP || warp == A_WARP) {
-        // Two independent copy streams: weight codes into their own deep ring
-        // (warp 0), pre-converted activation tiles into the A/B ring (warp 2).
+    if (warp == TMA_WARP || warp == X_WARP) {
+        // Two independent copy streams: weight codes into their own ring
+        // (warp 0), pre-converted x tiles into the operand ring (warp 2).
         const bool codes = warp == TMA_WARP;
         const int depth = codes ? CSTAGES : STAGES;
         if (lane == 0) {
             if (codes)
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
             int64_t g = 0;
-            int last_round[CSTAGES];
-            for (int s = 0; s < CSTAGES; ++s) last_round[s] = -1;
+            int last_round[STAGES > CSTAGES ? STAGES : CSTAGES];
+            for (int s = 0; s < depth; ++s) last_round[s] = -1;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int mt = t % MT, nt = t / MT;
-                const uint8_t *atile = xtiles + int64_t(mt) * KT * A_BYTES;
+                const int mx = t % MX, nw = t / MX;
+                const int mt0 = 2 * mx, nmt = min(2, MT - mt0);  // 128-row x tiles of this output tile
                 for (int kt = 0; kt < KT; ++kt, ++g) {
                     const int s = int(g % depth);
                     const int u = int(g / depth);
@@ -283,10 +296,13 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                     if (*abort_flag) { ok = false; break; }
                     if (codes) {
                         mbar_expect_tx(&ctl->codes_full[s], C_BYTES);
-                        tma_2d(stage_c(s), &qmap, kt * (BK / 4), nt * BN, &ctl->codes_full[s]);
+                        tma_2d(stage_c(s), &qmap, kt * (BK / 4), nw * BW, &ctl->codes_full[s]);
                     } else {
-                        mbar_expect_tx(&ctl->full_a[s], A_BYTES);
-                        bulk_g2s(stage_a(s), atile + int64_t(kt) * A_BYTES, A_BYTES, &ctl->full_a[s]);
+                        mbar_expect_tx(&ctl->x_full[s], uint32_t(nmt) * A_BYTES);
+                        for (int h = 0; h < nmt; ++h)
+                            bulk_g2s(stage_x(s) + uint32_t(h) * A_BYTES,
+                                     xtiles + (int64_t(mt0 + h) * KT + kt) * A_BYTES, A_BYTES,
+                                     &ctl->x_full[s]);
                     }
                     last_round[s] = u;
                 }
@@ -295,7 +311,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
             const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
             for (int s = 0; s < depth; ++s) {
                 if (last_round[s] < 0) continue;
-                mbar_wait_bounded(codes ? &ctl->codes_full[s] : &ctl->full_a[s], last_round[s] & 1,
+                mbar_wait_bounded(codes ? &ctl->codes_full[s] : &ctl->x_full[s], last_round[s] & 1,
                                   drain, status);
             }
         }
@@ -306,44 +322,44 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
             int i = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
-                const int ab = i & 1, ur = i >> 1;
-                if (ur > 0 && !mbar_wait_bounded(&ctl->tmem_empty[ab], (ur - 1) & 1, wait_ns, status)) {
+                if (i > 0 && !mbar_wait_bounded(&ctl->tmem_empty, (i - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t dt = tmem + uint32_t(ab * BN);
                 for (int kt = 0; kt < KT; ++kt, ++g) {
                     const int s = int(g % STAGES);
                     const uint32_t par = uint32_t(g / STAGES) & 1;
-                    if (!mbar_wait_bounded(&ctl->full_a[s], par, wait_ns, status) ||
-                        !mbar_wait_bounded(&ctl->full_b[s], par, wait_ns, status)) {
+                    if (!mbar_wait_bounded(&ctl->x_full[s], par, wait_ns, status) ||
+                        !mbar_wait_bounded(&ctl->a_full[s], par, wait_ns, status)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
                     }
                     if (*abort_flag) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t adesc = sw128_desc(stage_a(s));
-                    const uint64_t bdesc = sw128_desc(stage_b(s));
+                    const uint64_t bdesc = sw128_desc(stage_x(s));
+                    const uint32_t acol = tmem + A_COL0 + uint32_t(s) * (BK / 2);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_f16(dt, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kt | kk) != 0);
+                        tc_mma_f16_ta(tmem + ACC_COL, acol + uint32_t(kk) * 8, bdesc + 2 * kk, IDESC,
+                                      (kt | kk) != 0);
                     tc_commit(&ctl->empty[s]);
                 }
-                if (ok) tc_commit(&ctl->tmem_full[ab]);
+                if (ok) tc_commit(&ctl->tmem_full);
             }
         }
         __syncwarp();
     } else if (warp >= DEC_WARP0) {
-        const int dt = tid - DEC_WARP0 * 32;
-        const int pt = dt & (BN - 1);    // weight row in the tile
-        const int hw = dt >> 8;          // which 32 codes of the row's 64 (words 2hw, 2hw+1)
+        const int dw = warp - DEC_WARP0;       // 0..7
+        const int quarter = dw & 3;            // TMEM lane quarter of this warp (warp % 4)
+        const int khalf = dw >> 2;             // which 32 codes of the row's 64 per stage
+        const int pr = quarter * 32 + lane;    // weight row in the tile = TMEM lane
         int64_t g = 0;
         const bool dvec = (kb % 8) == 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
-            const int nt = t / MT;
-            const int row = nt * BN + pt;
+            const int nw = t / MX;
+            const int row = nw * BW + pr;
             const bool rvalid = row < N;
             const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
             // scales: 8 blocks (16 stages) per 16-byte load, one group ahead
@@ -368,22 +384,22 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                                        status)) {
                     *abort_flag = 1;
                     stop = true;
-                    break;
                 }
-                uint2 code;
-                asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
-                             : "=r"(code.x), "=r"(code.y)
-                             : "r"(stage_c(cs) + uint32_t(pt) * 16 + uint32_t(hw) * 8)
-                             : "memory");
+                uint2 code = make_uint2(0x55555555u, 0x55555555u);
+                if (!stop)
+                    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
+                                 : "=r"(code.x), "=r"(code.y)
+                                 : "r"(stage_c(cs) + uint32_t(pr) * 16 + uint32_t(khalf) * 8)
+                                 : "memory");
                 mbar_arrive(&ctl->codes_empty[cs]);
-                // the B slot is free once the MMAs of its previous round completed
+                // the A slot is free once the MMAs of its previous round completed
                 const int u = int(g / STAGES);
-                if (u > 0 && !mbar_wait_bounded(&ctl->empty[s], (u - 1) & 1, wait_ns, status)) {
+                if (!stop && u > 0 && !mbar_wait_bounded(&ctl->empty[s], (u - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     stop = true;
-                    break;
                 }
-                if (*abort_flag) { stop = true; break; }
+                // tcgen05.st is warp-collective: a stopping warp stops as a whole
+                if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
                 uint32_t dbits;
                 if (dvec) {
                     const int e = blk & 7;
@@ -394,71 +410,55 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                 }
                 if (!rvalid) dbits = 0;
                 const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(dbits)));
-                const uint32_t bb = stage_b(s);
+                uint32_t o[16];
+                {
+                    uint32_t oa[8], ob[8];
+                    decode_word(code.x, d2, oa);
+                    decode_word(code.y, d2, ob);
 #pragma unroll
-                for (int q = 0; q < 2; ++q) {
-                    uint32_t o[8];
-                    decode_word(q == 0 ? code.x : code.y, d2, o);
-                    const int j = 4 * hw + 2 * q;
-                    st_shared_v4(bb + sw128_off(pt, j), o[0], o[1], o[2], o[3]);
-                    st_shared_v4(bb + sw128_off(pt, j + 1), o[4], o[5], o[6], o[7]);
-                }
-                fence_proxy_async_smem();
-                mbar_arrive(&ctl->full_b[s]);
-            }
-            if (stop) break;
-        }
-    } else if (warp >= EPI_WARP0) {
-        const int ew = warp - EPI_WARP0;  // TMEM lanes 32*ew .. 32*ew+31
-        int i = 0;
-        const bool vec = (N % 4) == 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-            const int ab = i & 1, ur = i >> 1;
-            const int mt = t % MT, nt = t / MT;
-            if (!mbar_wait_bounded(&ctl->tmem_full[ab], ur & 1, wait_ns, status)) {
-                *abort_flag = 1;
-                break;
-            }
-            if (*abort_flag) break;
-            tc_fence_after();
-            // Each 32 x 32 f32 block: TMEM -> registers (thread = row) -> padded
-            // shared memory -> coalesced rows (8 lanes per 128-byte row segment).
-            float *st = epi_stage + ew * 32 * EPI_LD;
-            const int rsub = lane >> 3, csub = (lane & 7) * 4;
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + (uint32_t(ew * 32) << 16) + uint32_t(ab * BN + c * 32), r);
-                tc_wait_ld();
-                if (c == BN / 32 - 1) {
-                    tc_fence_before();
-                    mbar_arrive(&ctl->tmem_empty[ab]);
-                }
-#pragma unroll
-                for (int j = 0; j < 32; ++j) st[lane * EPI_LD + j] = __uint_as_float(r[j]);
-                __syncwarp();
-                const int col = nt * BN + c * 32 + csub;
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int rl = 4 * i + rsub;
-                    const int row = mt * BM + ew * 32 + rl;
-                    const float *sp = st + rl * EPI_LD + csub;
-                    float4 v = make_float4(sp[0], sp[1], sp[2], sp[3]);
-                    if (row < M) {
-                        const int64_t o = int64_t(row) * N + col;
-                        if (vec && col + 4 <= N) {
-                            if (residual) {
-                                const float4 rr = *reinterpret_cast<const float4 *>(residual + o);
-                                v.x += rr.x; v.y += rr.y; v.z += rr.z; v.w += rr.w;
-                            }
-                            *reinterpret_cast<float4 *>(out + o) = v;
-                        } else {
-                            const float vv[4] = {v.x, v.y, v.z, v.w};
-                            for (int e = 0; e < 4 && col + e < N; ++e)
-                                out[o + e] = vv[e] + (residual ? residual[o + e] : 0.f);
-                        }
+                    for (int j = 0; j < 8; ++j) {
+                        o[j] = oa[j];
+                        o[8 + j] = ob[j];
                     }
                 }
-                __syncwarp();
+                tmem_st16(tmem + (uint32_t(quarter * 32) << 16) + A_COL0 + uint32_t(s) * (BK / 2) +
+                              uint32_t(khalf) * 16,
+                          o);
+                tc_wait_st();
+                tc_fence_before();
+                mbar_arrive(&ctl->a_full[s]);
+            }
+            if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
+        }
+    } else if (warp >= EPI_WARP0) {
+        const int quarter = warp - EPI_WARP0;  // TMEM lanes 32*quarter .. +31 = output columns
+        int i = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int mx = t % MX, nw = t / MX;
+            if (!mbar_wait_bounded(&ctl->tmem_full, i & 1, wait_ns, status)) *abort_flag = 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+            tc_fence_after();
+            const int col = nw * BW + quarter * 32 + lane;
+            const bool cvalid = col < N;
+            for (int c = 0; c < BX / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + ACC_COL + uint32_t(c * 32), r);
+                tc_wait_ld();
+                if (c == BX / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(&ctl->tmem_empty);
+                }
+                const int row0 = mx * BX + c * 32;
+                if (!cvalid) continue;
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int row = row0 + j;
+                    if (row >= M) break;
+                    const int64_t o = int64_t(row) * N + col;
+                    float v = __uint_as_float(r[j]);
+                    if (residual) v += residual[o];
+                    out[o] = v;
+                }
             }
         }
     }
@@ -541,7 +541,7 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
     CUtensorMap qmap;
     const cuuint64_t gdim[2] = {cuuint64_t(k / 4), cuuint64_t(n)};
     const cuuint64_t gstride[1] = {cuuint64_t(k / 4)};
-    const cuuint32_t box[2] = {BK / 4, BN};
+    const cuuint32_t box[2] = {BK / 4, BW};
     const cuuint32_t estride[2] = {1, 1};
     if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(v.qs), gdim, gstride, box,
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -558,7 +558,7 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
     e = cudaFuncSetAttribute(tc_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = int64_t(MT) * ((n + BN - 1) / BN);
+    const int64_t ntiles = ((m + BX - 1) / BX) * ((n + BW - 1) / BW);
     const int64_t grid = std::min<int64_t>(ntiles, ctx.num_sms);
     tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
         qmap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
