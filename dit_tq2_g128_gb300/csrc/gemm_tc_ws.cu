@@ -6,34 +6,41 @@
 // pages' `gemm_tq2_g128_v10_simdgroup`: weights dequantised on chip as half,
 // f16 operands, f32 accumulation, staging overlapped with the matrix units;
 // "oxibonsai-kernels 0.1.5 src/gpu_backend/metal_graph/pipelines.rs").  On
-// sm_103a it is computed transposed, out^T = W . x^T, so that the decoded
-// weights can be the MMA's A operand in tensor memory:
+// sm_103a it is computed transposed, out^T = W . x^T:
 //
 //  * Pre-pass: x f32 [M,K] -> f16 tiles of 128 rows x 64 k (16 KB each), laid
 //    out exactly as the MMA's K-major SWIZZLE_128B shared-memory image, with
 //    the K permutation that matches the weight decode (pairs (i, i+8) of every
 //    16-wide group).  Rows past M are zero.  Two tiles (256 x rows) move per
-//    pipeline stage with cp.async.bulk: the B operand.
+//    pipeline stage with cp.async.bulk: the MMA's B operand.
 //  * Weight codes: a 2-D TMA load of the qs plane (128 rows x 16 bytes per
-//    stage).  8 decoder warps decode (c - 1) * d to f16 in registers and write
-//    the 128 x 64 A tile straight into tensor memory with tcgen05.st, so the
-//    decoded weights never touch shared memory (the shared-memory traffic per
-//    stage is the 32 KB x tile in and out of the tensor core only).
-//  * tcgen05.mma kind::f16, M = 128 weight rows, N = 256 x rows, K = 16,
-//    f32 accumulation in TMEM.  Output tile 256 (x rows) x 128 (weight rows);
-//    persistent CTAs walk the tiles.
+//    stage).  Decoder threads each turn one row's 64 codes into (c - 1) * d
+//    in f16 registers and store them as the A operand (128 rows x 64 k, the
+//    same swizzled image) in shared memory.
+//  * tcgen05.mma kind::f16, M = 128 weight rows, N = 256 x rows, K = 16, both
+//    operands in shared memory (the tensor core's full rate), f32
+//    accumulation in tensor memory.  TMEM holds two 256-column accumulators,
+//    so the epilogue of one output tile (256 x rows x 128 weight rows)
+//    overlaps the MMAs of the next.  Persistent CTAs walk the tiles.
 //  * Epilogue: TMEM lane = output column, so each tcgen05.ld gives a warp 32
-//    consecutive output columns of one output row: stores (and the residual
-//    loads) are 128-byte coalesced without staging.
+//    consecutive output columns of 32 output rows.  The warp stages that
+//    32 x 32 block in shared memory and hands it to a TMA tensor store (or a
+//    TMA reduce-add when the residual is the output itself), so the
+//    global writes are issued asynchronously.  When N is not a multiple of 4 (no
+//    16-byte row pitch for a tensor map) or the residual is a separate array,
+//    the warp stores directly (each store still 128-byte coalesced).
 //  * Roles: warp 0 issues the code TMA loads, warp 1 the MMAs (and owns TMEM),
-//    warp 2 the x-tile bulk copies, warps 4-7 run the epilogue, warps 8-15
-//    decode.  All mbarrier waits are bounded; on a timeout the roles stop, the
-//    issued copies and MMAs drain, and TMEM is freed before exit.
+//    warp 2 the x-tile bulk copies, warps 4-7 run the epilogue, warps 8-23
+//    decode (four sets of four warps; set j fills ring slot j, i.e. the
+//    stages g = j mod 4).  All mbarrier
+//    waits are bounded; on a timeout the roles stop, the issued copies and
+//    MMAs drain, and TMEM is freed before exit.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
 #include <algorithm>
 #include <climits>
+#include <cstring>
 #include <mutex>
 
 #include "tq2_internal.cuh"
@@ -47,16 +54,22 @@ constexpr int BW = 128;                  // weight rows per output tile (MMA M)
 constexpr int BK = 64, STAGES = 4, CSTAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;     // 16 KB: one pre-converted x tile
 constexpr int X_BYTES = BX * BK * 2;     // 32 KB: the B operand of one stage
+constexpr int W_BYTES = BW * BK * 2;     // 16 KB: the decoded A operand of one stage
 constexpr int C_BYTES = BW * BK / 4;     // 2 KB of raw codes
-constexpr int NUM_THREADS = 512;
+constexpr int NUM_THREADS = 768;
 // warp 0: code TMA issuer, warp 1: MMA issuer + TMEM owner, warp 2: x-tile
-// issuer, warps 4-7: epilogue, warps 8-15: decoders
+// issuer, warps 4-7: epilogue, warps 8-23: decoders (four sets of four warps,
+// one set per ring slot)
 constexpr int TMA_WARP = 0, MMA_WARP = 1, X_WARP = 2, EPI_WARP0 = 4, DEC_WARP0 = 8;
-constexpr int NUM_DEC = 256;             // two decoder threads per weight row (32 codes each)
+constexpr int DEC_SETS = 4;
+constexpr int NUM_DEC = 128;             // per stage: one decoder thread per weight row (64 codes)
 constexpr int NUM_EPI = 128;
+constexpr int EPI_NB = 1;                // staging buffers per epilogue warp
+constexpr int EPI_BYTES = 32 * 32 * 4;   // one 32 x 32 f32 block
+// Epilogue modes chosen by the host.
+constexpr int EPI_DIRECT = 0, EPI_TMA_STORE = 1, EPI_TMA_ADD = 2;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t ACC_COL = 0;          // f32 accumulator: 256 columns
-constexpr uint32_t A_COL0 = 256;         // decoded weights: STAGES x 32 columns
+constexpr uint32_t ACC_COL = 0;          // two f32 accumulators of BX columns
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16, both
 // K-major, N >> 3 at bits 17-22, M >> 4 at bits 24-28.
 constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BX >> 3) << 17) | (uint32_t(BW >> 4) << 24);
@@ -67,15 +80,22 @@ struct Ctl {
     uint64_t empty[STAGES];
     uint64_t codes_full[CSTAGES];
     uint64_t codes_empty[CSTAGES];
-    uint64_t tmem_full;
-    uint64_t tmem_empty;
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
     uint64_t drain;
     uint32_t tmem_base;
     int abort;
 };
 
-constexpr size_t SMEM_BYTES = size_t(STAGES) * X_BYTES + size_t(CSTAGES) * C_BYTES + sizeof(Ctl) + 1024;
+constexpr size_t EPI_TOTAL = size_t(4) * EPI_NB * EPI_BYTES;
+constexpr size_t SMEM_BYTES = size_t(STAGES) * (X_BYTES + W_BYTES) + size_t(CSTAGES) * C_BYTES +
+                              EPI_TOTAL + sizeof(Ctl) + 1024;
 static_assert(SMEM_BYTES <= 232448, "shared memory budget");
+// Decoder set j takes the stages g = j (mod 4); with ring depths that are
+// multiples of 4 every ring slot is always visited by the same set, which
+// keeps each set's barrier phases in step (no parity aliasing).
+static_assert(STAGES % DEC_SETS == 0 && CSTAGES % DEC_SETS == 0, "ring depths vs decoder sets");
+static_assert(ACC_COL + 2 * BX <= TMEM_COLS, "TMEM budget");
 
 __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
     return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
@@ -113,6 +133,31 @@ __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int
         : "memory");
 }
 
+// Tensor store (or reduce-add) of one staged box; completion tracked by bulk groups.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_add_2d(const CUtensorMap *map, int x, int y, uint32_t src) {
+    asm volatile(
+        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(x), "r"(y), "r"(src)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// At most EPI_NB - 1 of this thread's bulk groups may still be reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_nb() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(EPI_NB - 1) : "memory");
+}
+
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -125,30 +170,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr)
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_wait_st() {
-    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16, one CTA.
-__device__ __forceinline__ void tc_mma_f16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
-                                              uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -220,15 +241,15 @@ x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, 
 // Main kernel.
 
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict__ dpl,
-             const uint8_t *__restrict__ xtiles, const float *residual, float *out, int M, int N,
-             int K, unsigned int *status, uint64_t wait_ns) {
+tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+             const __half *__restrict__ dpl, const uint8_t *__restrict__ xtiles, const float *residual,
+             float *out, int M, int N, int K, int epi_mode, unsigned int *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
     const uint32_t sbase = raw_addr + pad;
-    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * X_BYTES +
-                                       size_t(CSTAGES) * C_BYTES);
+    Ctl *ctl = reinterpret_cast<Ctl *>(smem_raw + pad + size_t(STAGES) * (X_BYTES + W_BYTES) +
+                                       size_t(CSTAGES) * C_BYTES + EPI_TOTAL);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int KT = K / BK;
@@ -248,8 +269,10 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
             mbar_init(&ctl->codes_full[s], 1);
             mbar_init(&ctl->codes_empty[s], NUM_DEC);
         }
-        mbar_init(&ctl->tmem_full, 1);
-        mbar_init(&ctl->tmem_empty, NUM_EPI);
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&ctl->tmem_full[a], 1);
+            mbar_init(&ctl->tmem_empty[a], NUM_EPI);
+        }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         fence_proxy_async_smem();
@@ -264,10 +287,13 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort;
 
+    // shared memory: x ring | decoded-weight ring | code ring | epilogue staging | Ctl
     auto stage_x = [&](int s) { return sbase + uint32_t(s) * X_BYTES; };
+    auto stage_w = [&](int s) { return sbase + uint32_t(STAGES) * X_BYTES + uint32_t(s) * W_BYTES; };
     auto stage_c = [&](int s) {
-        return sbase + uint32_t(STAGES) * X_BYTES + uint32_t(s) * C_BYTES;
+        return sbase + uint32_t(STAGES) * (X_BYTES + W_BYTES) + uint32_t(s) * C_BYTES;
     };
+    const uint32_t ebase = sbase + uint32_t(STAGES) * (X_BYTES + W_BYTES) + uint32_t(CSTAGES) * C_BYTES;
 
     if (warp == TMA_WARP || warp == X_WARP) {
         // Two independent copy streams: weight codes into their own ring
@@ -322,11 +348,14 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
             int i = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
-                if (i > 0 && !mbar_wait_bounded(&ctl->tmem_empty, (i - 1) & 1, wait_ns, status)) {
+                const int a = i & 1;
+                // accumulator a was last used by tile i - 2: wait for its epilogue
+                if (i >= 2 && !mbar_wait_bounded(&ctl->tmem_empty[a], ((i >> 1) - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
                 tc_fence_after();
+                const uint32_t dcol = tmem + ACC_COL + uint32_t(a) * BX;
                 for (int kt = 0; kt < KT; ++kt, ++g) {
                     const int s = int(g % STAGES);
                     const uint32_t par = uint32_t(g / STAGES) & 1;
@@ -338,58 +367,48 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                     }
                     if (*abort_flag) { ok = false; break; }
                     tc_fence_after();
+                    const uint64_t adesc = sw128_desc(stage_w(s));
                     const uint64_t bdesc = sw128_desc(stage_x(s));
-                    const uint32_t acol = tmem + A_COL0 + uint32_t(s) * (BK / 2);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_f16_ta(tmem + ACC_COL, acol + uint32_t(kk) * 8, bdesc + 2 * kk, IDESC,
-                                      (kt | kk) != 0);
+                        tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kt | kk) != 0);
                     tc_commit(&ctl->empty[s]);
                 }
-                if (ok) tc_commit(&ctl->tmem_full);
+                if (ok) tc_commit(&ctl->tmem_full[a]);
             }
         }
         __syncwarp();
     } else if (warp >= DEC_WARP0) {
-        const int dw = warp - DEC_WARP0;       // 0..7
-        const int quarter = dw & 3;            // TMEM lane quarter of this warp (warp % 4)
-        const int khalf = dw >> 2;             // which 32 codes of the row's 64 per stage
-        const int pr = quarter * 32 + lane;    // weight row in the tile = TMEM lane
-        int64_t g = 0;
-        const bool dvec = (kb % 8) == 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x) {
+        const int dset = (warp - DEC_WARP0) >> 2;  // stages g = dset (mod 4), i.e. ring slot dset
+        const int pr = (warp & 3) * 32 + lane;     // weight row in the tile
+        const uint32_t rsw = uint32_t(pr & 7);     // SWIZZLE_128B phase of this row
+        const uint32_t rbase = uint32_t(pr >> 3) * 1024 + rsw * 128;
+        int64_t gbase = 0;
+        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, gbase += KT) {
             const int nw = t / MX;
             const int row = nw * BW + pr;
             const bool rvalid = row < N;
             const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
-            // scales: 8 blocks (16 stages) per 16-byte load, one group ahead
-            uint4 dv = make_uint4(0, 0, 0, 0), dv_next = make_uint4(0, 0, 0, 0);
-            if (dvec && rvalid) dv_next = __ldg(reinterpret_cast<const uint4 *>(drow));
-            uint32_t dscalar = 0;
+            const int kt0 = int(((dset - gbase) % DEC_SETS + DEC_SETS) % DEC_SETS);
+            // the scale of this thread's next stage, loaded one stage ahead
+            uint32_t dnext = (rvalid && kt0 < KT) ? ldg_u16(drow + (kt0 >> 1)) : 0u;
             bool stop = false;
-            for (int kt = 0; kt < KT; ++kt, ++g) {
+            for (int kt = kt0; kt < KT; kt += DEC_SETS) {
+                const int64_t g = gbase + kt;
                 const int cs = int(g % CSTAGES);
                 const int s = int(g % STAGES);
-                const int blk = kt >> 1;
-                if (dvec) {
-                    if ((kt & 15) == 0) {
-                        dv = dv_next;
-                        if (rvalid && blk + 8 < kb)
-                            dv_next = __ldg(reinterpret_cast<const uint4 *>(drow + blk + 8));
-                    }
-                } else if ((kt & 1) == 0 && rvalid) {
-                    dscalar = ldg_u16(drow + blk);
-                }
+                const uint32_t dbits = dnext;
+                if (rvalid && kt + DEC_SETS < KT) dnext = ldg_u16(drow + ((kt + DEC_SETS) >> 1));
                 if (!mbar_wait_bounded(&ctl->codes_full[cs], uint32_t(g / CSTAGES) & 1, wait_ns,
                                        status)) {
                     *abort_flag = 1;
                     stop = true;
                 }
-                uint2 code = make_uint2(0x55555555u, 0x55555555u);
+                uint4 code = make_uint4(0x55555555u, 0x55555555u, 0x55555555u, 0x55555555u);
                 if (!stop)
-                    asm volatile("ld.shared.v2.b32 {%0,%1}, [%2];"
-                                 : "=r"(code.x), "=r"(code.y)
-                                 : "r"(stage_c(cs) + uint32_t(pr) * 16 + uint32_t(khalf) * 8)
+                    asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];"
+                                 : "=r"(code.x), "=r"(code.y), "=r"(code.z), "=r"(code.w)
+                                 : "r"(stage_c(cs) + uint32_t(pr) * 16)
                                  : "memory");
                 mbar_arrive(&ctl->codes_empty[cs]);
                 // the A slot is free once the MMAs of its previous round completed
@@ -398,69 +417,92 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__restrict_
                     *abort_flag = 1;
                     stop = true;
                 }
-                // tcgen05.st is warp-collective: a stopping warp stops as a whole
-                if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
-                uint32_t dbits;
-                if (dvec) {
-                    const int e = blk & 7;
-                    const uint32_t wv = (e >> 1) == 0 ? dv.x : (e >> 1) == 1 ? dv.y : (e >> 1) == 2 ? dv.z : dv.w;
-                    dbits = (e & 1) ? (wv >> 16) : (wv & 0xFFFFu);
-                } else {
-                    dbits = dscalar;
-                }
-                if (!rvalid) dbits = 0;
-                const __half2 d2 = __half2half2(__ushort_as_half(static_cast<unsigned short>(dbits)));
-                uint32_t o[16];
-                {
-                    uint32_t oa[8], ob[8];
-                    decode_word(code.x, d2, oa);
-                    decode_word(code.y, d2, ob);
+                if (stop || *abort_flag) break;
+                const __half2 d2 =
+                    __half2half2(__ushort_as_half(static_cast<unsigned short>(rvalid ? dbits : 0u)));
+                // word w (k 16w..16w+15 of the stage) -> 16-byte chunks 2w, 2w+1 of the row
+                const uint32_t wbase = stage_w(s) + rbase;
+                const uint32_t cw[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) {
-                        o[j] = oa[j];
-                        o[8 + j] = ob[j];
-                    }
+                for (int w = 0; w < 4; ++w) {
+                    uint32_t o[8];
+                    decode_word(cw[w], d2, o);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wbase + (((2 * w) ^ rsw) << 4)),
+                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                 : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wbase + (((2 * w + 1) ^ rsw) << 4)),
+                                 "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                 : "memory");
                 }
-                tmem_st16(tmem + (uint32_t(quarter * 32) << 16) + A_COL0 + uint32_t(s) * (BK / 2) +
-                              uint32_t(khalf) * 16,
-                          o);
-                tc_wait_st();
-                tc_fence_before();
+                // make the generic-proxy stores visible to the tensor core
+                fence_proxy_async_smem();
                 mbar_arrive(&ctl->a_full[s]);
             }
             if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
         }
     } else if (warp >= EPI_WARP0) {
         const int quarter = warp - EPI_WARP0;  // TMEM lanes 32*quarter .. +31 = output columns
-        int i = 0;
+        const uint32_t ebuf = ebase + uint32_t(quarter) * EPI_NB * EPI_BYTES;
+        int i = 0, e = 0;
         for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
             const int mx = t % MX, nw = t / MX;
-            if (!mbar_wait_bounded(&ctl->tmem_full, i & 1, wait_ns, status)) *abort_flag = 1;
+            const int a = i & 1;
+            if (!mbar_wait_bounded(&ctl->tmem_full[a], (i >> 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             tc_fence_after();
-            const int col = nw * BW + quarter * 32 + lane;
-            const bool cvalid = col < N;
+            const int col0 = nw * BW + quarter * 32;
+            const int col = col0 + lane;
             for (int c = 0; c < BX / 32; ++c) {
                 uint32_t r[32];
-                tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + ACC_COL + uint32_t(c * 32), r);
+                tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + ACC_COL + uint32_t(a) * BX +
+                              uint32_t(c * 32),
+                          r);
                 tc_wait_ld();
                 if (c == BX / 32 - 1) {
                     tc_fence_before();
-                    mbar_arrive(&ctl->tmem_empty);
+                    mbar_arrive(&ctl->tmem_empty[a]);
                 }
                 const int row0 = mx * BX + c * 32;
-                if (!cvalid) continue;
+                if (row0 >= M || col0 >= N) continue;  // block wholly outside the output
+                if (epi_mode == EPI_DIRECT) {
+                    if (col >= N) continue;
 #pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const int row = row0 + j;
-                    if (row >= M) break;
-                    const int64_t o = int64_t(row) * N + col;
-                    float v = __uint_as_float(r[j]);
-                    if (residual) v += residual[o];
-                    out[o] = v;
+                    for (int j = 0; j < 32; ++j) {
+                        const int row = row0 + j;
+                        if (row >= M) break;
+                        const int64_t o = int64_t(row) * N + col;
+                        float v = __uint_as_float(r[j]);
+                        if (residual) v += residual[o];
+                        out[o] = v;
+                    }
+                } else {
+                    // Stage the 32 x 32 block (row j, column lane) and hand it
+                    // to the tensor engine; rows >= M and columns >= N of the
+                    // box are clipped by the tensor map.
+                    const uint32_t buf = ebuf + uint32_t(e % EPI_NB) * EPI_BYTES;
+                    if (lane == 0) bulk_wait_read_nb();  // the store that last used buf has read it
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        asm volatile("st.shared.b32 [%0], %1;" ::"r"(buf + uint32_t(j) * 128 + uint32_t(lane) * 4),
+                                     "r"(r[j])
+                                     : "memory");
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (epi_mode == EPI_TMA_ADD)
+                            tma_add_2d(&omap, col0, row0, buf);
+                        else
+                            tma_store_2d(&omap, col0, row0, buf);
+                        bulk_commit();
+                    }
+                    ++e;
                 }
             }
         }
+        // every tensor store must have finished before the CTA's shared memory goes away
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
     }
 
     tc_fence_before();
@@ -547,6 +589,21 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
             estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
+    // Output tensor map for the TMA epilogue: needs a 16-byte row pitch (n % 4
+    // == 0; the base is 16-byte aligned by the API's checks) and either no
+    // residual or an in-place residual (reduce-add into out).
+    int epi_mode = EPI_DIRECT;
+    CUtensorMap omap;
+    std::memset(&omap, 0, sizeof(omap));
+    if (n % 4 == 0 && (residual == nullptr || residual == out)) {
+        const cuuint64_t odim[2] = {cuuint64_t(n), cuuint64_t(m)};
+        const cuuint64_t ostride[1] = {cuuint64_t(n) * 4};
+        const cuuint32_t obox[2] = {32, 32};
+        if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, odim, ostride, obox, estride,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+            epi_mode = residual ? EPI_TMA_ADD : EPI_TMA_STORE;
+    }
     // pre-pass
     const int MT = int((m + BM - 1) / BM);
     const int64_t items = int64_t(MT) * BM * (k / 16);
@@ -561,8 +618,8 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
     const int64_t ntiles = ((m + BX - 1) / BX) * ((n + BW - 1) / BW);
     const int64_t grid = std::min<int64_t>(ntiles, ctx.num_sms);
     tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
-        qmap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
-        ctx.status, ctx.wait_ns);
+        qmap, omap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
+        epi_mode, ctx.status, ctx.wait_ns);
     return cudaPeekAtLastError();
 }
 

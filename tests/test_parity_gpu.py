@@ -312,6 +312,17 @@ def test_ws_inplace_and_repeat(tq2):
     assert np.array_equal(a, b)  # deterministic
 
 
+@pytest.mark.parametrize("m,n,k", [(300, 100, 640), (129, 36, 128), (513, 1028, 256), (77, 4, 384)])
+def test_ws_inplace_ragged(tq2, m, n, k):
+    # in-place residual with a 16-byte row pitch: the reduce-add epilogue,
+    # including boxes clipped at the M and N edges
+    p = tq2_synth.make_problem(m, n, k, seed=3 * m + n, residual=True)
+    w = upload(tq2, p)
+    eff = tq2.tq2_select_kernel(m, n, k)
+    check(run_ws(tq2, w, p, inplace=True), p, tol_for(tq2, eff),
+          cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16), what=f"ws in-place {m}x{n}x{k}")
+
+
 @pytest.mark.parametrize("n", tq2_synth.DIT_NS)
 def test_ws_dit_large_m(tq2, n):
     p = tq2_synth.dit(n)
