@@ -11,8 +11,11 @@
 //  * Pre-pass: x f32 [M,K] -> f16 tiles of 128 rows x 64 k (16 KB each), laid
 //    out exactly as the MMA's K-major SWIZZLE_128B shared-memory image, with
 //    the K permutation that matches the weight decode (pairs (i, i+8) of every
-//    16-wide group).  Rows past M are zero.  Two tiles (256 x rows) move per
-//    pipeline stage with cp.async.bulk: the MMA's B operand.
+//    16-wide group).  Rows past M are zero.  Two tiles (256 x rows) form the
+//    MMA's B operand of a pipeline stage.  CTAs run in clusters of two that
+//    work on neighbouring weight tiles of the same x rows: each CTA copies
+//    one of the two tiles with a multicast cp.async.bulk into both CTAs'
+//    shared memory, which halves the L2 traffic for x.
 //  * Weight codes: a 2-D TMA load of the qs plane (128 rows x 16 bytes per
 //    stage).  Decoder threads each turn one row's 64 codes into (c - 1) * d
 //    in f16 registers and store them as the A operand (128 rows x 64 k, the
@@ -21,7 +24,7 @@
 //    operands in shared memory (the tensor core's full rate), f32
 //    accumulation in tensor memory.  TMEM holds two 256-column accumulators,
 //    so the epilogue of one output tile (256 x rows x 128 weight rows)
-//    overlaps the MMAs of the next.  Persistent CTAs walk the tiles.
+//    overlaps the MMAs of the next.  Persistent clusters walk pairs of tiles.
 //  * Epilogue: TMEM lane = output column, so each tcgen05.ld gives a warp 32
 //    consecutive output columns of 32 output rows.  The warp stages that
 //    32 x 32 block in shared memory and hands it to a TMA tensor store (or a
@@ -75,8 +78,7 @@ constexpr uint32_t ACC_COL = 0;          // two f32 accumulators of BX columns
 constexpr uint32_t IDESC = (1u << 4) | (uint32_t(BX >> 3) << 17) | (uint32_t(BW >> 4) << 24);
 
 struct Ctl {
-    uint64_t x_full[STAGES];
-    uint64_t a_full[STAGES];
+    uint64_t full[STAGES];   // x tile landed (tx bytes + issuer arrival) and A decoded (decoder arrivals)
     uint64_t empty[STAGES];
     uint64_t codes_full[CSTAGES];
     uint64_t codes_empty[CSTAGES];
@@ -115,13 +117,35 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
                  : "memory");
 }
 
-__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes,
-                                         uint64_t *bar) {
+// Bulk copy into the same shared-memory offset of every CTA in `mask`; each
+// destination's mbarrier at `bar`'s offset receives the byte count.
+__device__ __forceinline__ void bulk_g2s_mc(uint32_t dst, const void *src, uint32_t bytes,
+                                            uint64_t *bar, uint16_t mask) {
     asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(dst),
-        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "h"(mask)
         : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
+// prior tcgen05 operations of this thread have completed.
+__device__ __forceinline__ void tc_commit_mc(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -240,7 +264,7 @@ x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, 
 // --------------------------------------------------------------------------
 // Main kernel.
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
              const __half *__restrict__ dpl, const uint8_t *__restrict__ xtiles, const float *residual,
              float *out, int M, int N, int K, int epi_mode, unsigned int *status, uint64_t wait_ns) {
@@ -256,14 +280,17 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
     const int MT = (M + BM - 1) / BM;           // 128-row x tiles in the workspace
     const int MX = (M + BX - 1) / BX;           // 256-row output tiles
     const int NW = (N + BW - 1) / BW;
-    const int ntiles = MX * NW;
+    // Tiles are walked in pairs (mx, 2*nwp + rank) by clusters of two CTAs.
+    const int rank = int(cluster_rank());
+    const int cl = int(blockIdx.x) >> 1, ncl = int(gridDim.x) >> 1;
+    const int ntiles = MX * ((NW + 1) / 2);
+    const uint16_t pair_mask = 0x3;
     const int64_t kb = K / kBlockW;
 
     if (tid == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&ctl->x_full[s], 1);
-            mbar_init(&ctl->a_full[s], NUM_DEC);
-            mbar_init(&ctl->empty[s], 1);
+            mbar_init(&ctl->full[s], NUM_DEC + 1);
+            mbar_init(&ctl->empty[s], 2);  // released by the MMAs of both CTAs of the pair
         }
         for (int s = 0; s < CSTAGES; ++s) {
             mbar_init(&ctl->codes_full[s], 1);
@@ -275,6 +302,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
+        fence_mbarrier_init();  // visible to the peer's multicast copies and commits
         fence_proxy_async_smem();
     }
     if (warp == MMA_WARP) {
@@ -282,7 +310,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    // the peer multicasts into this CTA's barriers: both must be initialised
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     volatile int *abort_flag = &ctl->abort;
@@ -297,7 +326,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
 
     if (warp == TMA_WARP || warp == X_WARP) {
         // Two independent copy streams: weight codes into their own ring
-        // (warp 0), pre-converted x tiles into the operand ring (warp 2).
+        // (warp 0), this CTA's half of the x tiles into both CTAs' operand
+        // rings (warp 2).
         const bool codes = warp == TMA_WARP;
         const int depth = codes ? CSTAGES : STAGES;
         if (lane == 0) {
@@ -307,8 +337,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             int last_round[STAGES > CSTAGES ? STAGES : CSTAGES];
             for (int s = 0; s < depth; ++s) last_round[s] = -1;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x) {
-                const int mx = t % MX, nw = t / MX;
+            for (int t = cl; t < ntiles && ok; t += ncl) {
+                const int mx = t % MX, nw = 2 * (t / MX) + rank;
                 const int mt0 = 2 * mx, nmt = min(2, MT - mt0);  // 128-row x tiles of this output tile
                 for (int kt = 0; kt < KT; ++kt, ++g) {
                     const int s = int(g % depth);
@@ -324,21 +354,40 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                         mbar_expect_tx(&ctl->codes_full[s], C_BYTES);
                         tma_2d(stage_c(s), &qmap, kt * (BK / 4), nw * BW, &ctl->codes_full[s]);
                     } else {
-                        mbar_expect_tx(&ctl->x_full[s], uint32_t(nmt) * A_BYTES);
-                        for (int h = 0; h < nmt; ++h)
-                            bulk_g2s(stage_x(s) + uint32_t(h) * A_BYTES,
-                                     xtiles + (int64_t(mt0 + h) * KT + kt) * A_BYTES, A_BYTES,
-                                     &ctl->x_full[s]);
+                        // lane 0 arrives with the byte count of both halves; the
+                        // CTA of rank h copies half h into both CTAs.  A half
+                        // may land before that arrival (the transaction count
+                        // goes transiently negative; the phase cannot complete
+                        // without the arrival).
+                        if (lane == 0) {
+                            mbar_expect_tx(&ctl->full[s], uint32_t(nmt) * A_BYTES);
+                            if (rank < nmt)
+                                bulk_g2s_mc(stage_x(s) + uint32_t(rank) * A_BYTES,
+                                            xtiles + (int64_t(mt0 + rank) * KT + kt) * A_BYTES, A_BYTES,
+                                            &ctl->full[s], pair_mask);
+                        }
                     }
                     last_round[s] = u;
                 }
             }
-            // Drain: every copy this thread issued must land before the CTA exits.
-            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
-            for (int s = 0; s < depth; ++s) {
-                if (last_round[s] < 0) continue;
-                mbar_wait_bounded(codes ? &ctl->codes_full[s] : &ctl->x_full[s], last_round[s] & 1,
-                                  drain, status);
+            // Drain: every copy issued into shared memory must land before the
+            // CTAs exit.  Code copies are awaited on their own barriers.  On
+            // the normal path every x stage was consumed by both CTAs' MMAs,
+            // so all x copies have landed; after an abort the stages may never
+            // complete, so the issuer gives its copies in flight (a few
+            // microseconds each) a fixed 200 us.  Both CTAs leave through a
+            // cluster barrier, so the peer's copies into this CTA are covered
+            // by the peer's own drain.
+            if (codes) {
+                const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+                for (int s = 0; s < depth; ++s) {
+                    if (last_round[s] < 0) continue;
+                    mbar_wait_bounded(&ctl->codes_full[s], last_round[s] & 1, drain, status);
+                }
+            } else if (!ok || *abort_flag) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 200000ull) {
+                }
             }
         }
         __syncwarp();
@@ -347,7 +396,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             int64_t g = 0;
             int i = 0;
             bool ok = true;
-            for (int t = blockIdx.x; t < ntiles && ok; t += gridDim.x, ++i) {
+            for (int t = cl; t < ntiles && ok; t += ncl, ++i) {
                 const int a = i & 1;
                 // accumulator a was last used by tile i - 2: wait for its epilogue
                 if (i >= 2 && !mbar_wait_bounded(&ctl->tmem_empty[a], ((i >> 1) - 1) & 1, wait_ns, status)) {
@@ -359,8 +408,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 for (int kt = 0; kt < KT; ++kt, ++g) {
                     const int s = int(g % STAGES);
                     const uint32_t par = uint32_t(g / STAGES) & 1;
-                    if (!mbar_wait_bounded(&ctl->x_full[s], par, wait_ns, status) ||
-                        !mbar_wait_bounded(&ctl->a_full[s], par, wait_ns, status)) {
+                    if (!mbar_wait_bounded(&ctl->full[s], par, wait_ns, status)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -372,7 +420,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
                         tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kt | kk) != 0);
-                    tc_commit(&ctl->empty[s]);
+                    tc_commit_mc(&ctl->empty[s], pair_mask);
                 }
                 if (ok) tc_commit(&ctl->tmem_full[a]);
             }
@@ -384,8 +432,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         const uint32_t rsw = uint32_t(pr & 7);     // SWIZZLE_128B phase of this row
         const uint32_t rbase = uint32_t(pr >> 3) * 1024 + rsw * 128;
         int64_t gbase = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, gbase += KT) {
-            const int nw = t / MX;
+        for (int t = cl; t < ntiles; t += ncl, gbase += KT) {
+            const int nw = 2 * (t / MX) + rank;
             const int row = nw * BW + pr;
             const bool rvalid = row < N;
             const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
@@ -411,6 +459,14 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                                  : "r"(stage_c(cs) + uint32_t(pr) * 16)
                                  : "memory");
                 mbar_arrive(&ctl->codes_empty[cs]);
+                // decode into registers first, then wait for the slot
+                const __half2 d2 =
+                    __half2half2(__ushort_as_half(static_cast<unsigned short>(rvalid ? dbits : 0u)));
+                uint32_t o[4][8];
+                decode_word(code.x, d2, o[0]);
+                decode_word(code.y, d2, o[1]);
+                decode_word(code.z, d2, o[2]);
+                decode_word(code.w, d2, o[3]);
                 // the A slot is free once the MMAs of its previous round completed
                 const int u = int(g / STAGES);
                 if (!stop && u > 0 && !mbar_wait_bounded(&ctl->empty[s], (u - 1) & 1, wait_ns, status)) {
@@ -418,25 +474,20 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     stop = true;
                 }
                 if (stop || *abort_flag) break;
-                const __half2 d2 =
-                    __half2half2(__ushort_as_half(static_cast<unsigned short>(rvalid ? dbits : 0u)));
                 // word w (k 16w..16w+15 of the stage) -> 16-byte chunks 2w, 2w+1 of the row
                 const uint32_t wbase = stage_w(s) + rbase;
-                const uint32_t cw[4] = {code.x, code.y, code.z, code.w};
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
-                    uint32_t o[8];
-                    decode_word(cw[w], d2, o);
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wbase + (((2 * w) ^ rsw) << 4)),
-                                 "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                 "r"(o[w][0]), "r"(o[w][1]), "r"(o[w][2]), "r"(o[w][3])
                                  : "memory");
                     asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(wbase + (((2 * w + 1) ^ rsw) << 4)),
-                                 "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                 "r"(o[w][4]), "r"(o[w][5]), "r"(o[w][6]), "r"(o[w][7])
                                  : "memory");
                 }
                 // make the generic-proxy stores visible to the tensor core
                 fence_proxy_async_smem();
-                mbar_arrive(&ctl->a_full[s]);
+                mbar_arrive(&ctl->full[s]);
             }
             if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
         }
@@ -444,8 +495,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         const int quarter = warp - EPI_WARP0;  // TMEM lanes 32*quarter .. +31 = output columns
         const uint32_t ebuf = ebase + uint32_t(quarter) * EPI_NB * EPI_BYTES;
         int i = 0, e = 0;
-        for (int t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-            const int mx = t % MX, nw = t / MX;
+        for (int t = cl; t < ntiles; t += ncl, ++i) {
+            const int mx = t % MX, nw = 2 * (t / MX) + rank;
             const int a = i & 1;
             if (!mbar_wait_bounded(&ctl->tmem_full[a], (i >> 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -519,6 +570,9 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    // The peer may still arrive on this CTA's barriers until its own MMAs
+    // have drained: leave together.
+    cluster_sync();
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -615,8 +669,9 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
     e = cudaFuncSetAttribute(tc_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = ((m + BX - 1) / BX) * ((n + BW - 1) / BW);
-    const int64_t grid = std::min<int64_t>(ntiles, ctx.num_sms);
+    // clusters of two CTAs, each cluster a pair of neighbouring weight tiles
+    const int64_t ntiles = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2);
+    const int64_t grid = 2 * std::min<int64_t>(ntiles, ctx.num_sms / 2);
     tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
         qmap, omap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
         epi_mode, ctx.status, ctx.wait_ns);
