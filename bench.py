@@ -242,7 +242,12 @@ def run_ours(args, world, rank, local, pg):
     gt = graph_of(step, args.steps, torch)
     gw.replay()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
+    smi_id = str(local)
+    try:  # nvidia-smi numbers GPUs physically; the CUDA ordinal may differ
+        smi_id = "GPU-" + str(props.uuid)
+    except Exception:
+        pass
+    with ClockSampler(smi_id) as clk:
         # sustained window for the clock record (same graph, >= 1 s of load)
         t_end = time.time() + (0.0 if args.no_clock_window else 1.0)
         while time.time() < t_end:
@@ -294,7 +299,7 @@ def run_ours(args, world, rank, local, pg):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 (exact f32 products, f32 accumulation)",
+        "dtype": "f32 in/out; x as 23-bit fixed point per 64-weight segment, int32 (dp4a) ternary dot products, f32 scale and sum",
         "data": "synthetic (seeded numpy: x~N(0,1), codes P(0)=0.4 P(+-1)=0.3, d=f16(|N(0,0.02)|+1e-4))",
         "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288,
                    "weight_bytes": wbytes, "kernel": "tq2_gemv",
@@ -337,9 +342,14 @@ def run_ours(args, world, rank, local, pg):
                 tq2.tq2_gemm_ws(wl[i % c], xl[i % c], None, ol[i % c], q.m, q.n, q.k, wsl[i % c],
                                 wsl[i % c].numel())
 
+            def gstep_direct(i, q=q, wl=wl, xl=xl, ol=ol, c=c):
+                tq2.tq2_gemm_with(tq2.TQ2_KERNEL_TC_DIRECT, wl[i % c], xl[i % c], None, ol[i % c],
+                                  q.m, q.n, q.k)
+
             flops = 2.0 * q.m * q.n * q.k
             res = {}
-            for name, fn in (("tq2_gemm", gstep), ("tq2_gemm_ws", gstep_ws)):
+            kernels_per_call = {"tq2_gemm": 2, "tq2_gemm_ws": 2, "tc_direct": 1}
+            for name, fn in (("tq2_gemm", gstep), ("tq2_gemm_ws", gstep_ws), ("tc_direct", gstep_direct)):
                 for i in range(3):
                     fn(i)
                 torch.cuda.synchronize()
@@ -348,22 +358,25 @@ def run_ours(args, world, rank, local, pg):
                 gg.replay()
                 torch.cuda.synchronize()
                 tg = time_graph(gg, torch, pg, device, reps=3) / args.gemm_steps
-                launches += args.gemm_steps * (1 if name == "tq2_gemm" else 2)
+                launches += args.gemm_steps * kernels_per_call[name]
                 res[name] = (tg, flops / tg / 1e12)
-            tg, tfl = res["tq2_gemm_ws"]
-            gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "entry": "tq2_gemm_ws",
+            tg, tfl = res["tq2_gemm"]
+            gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "entry": "tq2_gemm",
                              "us_per_call": round(tg * 1e6, 2),
                              "tflops": round(tfl, 1), "frac_of_bf16_burst": round(tfl / bf16, 4),
                              "frac_of_bf16_sustained": round(tfl / bf16s, 4),
-                             "tq2_gemm_no_workspace": {"us_per_call": round(res["tq2_gemm"][0] * 1e6, 2),
-                                                       "tflops": round(res["tq2_gemm"][1], 1)},
+                             "tq2_gemm_ws": {"us_per_call": round(res["tq2_gemm_ws"][0] * 1e6, 2),
+                                             "tflops": round(res["tq2_gemm_ws"][1], 1)},
+                             "tc_direct": {"us_per_call": round(res["tc_direct"][0] * 1e6, 2),
+                                           "tflops": round(res["tc_direct"][1], 1)},
                              "l2": f"{c} rotating (x, w, out) copies"}
             del wl, xl, ol, wq, wsl
             torch.cuda.empty_cache()
         top = gemm[f"n{max(int(k[1:]) for k in gemm)}"]
         line["gemm_m1536"] = {
-            "kernel": "tq2_gemm_ws -> x f16-tile pre-pass + persistent tcgen05 kind::f16 kernel "
-                      "(f16 operands, f32 accumulation in TMEM); tq2_gemm (in-kernel conversion) alongside",
+            "kernel": "tq2_gemm -> x f16-tile pre-pass into a stream-ordered temporary + clustered "
+                      "persistent tcgen05 kind::f16 kernel (f16 operands, f32 accumulation in TMEM); "
+                      "tq2_gemm_ws (caller workspace) and tc_direct (in-kernel x conversion) alongside",
             "per_n": gemm,
             "roofline": {"bound": "tensor", "unit": "TFLOP/s",
                          "achieved": top["tflops"], "peak": bf16,

@@ -177,7 +177,7 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
     if (kernel == TQ2_KERNEL_AUTO) kernel = tq2_select_kernel(m, n, k);
     if (kernel == TQ2_KERNEL_GEMV && m != 1) return TQ2_ERR_INVALID_ARG;
     if (kernel == TQ2_KERNEL_SKINNY && m > tq2::kSkinnyMaxM) return TQ2_ERR_INVALID_ARG;
-    if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_F32REF) return TQ2_ERR_INVALID_ARG;
+    if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_TC_DIRECT) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
     st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
     if (st != TQ2_OK) return st;
@@ -185,7 +185,20 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
         case TQ2_KERNEL_GEMV: return finish(tq2::launch_gemv(w_soa, x, residual, out, n, k, ctx));
         case TQ2_KERNEL_SKINNY:
             return finish(tq2::launch_skinny(w_soa, x, residual, out, m, n, k, ctx));
-        case TQ2_KERNEL_TC: return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
+        case TQ2_KERNEL_TC: {
+            // x -> f16 tiles in a stream-ordered temporary, then the clustered
+            // kernel; without the temporary, the kernel that converts x itself
+            void *ws = nullptr;
+            if (cudaMallocAsync(&ws, tq2::tc_ws_bytes(m, k), ctx.stream) == cudaSuccess) {
+                const cudaError_t e = tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, ws, ctx);
+                const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
+                return finish(e != cudaSuccess ? e : f);
+            }
+            (void)cudaGetLastError();  // the failed allocation is not an error of the call
+            return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
+        }
+        case TQ2_KERNEL_TC_DIRECT:
+            return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
         default: return finish(tq2::launch_f32ref(w_soa, x, residual, out, m, n, k, ctx));
     }
 }

@@ -79,8 +79,12 @@ typedef enum {
     TQ2_KERNEL_AUTO = 0,
     TQ2_KERNEL_GEMV = 1,   /* M == 1 only: f32 CUDA-core decode GEMV */
     TQ2_KERNEL_SKINNY = 2, /* small M: f32 CUDA-core kernel, weights decoded once per M rows */
-    TQ2_KERNEL_TC = 3,     /* tcgen05 tensor-core kernel: f16 operands, f32 accumulation in TMEM */
-    TQ2_KERNEL_F32REF = 4  /* exact-f32 CUDA-core tiled kernel */
+    TQ2_KERNEL_TC = 3,     /* tcgen05 tensor-core path: x converted once to f16 tiles in a
+                              stream-ordered temporary, then the clustered kernel; f16
+                              operands, f32 accumulation in TMEM */
+    TQ2_KERNEL_F32REF = 4, /* exact-f32 CUDA-core tiled kernel */
+    TQ2_KERNEL_TC_DIRECT = 5 /* tcgen05 kernel that converts x itself (no temporary memory);
+                                same arithmetic as TQ2_KERNEL_TC */
 } tq2_kernel;
 
 /* Bytes of a weight of n rows and k columns in either layout: n*(k/128)*34.
@@ -127,7 +131,13 @@ int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *ou
  * Arithmetic: the tensor-core kernel rounds x to binary16 (round to nearest
  * even; |x| must stay below 65504) and multiplies by the exactly representable
  * binary16 weights (c-1)*d with f32 accumulation; the CUDA-core kernels use
- * exact f32 products and f32 accumulation. */
+ * exact f32 products and f32 accumulation.
+ * Memory: on the tensor-core path the call takes a temporary of
+ * tq2_gemm_workspace_bytes(m,n,k) bytes from the device's default memory pool,
+ * ordered on `stream` (cudaMallocAsync, released by cudaFreeAsync on the same
+ * stream; both are legal inside stream capture).  If that allocation fails it
+ * runs TQ2_KERNEL_TC_DIRECT instead, which needs no temporary.  Callers that
+ * manage memory themselves use tq2_gemm_ws or tq2_gemm_noalloc. */
 int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t m, int64_t n, int64_t k, void *stream);
 
@@ -187,8 +197,9 @@ int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, f
                      int64_t m, int64_t n, int64_t k, void *stream);
 
 /* tq2_gemm with an explicit kernel choice (a tq2_kernel value), for
- * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 (else
- * TQ2_ERR_INVALID_ARG). */
+ * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 and
+ * TQ2_KERNEL_SKINNY m <= 16 (else TQ2_ERR_INVALID_ARG).  TQ2_KERNEL_TC
+ * allocates as tq2_gemm does. */
 int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *residual,
                   float *out, int64_t m, int64_t n, int64_t k, void *stream);
 

@@ -100,6 +100,8 @@ def test_argument_errors_are_returned_before_any_launch(tq2):
     assert rc_gemm(tq2, W, X, None, O, 2, 4, 128, tq2.TQ2_KERNEL_GEMV) == tq2.TQ2_ERR_INVALID_ARG
     assert rc_gemm(tq2, W, X, None, O, 17, 4, 128, tq2.TQ2_KERNEL_SKINNY) == tq2.TQ2_ERR_INVALID_ARG
     assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 9) == tq2.TQ2_ERR_INVALID_ARG
+    assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 6) == tq2.TQ2_ERR_INVALID_ARG
+    assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, -1) == tq2.TQ2_ERR_INVALID_ARG
 
 
 def test_workspace_size_and_errors(tq2):

@@ -30,7 +30,7 @@ def tq2():
 
 
 def tol_for(tq2, kernel):
-    return TOL_TC if kernel == tq2.TQ2_KERNEL_TC else TOL_F32
+    return TOL_TC if kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT) else TOL_F32
 
 
 def upload(tq2, p):
@@ -157,7 +157,7 @@ def test_gemv_quantisation_bound_with_wide_dynamic_range(tq2):
 # ---------------------------------------------------------------------------
 # all kernels on the small configuration and on ragged shapes
 
-KERNELS = ["TQ2_KERNEL_TC", "TQ2_KERNEL_F32REF", "TQ2_KERNEL_SKINNY"]
+KERNELS = ["TQ2_KERNEL_TC", "TQ2_KERNEL_TC_DIRECT", "TQ2_KERNEL_F32REF", "TQ2_KERNEL_SKINNY"]
 
 
 @pytest.mark.parametrize("kname", KERNELS)
@@ -166,7 +166,7 @@ def test_small_config_each_kernel(tq2, kname, residual):
     p = tq2_synth.make_problem(8, 1024, 1024, seed=0, residual=residual)
     w = upload(tq2, p)
     kernel = getattr(tq2, kname)
-    check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), cos=kernel == tq2.TQ2_KERNEL_TC,
+    check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), cos=tol_for(tq2, kernel) == TOL_TC,
           what=kname)
 
 
@@ -183,7 +183,7 @@ def test_ragged_shapes(tq2, m, n, k, kname):
     w = upload(tq2, p)
     eff = tq2.tq2_select_kernel(m, n, k) if kernel == tq2.TQ2_KERNEL_AUTO else kernel
     out = run(tq2, kernel, w, p)
-    check(out, p, tol_for(tq2, eff), cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16),
+    check(out, p, tol_for(tq2, eff), cos=(tol_for(tq2, eff) == TOL_TC and n >= 16),
           what=f"{kname} {m}x{n}x{k}")
 
 
@@ -201,7 +201,8 @@ def test_code3_decodes_to_plus_two_everywhere(tq2):
     p = tq2_synth.make_problem(m, n, k, seed=3)
     p.w_aos[:, :, :32] = 0xFF
     w = upload(tq2, p)
-    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_F32REF, tq2.TQ2_KERNEL_SKINNY):
+    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT, tq2.TQ2_KERNEL_F32REF,
+                   tq2.TQ2_KERNEL_SKINNY):
         check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), what=f"code3 {kernel}")
     p1 = tq2_synth.make_problem(1, n, k, seed=3)
     p1.w_aos[:] = p.w_aos
@@ -213,7 +214,7 @@ def test_zero_weights_give_residual(tq2):
     p = tq2_synth.make_problem(m, n, k, seed=9, residual=True)
     p.w_aos[:, :, :32] = 0x55
     w = upload(tq2, p)
-    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_F32REF):
+    for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT, tq2.TQ2_KERNEL_F32REF):
         out = run(tq2, kernel, w, p)
         assert np.array_equal(out, p.residual), kernel
 
@@ -222,7 +223,7 @@ def test_empty_problems_are_noops(tq2):
     w = torch.zeros(34, dtype=torch.uint8, device="cuda")
     x = torch.zeros(128, device="cuda")
     out = torch.full((4,), 7.0, device="cuda")
-    for kernel in (0, 1, 2, 3, 4):
+    for kernel in (0, 1, 2, 3, 4, 5):
         tq2.tq2_gemm_with(kernel, w, x, None, out, 0, 1, 128)
         tq2.tq2_gemm_with(kernel, w, x, None, out, 1, 0, 128)
     torch.cuda.synchronize()
@@ -256,6 +257,13 @@ def test_dit_large_m_tc(tq2, n):
     out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
     assert tq2.tq2_select_kernel(p.m, p.n, p.k) == tq2.TQ2_KERNEL_TC
     check(out, p, TOL_TC, rows=sample_rows(p.m), cos=True, what=f"dit n={n}")
+
+
+def test_dit_large_m_tc_direct(tq2):
+    p = tq2_synth.dit(3072)
+    w = upload(tq2, p)
+    out = run(tq2, tq2.TQ2_KERNEL_TC_DIRECT, w, p)
+    check(out, p, TOL_TC, rows=sample_rows(p.m), cos=True, what="dit n=3072 tc_direct")
 
 
 def test_dit_large_m_f32ref(tq2):
@@ -349,19 +357,21 @@ def test_ws_skinny(tq2, m):
 # bounded device waits
 
 
-def test_wait_timeout_is_reported_and_context_survives(tq2):
+@pytest.mark.parametrize("kname", ["TQ2_KERNEL_TC", "TQ2_KERNEL_TC_DIRECT"])
+def test_wait_timeout_is_reported_and_context_survives(tq2, kname):
+    kernel = getattr(tq2, kname)
     p = tq2_synth.make_problem(128, 256, 2048, seed=1)
     w = upload(tq2, p)
     assert tq2.tq2_device_status() == tq2.TQ2_OK
     old = tq2.tq2_set_wait_timeout_ns(0)
     try:
-        run(tq2, tq2.TQ2_KERNEL_TC, w, p)
+        run(tq2, kernel, w, p)
         st = tq2.tq2_device_status()
     finally:
         tq2.tq2_set_wait_timeout_ns(old)
     assert st == tq2.TQ2_ERR_TIMEOUT
     assert tq2.tq2_device_status() == tq2.TQ2_OK  # cleared by the read
-    check(run(tq2, tq2.TQ2_KERNEL_TC, w, p), p, TOL_TC, cos=True, what="after timeout")
+    check(run(tq2, kernel, w, p), p, TOL_TC, cos=True, what="after timeout")
     assert tq2.tq2_device_status() == tq2.TQ2_OK
 
 
