@@ -259,6 +259,7 @@ constexpr int kGvChunk = 2048;  // weights per warp-chunk (32 lanes x 64)
 // shared memory and are summed per row at the end (plus the residual).
 
 constexpr int kSegWords = 52;  // 48 limb words per segment, padded (conflict-free 16-byte reads)
+constexpr int kGvQuantPasses = 4;  // x quantisation items per thread: 4 x 1024 x 4 values = K <= 16384
 
 __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint32_t bytes,
                                             uint64_t *bar) {
@@ -291,7 +292,7 @@ struct GvsParams {
     int n, k, C;       // rows, K, 2048-weight chunks per row
     int rbase, rextra; // CTA b owns rbase (+1 if b < rextra) rows starting at b*rbase + min(b, rextra)
     // shared-memory offsets (bytes), computed on the host
-    uint32_t off_x, off_limbs, off_scale, off_sum, off_d, off_partial, off_bar;
+    uint32_t off_limbs, off_scale, off_sum, off_d, off_partial, off_bar;
     int rs;            // rows per stage
     int ns;            // ring slots
     int consumers;     // consumer warps = groups * C
@@ -314,9 +315,11 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
     const int R0 = b * P.rbase + min(b, P.rextra);
     const int rows = P.rbase + (b < P.rextra ? 1 : 0);
     const int nstages = (rows + P.rs - 1) / P.rs;
-    const uint32_t stage_bytes = uint32_t(P.rs * kq);
+    const bool dbulk = (kb % 8) == 0;  // row scales travel with their stage (16-byte multiples)
+    const uint32_t code_bytes = uint32_t(P.rs * kq);
+    const uint32_t stage_bytes = code_bytes + (dbulk ? uint32_t(P.rs * kb * 2) : 0u);
 
-    // shared memory: [ring][raw x][limbs][seg scale][seg sum X][d rows][partials][barriers]
+    // shared memory: [ring][limbs][seg scale][seg sum X][d rows][partials][barriers]
     uint8_t *ring = gvs_smem;
     uint32_t *limbs = reinterpret_cast<uint32_t *>(gvs_smem + P.off_limbs);
     float *sscale = reinterpret_cast<float *>(gvs_smem + P.off_scale);
@@ -324,10 +327,31 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
     __half *dsm = reinterpret_cast<__half *>(gvs_smem + P.off_d);
     float *partial = reinterpret_cast<float *>(gvs_smem + P.off_partial);
     uint64_t *full = reinterpret_cast<uint64_t *>(gvs_smem + P.off_bar);
-    uint64_t *empty = full + P.ns + 2;  // full[P.ns]: the x copy, full[P.ns + 1]: the scale copy
+    uint64_t *empty = full + P.ns;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + P.ns);
     const uint32_t ring_addr = smem_u32(ring);
-    float *xraw = reinterpret_cast<float *>(gvs_smem + P.off_x);
+
+    // x first: every thread loads the four elements it quantises below, before
+    // the weight stream is requested, so that x is not queued behind it.
+    // Thread (segment, word q, group t) owns the four weights 16q + 4m + t
+    // (m = 0..3) of its segment -- exactly the bytes of its three limb words.
+    // (Warp 0 loads after initialising the barriers: the proxy fence there
+    // would otherwise wait for its loads.)
+    const int nthr = nseg * 16;  // 16 threads per segment; blockDim.x is a multiple of 16
+    float xe[kGvQuantPasses][4];  // pass p: item threadIdx.x + p * blockDim.x (the host bounds nthr)
+    auto load_x = [&]() {
+#pragma unroll
+        for (int p = 0; p < kGvQuantPasses; ++p) {
+            const int qi = int(threadIdx.x) + p * int(blockDim.x);
+            const int qseg = qi >> 4, qq = (qi >> 2) & 3, qt = qi & 3;
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                const int kk = qseg * 64 + 16 * qq + 4 * mm + qt;
+                xe[p][mm] = (qi < nthr && kk < k) ? __ldg(x + kk) : 0.f;
+            }
+        }
+    };
+    if (warp != 0) load_x();
 
     // barriers: the lanes of warp 0 initialise them in parallel
     if (warp == 0) {
@@ -335,59 +359,40 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 32 * C);
         }
-        if (lane == 0) {
-            mbar_init(&full[P.ns], 1);
-            mbar_init(&full[P.ns + 1], 1);
-            *abort_flag = 0;
-        }
+        if (lane == 0) *abort_flag = 0;
         fence_proxy_async_smem();   // the inits are visible to the copy engine
+        load_x();
     }
     __syncthreads();
-    const bool dbulk = (kb % 8) == 0;
-    if (threadIdx.x == 0) {
-        const uint32_t xbytes = uint32_t(k) * 4;
-        const uint32_t dbytes = (dbulk && rows > 0) ? uint32_t(int64_t(rows) * kb * 2) : 0u;
-        mbar_expect_tx_gv(&full[P.ns], xbytes);
-        bulk_g2s_gv(smem_u32(xraw), x, xbytes, &full[P.ns]);
-        if (dbytes) {
-            mbar_expect_tx_gv(&full[P.ns + 1], dbytes);
-            bulk_g2s_gv(smem_u32(dsm), dpl + int64_t(R0) * kb, dbytes, &full[P.ns + 1]);
-        }
-    }
     // ---- producer warp, part 1: the first ring-full of stages needs no slot to
     // free up; its 32 lanes issue those copies in parallel
     const bool producer = warp == consumers && lane == 0;
     const uint8_t *src = qs + int64_t(R0) * kq;
+    const __half *dsrc_rows = dpl + int64_t(R0) * kb;
     auto issue = [&](int st) {
         const int slot = st % P.ns;
         const int r = min(P.rs, rows - st * P.rs);
         const uint32_t bytes = uint32_t(r * kq);
-        mbar_expect_tx_gv(&full[slot], bytes);
-        bulk_g2s_gv(ring_addr + uint32_t(slot) * stage_bytes, src + int64_t(st) * stage_bytes, bytes,
-                    &full[slot]);
+        const uint32_t dbytes = dbulk ? uint32_t(r * kb * 2) : 0u;
+        const uint32_t dst = ring_addr + uint32_t(slot) * stage_bytes;
+        mbar_expect_tx_gv(&full[slot], bytes + dbytes);
+        bulk_g2s_gv(dst, src + int64_t(st) * code_bytes, bytes, &full[slot]);
+        if (dbytes)
+            bulk_g2s_gv(dst + code_bytes, dsrc_rows + int64_t(st) * P.rs * kb, dbytes, &full[slot]);
     };
     const int first = min(nstages, P.ns);
     if (warp == consumers)
         for (int st = lane; st < first; st += 32) issue(st);
-    // ---- everyone: quantise x per 64-weight segment.  Thread (segment, word q,
-    // group t) owns the four weights 16q + 4m + t (m = 0..3) of its segment --
-    // exactly the bytes of its three limb words -- so it writes whole words.
-    // (Rolled loops throughout: this code runs once per launch, so a small
-    // instruction footprint matters more than unrolling.)
-    if (!mbar_wait_bounded(&full[P.ns], 0, wait_ns, status)) *abort_flag = 1;
-    const int nthr = nseg * 16;  // 16 threads per segment; blockDim.x is a multiple of 16
-#pragma unroll 1
-    for (int i0 = 0; i0 < nthr; i0 += blockDim.x) {
-        const int i = i0 + threadIdx.x;
-        const int seg = i >> 4, q = (i >> 2) & 3, t = i & 3;
-        float xe[4];
+    // ---- everyone: quantise x per 64-weight segment (from the registers
+    // loaded above; 16 threads per segment find its max |x| with shuffles)
+#pragma unroll
+    for (int p = 0; p < kGvQuantPasses; ++p) {
+        if (p * int(blockDim.x) >= nthr) break;  // block-uniform
+        const int qi = int(threadIdx.x) + p * int(blockDim.x);
+        const int qseg = qi >> 4, qq = (qi >> 2) & 3, qt = qi & 3;
         float m = 0.f;
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            const int kk = seg * 64 + 16 * q + 4 * mm + t;
-            xe[mm] = (i < nthr && kk < k) ? xraw[kk] : 0.f;
-            m = fmaxf(m, fabsf(xe[mm]));
-        }
+        for (int mm = 0; mm < 4; ++mm) m = fmaxf(m, fabsf(xe[p][mm]));
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         const float inv = m > 0.f ? 4194304.0f / m : 0.f;  // 2^22 / s, correctly rounded
@@ -396,7 +401,7 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
         int sx = 0;
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
-            const int X = max(-4194304, min(4194304, __float2int_rn(xe[mm] * inv)));
+            const int X = max(-4194304, min(4194304, __float2int_rn(xe[p][mm] * inv)));
             sx += X;
             l0 |= uint32_t(X & 0xFF) << (8 * mm);
             l1 |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
@@ -404,14 +409,14 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
         }
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
-        if (i < nthr) {
-            uint32_t *lw = limbs + seg * kSegWords + (q * 4 + t) * 3;
+        if (qi < nthr) {
+            uint32_t *lw = limbs + qseg * kSegWords + (qq * 4 + qt) * 3;
             lw[0] = l0;
             lw[1] = l1;
             lw[2] = l2;
-            if ((i & 15) == 0) {
-                sscale[seg] = m * (1.0f / 4194304.0f);  // s * 2^-22
-                ssum[seg] = sx;
+            if ((qi & 15) == 0) {
+                sscale[qseg] = m * (1.0f / 4194304.0f);  // s * 2^-22
+                ssum[qseg] = sx;
             }
         }
     }
@@ -444,8 +449,6 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
         // touched by one group, in stage order: no warp can wait on a slot's
         // next round before the group released the current one.
         const int g = warp / C, c = warp % C;
-        if (dbulk && rows > 0 && !mbar_wait_bounded(&full[P.ns + 1], 0, wait_ns, status))
-            *abort_flag = 1;
         const int seg = c * 32 + lane;
         const int kw0 = seg * 64;
         const bool active = kw0 < k;
@@ -460,6 +463,8 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             const int r0 = st * P.rs;                 // first row (CTA-relative) of the stage
             const int nv = min(P.rs, rows - r0);      // warp-uniform, >= 1
             const uint8_t *base = ring + size_t(slot) * stage_bytes + kw_rd / 4;
+            const __half *sd = dbulk ? reinterpret_cast<const __half *>(ring + size_t(slot) * stage_bytes + code_bytes)
+                                     : dsm + int64_t(r0) * kb;  // this stage's row scales
             // codes are read straight from the ring, word by word
             const uint8_t *rowp[RS];
 #pragma unroll
@@ -495,7 +500,7 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             for (int uu = 0; uu < RS; ++uu) {
                 const int ur = uu < nv ? uu : nv - 1;
                 const int tot = a2[uu] * 65536 + a1[uu] * 256 + a0[uu] - sx;
-                const float d = __half2float(dsm[int64_t(r0 + ur) * kb + kw_rd / kBlockW]);
+                const float d = __half2float(sd[int64_t(ur) * kb + kw_rd / kBlockW]);
                 v[uu] = float(tot) * (sc * d);
             }
             butterfly<RS>(v, lane);
@@ -535,10 +540,12 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.rextra = int(n % grid);
     P.rows_cta = P.rbase + (P.rextra ? 1 : 0);
     const int nseg = C * 32;
-    const size_t stage_bytes = size_t(P.rs) * kq;
+    const bool dbulk = (kb % 8) == 0;  // scales travel with their stage in the ring
+    const size_t stage_bytes = size_t(P.rs) * kq + (dbulk ? size_t(P.rs) * kb * 2 : 0);
+    const size_t dsm_bytes = dbulk ? 0 : size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2;
     const size_t lwords = size_t(nseg) * kSegWords;
-    const size_t fixed = size_t(k) * 4 + lwords * 4 + size_t(nseg) * 8 +
-                         size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2 +
+    if (size_t(nseg) * 16 > size_t(threads) * kGvQuantPasses) return cudaErrorNotSupported;
+    const size_t fixed = lwords * 4 + size_t(nseg) * 8 + dsm_bytes +
                          size_t((P.rows_cta * C + 1) & ~1) * 4;
     const size_t budget = 220 * 1024;
     if (fixed + stage_bytes + 64 * 16 + 32 > budget) return cudaErrorNotSupported;
@@ -554,14 +561,13 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     }
     P.ns = ns;
     P.consumers = P.groups * C;
-    P.off_x = uint32_t(size_t(ns) * stage_bytes);
-    P.off_limbs = uint32_t(P.off_x + size_t(k) * 4);
+    P.off_limbs = uint32_t(size_t(ns) * stage_bytes);
     P.off_scale = uint32_t(P.off_limbs + lwords * 4);
     P.off_sum = uint32_t(P.off_scale + size_t(nseg) * 4);
     P.off_d = uint32_t(P.off_sum + size_t(nseg) * 4);
-    P.off_partial = uint32_t(P.off_d + size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2);
+    P.off_partial = uint32_t(P.off_d + dsm_bytes);
     P.off_bar = uint32_t(P.off_partial + size_t((P.rows_cta * C + 1) & ~1) * 4);
-    const size_t smem = size_t(P.off_bar) + size_t(2 * ns + 2) * 8 + 16;
+    const size_t smem = size_t(P.off_bar) + size_t(2 * ns) * 8 + 16;
     cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
