@@ -259,7 +259,8 @@ constexpr int kGvChunk = 2048;  // weights per warp-chunk (32 lanes x 64)
 // shared memory and are summed per row at the end (plus the residual).
 
 constexpr int kSegWords = 52;  // 48 limb words per segment, padded (conflict-free 16-byte reads)
-constexpr int kGvQuantPasses = 4;  // x quantisation items per thread: 4 x 1024 x 4 values = K <= 16384
+constexpr int kGvThreads = 512;    // two CTAs per SM (registers, threads and shared memory)
+constexpr int kGvMaxSegs = 256;    // 64-weight segments of x: K <= 16384
 
 __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint32_t bytes,
                                             uint64_t *bar) {
@@ -268,6 +269,10 @@ __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint3
             "r"(dst),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx_gv(uint64_t *bar, uint32_t bytes) {
@@ -301,7 +306,7 @@ struct GvsParams {
 };
 
 template <int RS>  // rows per stage
-__global__ void __launch_bounds__(1024, 1)
+__global__ void __launch_bounds__(kGvThreads, 2)
 gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
                    const float *__restrict__ x, const float *residual, float *out, GvsParams P,
                    unsigned int *status, uint64_t wait_ns) {
@@ -310,7 +315,8 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
     const int k = P.k, C = P.C;
     const int64_t kq = k / 4, kb = k / kBlockW;
     const int nseg = C * 32;                 // 64-weight segments incl. padding past K
-    const int consumers = P.consumers;       // warp `consumers` is the producer
+    const int consumers = P.consumers;       // warps 0 .. consumers-1
+    const int pwarp = int(blockDim.x >> 5) - 1;  // the producer: the last warp
     const int b = int(blockIdx.x);
     const int R0 = b * P.rbase + min(b, P.rextra);
     const int rows = P.rbase + (b < P.rextra ? 1 : 0);
@@ -331,28 +337,6 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + P.ns);
     const uint32_t ring_addr = smem_u32(ring);
 
-    // x first: every thread loads the four elements it quantises below, before
-    // the weight stream is requested, so that x is not queued behind it.
-    // Thread (segment, word q, group t) owns the four weights 16q + 4m + t
-    // (m = 0..3) of its segment -- exactly the bytes of its three limb words.
-    // (Warp 0 loads after initialising the barriers: the proxy fence there
-    // would otherwise wait for its loads.)
-    const int nthr = nseg * 16;  // 16 threads per segment; blockDim.x is a multiple of 16
-    float xe[kGvQuantPasses][4];  // pass p: item threadIdx.x + p * blockDim.x (the host bounds nthr)
-    auto load_x = [&]() {
-#pragma unroll
-        for (int p = 0; p < kGvQuantPasses; ++p) {
-            const int qi = int(threadIdx.x) + p * int(blockDim.x);
-            const int qseg = qi >> 4, qq = (qi >> 2) & 3, qt = qi & 3;
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                const int kk = qseg * 64 + 16 * qq + 4 * mm + qt;
-                xe[p][mm] = (qi < nthr && kk < k) ? __ldg(x + kk) : 0.f;
-            }
-        }
-    };
-    if (warp != 0) load_x();
-
     // barriers: the lanes of warp 0 initialise them in parallel
     if (warp == 0) {
         for (int i = lane; i < P.ns; i += 32) {
@@ -361,12 +345,11 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
         }
         if (lane == 0) *abort_flag = 0;
         fence_proxy_async_smem();   // the inits are visible to the copy engine
-        load_x();
     }
     __syncthreads();
     // ---- producer warp, part 1: the first ring-full of stages needs no slot to
     // free up; its 32 lanes issue those copies in parallel
-    const bool producer = warp == consumers && lane == 0;
+    const bool producer = warp == pwarp && lane == 0;
     const uint8_t *src = qs + int64_t(R0) * kq;
     const __half *dsrc_rows = dpl + int64_t(R0) * kb;
     auto issue = [&](int st) {
@@ -380,45 +363,87 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
         if (dbytes)
             bulk_g2s_gv(dst + code_bytes, dsrc_rows + int64_t(st) * P.rs * kb, dbytes, &full[slot]);
     };
+    // The weights go to L2 before waiting for the preceding kernel.  A
+    // prefetch cannot leave stale data behind (L2 is the point of coherence,
+    // and the copies below read through it after the wait).
+    if (warp == pwarp) {
+        for (int st = lane; st < nstages; st += 32) {
+            const int r = min(P.rs, rows - st * P.rs);
+            bulk_prefetch_l2(src + int64_t(st) * code_bytes, uint32_t(r * kq));
+            if (dbulk) bulk_prefetch_l2(dsrc_rows + int64_t(st) * P.rs * kb, uint32_t(r * kb * 2));
+        }
+    }
+    // Everything a preceding kernel may have written (x, the weights, out and
+    // the residual) is touched only after this.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int first = min(nstages, P.ns);
-    if (warp == consumers)
+    if (warp == pwarp)
         for (int st = lane; st < first; st += 32) issue(st);
-    // ---- everyone: quantise x per 64-weight segment (from the registers
-    // loaded above; 16 threads per segment find its max |x| with shuffles)
+    // ---- everyone: quantise x per 64-weight segment.  Item (segment, word q,
+    // group t) loads the four consecutive elements 16q + 4t + m (m = 0..3) in
+    // one 16-byte read; 16 items per segment find its max |x| with shuffles.
+    // A 4 x 4 byte transpose among the four items of word q then leaves item
+    // (q, t) with the limb words whose byte m holds weight 16q + 4m + t, the
+    // order in which the dot products unpack the codes.  Items are taken three
+    // passes at a time, loads first.  The producer warp takes no items (it is
+    // busy issuing the copies).
+    const int nthr = nseg * 16;  // a multiple of 512: warp-uniform bounds
+    const int nq = int(blockDim.x) - 32;  // item threads (a multiple of 32)
+#pragma unroll 1
+    for (int p0 = 0; warp != pwarp && p0 * nq < nthr; p0 += 3) {  // warp-uniform
+        float4 xv[3];
 #pragma unroll
-    for (int p = 0; p < kGvQuantPasses; ++p) {
-        if (p * int(blockDim.x) >= nthr) break;  // block-uniform
-        const int qi = int(threadIdx.x) + p * int(blockDim.x);
+        for (int pp = 0; pp < 3; ++pp) {
+            const int qi = int(threadIdx.x) + (p0 + pp) * nq;
+            const int kk = (qi >> 4) * 64 + 16 * ((qi >> 2) & 3) + 4 * (qi & 3);
+            xv[pp] = (qi < nthr && kk < k) ? __ldg(reinterpret_cast<const float4 *>(x + kk))
+                                           : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+    for (int pp = 0; pp < 3; ++pp) {
+        const int p = p0 + pp;
+        if (p * nq >= nthr) break;  // uniform over the item threads
+        const int qi = int(threadIdx.x) + p * nq;
         const int qseg = qi >> 4, qq = (qi >> 2) & 3, qt = qi & 3;
+        const float xe[4] = {xv[pp].x, xv[pp].y, xv[pp].z, xv[pp].w};
         float m = 0.f;
 #pragma unroll
-        for (int mm = 0; mm < 4; ++mm) m = fmaxf(m, fabsf(xe[p][mm]));
+        for (int mm = 0; mm < 4; ++mm) m = fmaxf(m, fabsf(xe[mm]));
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         const float inv = m > 0.f ? 4194304.0f / m : 0.f;  // 2^22 / s, correctly rounded
         // |X| <= 2^22 (the rounded reciprocal may overshoot by half an ulp)
-        uint32_t l0 = 0, l1 = 0, l2 = 0;
+        uint32_t r[3] = {0, 0, 0};  // limb l of weight 16q + 4t + mm in byte mm
         int sx = 0;
 #pragma unroll
         for (int mm = 0; mm < 4; ++mm) {
-            const int X = max(-4194304, min(4194304, __float2int_rn(xe[p][mm] * inv)));
+            const int X = max(-4194304, min(4194304, __float2int_rn(xe[mm] * inv)));
             sx += X;
-            l0 |= uint32_t(X & 0xFF) << (8 * mm);
-            l1 |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
-            l2 |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
+            r[0] |= uint32_t(X & 0xFF) << (8 * mm);
+            r[1] |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
+            r[2] |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
         }
 #pragma unroll
         for (int o = 8; o >= 1; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
+        // transpose: item t gathers byte t of the four items' words
+#pragma unroll
+        for (int l = 0; l < 3; ++l) {
+            const uint32_t o1 = __shfl_xor_sync(0xffffffffu, r[l], 1);
+            const uint32_t h = (qt & 1) ? __byte_perm(r[l], o1, 0x3715) : __byte_perm(r[l], o1, 0x6240);
+            const uint32_t o2 = __shfl_xor_sync(0xffffffffu, h, 2);
+            r[l] = (qt & 2) ? __byte_perm(h, o2, 0x3276) : __byte_perm(h, o2, 0x5410);
+        }
         if (qi < nthr) {
             uint32_t *lw = limbs + qseg * kSegWords + (qq * 4 + qt) * 3;
-            lw[0] = l0;
-            lw[1] = l1;
-            lw[2] = l2;
+            lw[0] = r[0];
+            lw[1] = r[1];
+            lw[2] = r[2];
             if ((qi & 15) == 0) {
                 sscale[qseg] = m * (1.0f / 4194304.0f);  // s * 2^-22
                 ssum[qseg] = sx;
             }
         }
+    }
     }
     if (!dbulk) {
         const unsigned short *dsrc = reinterpret_cast<const unsigned short *>(dpl + int64_t(R0) * kb);
@@ -427,6 +452,13 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
     }
     __syncthreads();
 
+    // Programmatic dependent launch: once this CTA holds x and has its
+    // weight copies in flight, the next kernel of the stream may start
+    // launching.  Two CTAs of this kernel fit on one SM, so the next call's
+    // set-up and weight prefetch overlap this call's arithmetic (which needs
+    // no memory bandwidth); the next call reads nothing a predecessor may
+    // write before its own griddepcontrol.wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (producer) {
         // ---- producer, part 2: refill slots as the consumers release them
         for (int st = P.ns; st < nstages; ++st) {
@@ -465,15 +497,16 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             const uint8_t *base = ring + size_t(slot) * stage_bytes + kw_rd / 4;
             const __half *sd = dbulk ? reinterpret_cast<const __half *>(ring + size_t(slot) * stage_bytes + code_bytes)
                                      : dsm + int64_t(r0) * kb;  // this stage's row scales
-            // codes are read straight from the ring, word by word
-            const uint8_t *rowp[RS];
+            // each lane's 16 code bytes of a row in one conflict-free 16-byte read
+            uint4 cw[RS];
 #pragma unroll
-            for (int uu = 0; uu < RS; ++uu) rowp[uu] = base + size_t(uu < nv ? uu : nv - 1) * kq;
+            for (int uu = 0; uu < RS; ++uu)
+                cw[uu] = *reinterpret_cast<const uint4 *>(base + size_t(uu < nv ? uu : nv - 1) * kq);
             int a0[RS], a1[RS], a2[RS];
 #pragma unroll
             for (int uu = 0; uu < RS; ++uu) a0[uu] = a1[uu] = a2[uu] = 0;
             const uint4 *lw = reinterpret_cast<const uint4 *>(limbs + seg * kSegWords);
-#pragma unroll 1
+#pragma unroll
             for (int q = 0; q < 4; ++q) {
                 // limb words (q, t, l) for t = 0..3, l = 0..2: 12 words
                 const uint4 L0 = lw[3 * q + 0], L1 = lw[3 * q + 1], L2 = lw[3 * q + 2];
@@ -481,7 +514,7 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
                                          L2.x, L2.y, L2.z, L2.w};
 #pragma unroll
                 for (int uu = 0; uu < RS; ++uu) {
-                    const uint32_t wq = *reinterpret_cast<const uint32_t *>(rowp[uu] + 4 * q);
+                    const uint32_t wq = q == 0 ? cw[uu].x : q == 1 ? cw[uu].y : q == 2 ? cw[uu].z : cw[uu].w;
 #pragma unroll
                     for (int t = 0; t < 4; ++t) {
                         const uint32_t v = (wq >> (2 * t)) & 0x03030303u;
@@ -533,8 +566,8 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.k = int(k);
     P.C = C;
     P.rs = 4;
-    P.groups = 30 / C;  // consumer warp groups of C warps (one per chunk)
-    const int threads = 1024;  // 30 consumer warps at most, the producer warp, one helper
+    const int threads = kGvThreads;  // consumer warps, the producer warp, one spare
+    P.groups = std::max(1, (threads / 32 - 2) / C);  // consumer warp groups of C warps (one per chunk)
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + P.rs - 1) / P.rs));
     P.rbase = int(n / grid);
     P.rextra = int(n % grid);
@@ -544,10 +577,10 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     const size_t stage_bytes = size_t(P.rs) * kq + (dbulk ? size_t(P.rs) * kb * 2 : 0);
     const size_t dsm_bytes = dbulk ? 0 : size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2;
     const size_t lwords = size_t(nseg) * kSegWords;
-    if (size_t(nseg) * 16 > size_t(threads) * kGvQuantPasses) return cudaErrorNotSupported;
+    if (nseg > kGvMaxSegs) return cudaErrorNotSupported;
     const size_t fixed = lwords * 4 + size_t(nseg) * 8 + dsm_bytes +
                          size_t((P.rows_cta * C + 1) & ~1) * 4;
-    const size_t budget = 220 * 1024;
+    const size_t budget = 108 * 1024;  // two CTAs per SM
     if (fixed + stage_bytes + 64 * 16 + 32 > budget) return cudaErrorNotSupported;
     // ring: enough slots for all of a CTA's stages if shared memory allows (no
     // refill round trips), as a multiple of the group count
@@ -571,10 +604,24 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    // the largest shared-memory carve-out, so that two CTAs fit on an SM
+    e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    if (e != cudaSuccess) return e;
     const SoaView v = soa_view(w_soa, n, k);
-    gemv_stream_kernel<4><<<static_cast<unsigned>(grid), threads, smem, ctx.stream>>>(
-        v.qs, v.d, x, residual, out, P, ctx.status, ctx.wait_ns);
-    return cudaPeekAtLastError();
+    // programmatic dependent launch (see the kernel): the launch may begin
+    // before the preceding kernel of the stream has finished
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<4>, v.qs, v.d, x, residual, out, P, ctx.status,
+                              ctx.wait_ns);
 }
 
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
