@@ -399,51 +399,72 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             xv[pp] = (qi < nthr && kk < k) ? __ldg(reinterpret_cast<const float4 *>(x + kk))
                                            : make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // the three items' shuffle chains are interleaved step by step
+        float m[3], xe[3][4];
 #pragma unroll
-    for (int pp = 0; pp < 3; ++pp) {
-        const int p = p0 + pp;
-        if (p * nq >= nthr) break;  // uniform over the item threads
-        const int qi = int(threadIdx.x) + p * nq;
-        const int qseg = qi >> 4, qq = (qi >> 2) & 3, qt = qi & 3;
-        const float xe[4] = {xv[pp].x, xv[pp].y, xv[pp].z, xv[pp].w};
-        float m = 0.f;
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) m = fmaxf(m, fabsf(xe[mm]));
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        const float inv = m > 0.f ? 4194304.0f / m : 0.f;  // 2^22 / s, correctly rounded
-        // |X| <= 2^22 (the rounded reciprocal may overshoot by half an ulp)
-        uint32_t r[3] = {0, 0, 0};  // limb l of weight 16q + 4t + mm in byte mm
-        int sx = 0;
-#pragma unroll
-        for (int mm = 0; mm < 4; ++mm) {
-            const int X = max(-4194304, min(4194304, __float2int_rn(xe[mm] * inv)));
-            sx += X;
-            r[0] |= uint32_t(X & 0xFF) << (8 * mm);
-            r[1] |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
-            r[2] |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
+        for (int pp = 0; pp < 3; ++pp) {
+            xe[pp][0] = xv[pp].x; xe[pp][1] = xv[pp].y; xe[pp][2] = xv[pp].z; xe[pp][3] = xv[pp].w;
+            m[pp] = fmaxf(fmaxf(fabsf(xe[pp][0]), fabsf(xe[pp][1])), fmaxf(fabsf(xe[pp][2]), fabsf(xe[pp][3])));
         }
 #pragma unroll
-        for (int o = 8; o >= 1; o >>= 1) sx += __shfl_xor_sync(0xffffffffu, sx, o);
-        // transpose: item t gathers byte t of the four items' words
+        for (int o = 8; o >= 1; o >>= 1)
 #pragma unroll
-        for (int l = 0; l < 3; ++l) {
-            const uint32_t o1 = __shfl_xor_sync(0xffffffffu, r[l], 1);
-            const uint32_t h = (qt & 1) ? __byte_perm(r[l], o1, 0x3715) : __byte_perm(r[l], o1, 0x6240);
-            const uint32_t o2 = __shfl_xor_sync(0xffffffffu, h, 2);
-            r[l] = (qt & 2) ? __byte_perm(h, o2, 0x3276) : __byte_perm(h, o2, 0x5410);
-        }
-        if (qi < nthr) {
-            uint32_t *lw = limbs + qseg * kSegWords + (qq * 4 + qt) * 3;
-            lw[0] = r[0];
-            lw[1] = r[1];
-            lw[2] = r[2];
-            if ((qi & 15) == 0) {
-                sscale[qseg] = m * (1.0f / 4194304.0f);  // s * 2^-22
-                ssum[qseg] = sx;
+            for (int pp = 0; pp < 3; ++pp) m[pp] = fmaxf(m[pp], __shfl_xor_sync(0xffffffffu, m[pp], o));
+        uint32_t r[3][3];  // item pp, limb l: weight 16q + 4t + mm in byte mm
+        int sx[3];
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp) {
+            // 2^22 / s: the correctly rounded reciprocal times 2^22 (exact
+            // scaling), i.e. the correctly rounded quotient
+            const float inv = m[pp] > 0.f ? __frcp_rn(m[pp]) * 4194304.0f : 0.f;
+            r[pp][0] = r[pp][1] = r[pp][2] = 0;
+            sx[pp] = 0;
+#pragma unroll
+            for (int mm = 0; mm < 4; ++mm) {
+                // |X| <= 2^22 (the rounded reciprocal may overshoot by half an ulp)
+                const int X = max(-4194304, min(4194304, __float2int_rn(xe[pp][mm] * inv)));
+                sx[pp] += X;
+                r[pp][0] |= uint32_t(X & 0xFF) << (8 * mm);
+                r[pp][1] |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
+                r[pp][2] |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
             }
         }
-    }
+#pragma unroll
+        for (int o = 8; o >= 1; o >>= 1)
+#pragma unroll
+            for (int pp = 0; pp < 3; ++pp) sx[pp] += __shfl_xor_sync(0xffffffffu, sx[pp], o);
+        // transpose: item t gathers byte t of the four items' words of word q
+        const int qt = int(threadIdx.x) & 3;
+        uint32_t h[3][3];
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp)
+#pragma unroll
+            for (int l = 0; l < 3; ++l) {
+                const uint32_t o1 = __shfl_xor_sync(0xffffffffu, r[pp][l], 1);
+                h[pp][l] = (qt & 1) ? __byte_perm(r[pp][l], o1, 0x3715) : __byte_perm(r[pp][l], o1, 0x6240);
+            }
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp)
+#pragma unroll
+            for (int l = 0; l < 3; ++l) {
+                const uint32_t o2 = __shfl_xor_sync(0xffffffffu, h[pp][l], 2);
+                r[pp][l] = (qt & 2) ? __byte_perm(h[pp][l], o2, 0x3276) : __byte_perm(h[pp][l], o2, 0x5410);
+            }
+#pragma unroll
+        for (int pp = 0; pp < 3; ++pp) {
+            const int qi = int(threadIdx.x) + (p0 + pp) * nq;
+            if (qi < nthr) {
+                const int qseg = qi >> 4, qq = (qi >> 2) & 3;
+                uint32_t *lw = limbs + qseg * kSegWords + (qq * 4 + qt) * 3;
+                lw[0] = r[pp][0];
+                lw[1] = r[pp][1];
+                lw[2] = r[pp][2];
+                if ((qi & 15) == 0) {
+                    sscale[qseg] = m[pp] * (1.0f / 4194304.0f);  // s * 2^-22
+                    ssum[qseg] = sx[pp];
+                }
+            }
+        }
     }
     if (!dbulk) {
         const unsigned short *dsrc = reinterpret_cast<const unsigned short *>(dpl + int64_t(R0) * kb);
