@@ -96,6 +96,12 @@ def barrier(pg):
         pg.barrier()
 
 
+def whole_job_rate(world, units_per_rank, seconds):
+    """Units per second of the whole job: every rank processes `units_per_rank`
+    independent units (weak scaling) and `seconds` is the max over ranks."""
+    return world * units_per_rank / seconds
+
+
 class ClockSampler:
     """nvidia-smi clock / throttle-reason sampling while the GPU is busy."""
 
@@ -256,7 +262,7 @@ def run_ours(args, world, rank, local, pg):
         t_step = time_graph(gt, torch, pg, device, reps=1)
     clocks = clk.summary()
     per_launch = t_step / args.steps
-    value = world * wbytes * args.steps / t_step / 1e9
+    value = whole_job_rate(world, wbytes * args.steps, t_step) / 1e9
     achieved = wbytes / per_launch / 1e9
 
     # ---- end to end through the C ABI with host buffers
@@ -283,7 +289,7 @@ def run_ours(args, world, rank, local, pg):
     torch.cuda.synchronize()
     barrier(pg)
     t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, pg, device)
-    e2e = {"value": world * wbytes * args.steps / t_e2e / 1e9, "unit": "GB/s",
+    e2e = {"value": whole_job_rate(world, wbytes * args.steps, t_e2e) / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(out_host.numel() * 4),
            "note": "weights resident (uploaded once); x up and out down every step, pinned host buffers"}
 
