@@ -388,7 +388,12 @@ def run_ours(args, world, rank, local, pg):
                          "achieved": top["tflops"], "peak": bf16,
                          "frac": round(top["tflops"] / bf16, 4),
                          "peak_source": f"{peak_src} dense bf16 burst (f16 runs at the bf16 rate)",
-                         "traffic": None},
+                         "traffic": (ncu_traffic("tc_ws_m1536_k3072_n12288",
+                                                 ["dit_tq2_g128_gb300/csrc/gemm_tc_ws.cu"])
+                                     if top["n"] == 12288 else None),
+                         "traffic_note": "DRAM bytes of one tc_ws_kernel launch (the pre-pass is a "
+                                         "separate launch); algorithmic: x f16 9.4 MB + weights "
+                                         "10.0 MB read, 75.5 MB of output written"},
             "note": "timed separately from `value`; steps per N captured in a CUDA graph"}
     return line
 
