@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--gemm-n", type=int, default=0, help="only this N of the large-M set")
     ap.add_argument("--no-clock-window", action="store_true",
                     help="skip the 1 s sustained window that feeds the clock record")
+    ap.add_argument("--suite", action="store_true",
+                    help="instead of the bench line: every workload configuration (time per call, "
+                         "rate, parity on sampled rows against the oracle, oracle time on the sample)")
     return ap.parse_args()
 
 
@@ -399,6 +402,113 @@ def run_ours(args, world, rank, local, pg):
 
 
 # ---------------------------------------------------------------------------
+# --suite: all workload configurations
+
+
+def run_suite(args, local):
+    import torch
+    import oracle
+    import dit_tq2_g128_gb300 as tq2
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 126 * 2 ** 20))
+    rows_out = []
+
+    def timed(fn, steps):
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        g = graph_of(fn, steps, torch)
+        g.replay()
+        torch.cuda.synchronize()
+        ts = []
+        for _ in range(3):
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record()
+            g.replay()
+            e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1) / 1e3 / steps)
+        return statistics.median(ts)
+
+    def parity(out, p, rows):
+        """max |gpu - oracle| / sum|x w| over the sampled elements; min row cosine; oracle seconds."""
+        t0 = time.perf_counter()
+        ref, scale = oracle.matmul(p.w_aos, p.x, p.residual, n=p.n, k=p.k, rows=rows)
+        t_or = time.perf_counter() - t0
+        got = np.asarray(out, dtype=np.float64).reshape(-1, p.n)[rows]
+        rel = float(np.max(np.abs(got - ref) / np.maximum(scale, 1e-30)))
+        num = np.sum(got * ref, axis=1)
+        den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+        cos = float(np.min(np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)))
+        return rel, cos, t_or
+
+    def sample(m, count):
+        return np.unique(np.concatenate([[0, m - 1], np.random.default_rng(1).integers(0, m, count)]))
+
+    def one(name, p, kernel_entry, steps, sample_rows):
+        wbytes = tq2.tq2_soa_bytes(p.n, p.k)
+        per = wbytes + p.m * p.k * 4 + p.m * p.n * 4
+        c = max(2, -(-2 * l2 // per) + 1) if per < l2 else 1
+        w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
+        ws = [w0] + [w0.clone() for _ in range(c - 1)]
+        x = torch.from_numpy(p.x).to(device)
+        r = None if p.residual is None else torch.from_numpy(p.residual).to(device)
+        outs = [torch.empty((p.m, p.n), dtype=torch.float32, device=device) for _ in range(c)]
+
+        def fn(i):
+            if kernel_entry == "gemv":
+                tq2.tq2_gemv(ws[i % c], x, r, outs[i % c], p.n, p.k)
+            else:
+                tq2.tq2_gemm(ws[i % c], x, r, outs[i % c], p.m, p.n, p.k)
+
+        t = timed(fn, steps)
+        fn(0)
+        torch.cuda.synchronize()
+        assert tq2.tq2_device_status() == tq2.TQ2_OK
+        rows = sample(p.m, sample_rows) if p.m > sample_rows else np.arange(p.m)
+        rel, cos, t_or = parity(outs[0].cpu().numpy(), p, rows)
+        kern = tq2.KERNEL_NAMES[tq2.tq2_select_kernel(p.m, p.n, p.k)]
+        rec = {"config": name, "m": p.m, "n": p.n, "k": p.k, "kernel": kern,
+               "us_per_call": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+               "TFLOPs": round(2.0 * p.m * p.n * p.k / t / 1e12, 2),
+               "max_err_over_sum_abs_xw": rel, "min_row_cos": cos,
+               "parity_rows": int(rows.size),
+               "oracle_s_full_extrapolated": round(t_or * p.m / rows.size, 3),
+               "l2": f"{c} rotating weight copies" if c > 1 else "inputs larger than L2"}
+        del ws, outs, x, r, w0
+        torch.cuda.empty_cache()
+        return rec, t
+
+    rows_out.append(one("1 small", tq2_synth.small(), "gemm", 50, 8)[0])
+    rows_out.append(one("2a decode gate/up", tq2_synth.decode_gate_up(), "gemv", 200, 1)[0])
+    rows_out.append(one("2b decode down + residual", tq2_synth.decode_down(), "gemv", 200, 1)[0])
+    for m in tq2_synth.SKINNY_MS:
+        rows_out.append(one(f"3 skinny m={m}", tq2_synth.skinny(m), "gemv" if m == 1 else "gemm",
+                            100, 16)[0])
+    for n in tq2_synth.DIT_NS:
+        rows_out.append(one(f"4 dit n={n}", tq2_synth.dit(n), "gemm", 10, 16)[0])
+    # config 5: the 100 layers one after another (each timed on its own, summed)
+    tot_t, tot_f, worst, cmin, t_or5 = 0.0, 0.0, 0.0, 1.0, 0.0
+    for li in range(len(tq2_synth.DIT_FORWARD_SHAPES)):
+        p = tq2_synth.dit_forward_layer(li)
+        rec, t = one(f"5 layer {li}", p, "gemm", 3, 2)
+        tot_t += t
+        tot_f += 2.0 * p.m * p.n * p.k
+        worst = max(worst, rec["max_err_over_sum_abs_xw"])
+        cmin = min(cmin, rec["min_row_cos"])
+        t_or5 += rec["oracle_s_full_extrapolated"]
+    rows_out.append({"config": "5 dit forward (100 layers, M=4096)", "kernel": "tc",
+                     "us_total": round(tot_t * 1e6, 1), "TFLOPs": round(tot_f / tot_t / 1e12, 2),
+                     "max_err_over_sum_abs_xw": worst, "min_row_cos": cmin,
+                     "parity_rows": "2 sampled rows per layer",
+                     "oracle_s_full_extrapolated": round(t_or5, 1)})
+    return {"suite": rows_out, "oracle_threads": oracle.threads()}
+
+
+# ---------------------------------------------------------------------------
 # CPU oracle (cpu_baseline leg, and the --impl reference arm)
 
 
@@ -447,6 +557,9 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse()
+    if args.suite:
+        print(json.dumps(run_suite(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)
+        return
     world, rank, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
         line = run_reference(args, world, rank)

@@ -517,14 +517,25 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 if (row0 >= M || col0 >= N) continue;  // block wholly outside the output
                 if (epi_mode == EPI_DIRECT) {
                     if (col >= N) continue;
-#pragma unroll 8
-                    for (int j = 0; j < 32; ++j) {
-                        const int row = row0 + j;
-                        if (row >= M) break;
-                        const int64_t o = int64_t(row) * N + col;
-                        float v = __uint_as_float(r[j]);
-                        if (residual) v += residual[o];
-                        out[o] = v;
+                    const int nr = min(32, M - row0);  // rows of this block inside the output
+                    float *op = out + int64_t(row0) * N + col;
+                    if (residual) {
+                        // 16 residual loads in flight before their first use
+                        const float *rp = residual + int64_t(row0) * N + col;
+#pragma unroll
+                        for (int h = 0; h < 32; h += 16) {
+                            float rv[16];
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                rv[j] = h + j < nr ? __ldcs(rp + int64_t(h + j) * N) : 0.f;
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                if (h + j < nr) op[int64_t(h + j) * N] = __uint_as_float(r[h + j]) + rv[j];
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nr) op[int64_t(j) * N] = __uint_as_float(r[j]);
                     }
                 } else {
                     // Stage the 32 x 32 block (row j, column lane) and hand it
