@@ -189,7 +189,7 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
             // x -> f16 tiles in a stream-ordered temporary, then the clustered
             // kernel; without the temporary, the kernel that converts x itself
             void *ws = nullptr;
-            if (cudaMallocAsync(&ws, tq2::tc_ws_bytes(m, k), ctx.stream) == cudaSuccess) {
+            if (cudaMallocAsync(&ws, tq2::tc_ws_bytes(m, n, k), ctx.stream) == cudaSuccess) {
                 const cudaError_t e = tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, ws, ctx);
                 const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
                 return finish(e != cudaSuccess ? e : f);
@@ -207,7 +207,7 @@ size_t tq2_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k) {
     bool noop = false;
     if (check_shape(m, n, k, &noop) != TQ2_OK || noop) return 0;
     if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC) return 0;
-    return tq2::tc_ws_bytes(m, k);
+    return tq2::tc_ws_bytes(m, n, k);
 }
 
 int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float *out, int64_t m,
@@ -217,7 +217,7 @@ int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float 
     if (st != TQ2_OK || noop) return st;
     if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC)
         return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
-    const size_t need = tq2::tc_ws_bytes(m, k);
+    const size_t need = tq2::tc_ws_bytes(m, n, k);
     if (!workspace || workspace_bytes < need) return TQ2_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 127u) != 0) return TQ2_ERR_MISALIGNED;
     const size_t wb = size_t(n) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
@@ -238,7 +238,7 @@ int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, f
     if (st != TQ2_OK || noop) return st;
     if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC)  // these kernels use no scratch
         return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
-    if (tq2::tc_ws_bytes(m, k) > tq2::kNoAllocScratchBytes) return TQ2_ERR_TOO_LARGE;
+    if (tq2::tc_ws_bytes(m, n, k) > tq2::kNoAllocScratchBytes) return TQ2_ERR_TOO_LARGE;
     tq2::LaunchCtx ctx;
     st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
     if (st != TQ2_OK) return st;

@@ -267,7 +267,8 @@ x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
              const __half *__restrict__ dpl, const uint8_t *__restrict__ xtiles, const float *residual,
-             float *out, int M, int N, int K, int epi_mode, unsigned int *status, uint64_t wait_ns) {
+             float *out, int M, int N, int K, int epi_mode, int ksplit, float *partial,
+             unsigned int *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
     const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
@@ -285,6 +286,22 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
     const int cl = int(blockIdx.x) >> 1, ncl = int(gridDim.x) >> 1;
     const int ntiles = MX * ((NW + 1) / 2);
     const uint16_t pair_mask = 0x3;
+    // Work item t: output tile pair t / ksplit, K slice t % ksplit (split-K for
+    // shapes with fewer tile pairs than clusters; slices go to `partial`).
+    const int nitems = ntiles * ksplit;
+    struct Item {
+        int mx, nw, ks, kbeg, nk;
+    };
+    auto item = [&](int t) {
+        Item it;
+        const int tile = t / ksplit;
+        it.ks = t % ksplit;
+        it.mx = tile % MX;
+        it.nw = 2 * (tile / MX) + rank;
+        it.kbeg = int(int64_t(it.ks) * KT / ksplit);
+        it.nk = int(int64_t(it.ks + 1) * KT / ksplit) - it.kbeg;
+        return it;
+    };
     const int64_t kb = K / kBlockW;
 
     if (tid == 0) {
@@ -337,10 +354,12 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             int last_round[STAGES > CSTAGES ? STAGES : CSTAGES];
             for (int s = 0; s < depth; ++s) last_round[s] = -1;
             bool ok = true;
-            for (int t = cl; t < ntiles && ok; t += ncl) {
-                const int mx = t % MX, nw = 2 * (t / MX) + rank;
+            for (int t = cl; t < nitems && ok; t += ncl) {
+                const Item it = item(t);
+                const int mx = it.mx, nw = it.nw;
                 const int mt0 = 2 * mx, nmt = min(2, MT - mt0);  // 128-row x tiles of this output tile
-                for (int kt = 0; kt < KT; ++kt, ++g) {
+                for (int j = 0; j < it.nk; ++j, ++g) {
+                    const int kt = it.kbeg + j;
                     const int s = int(g % depth);
                     const int u = int(g / depth);
                     uint64_t *freed = codes ? &ctl->codes_empty[s] : &ctl->empty[s];
@@ -396,7 +415,8 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             int64_t g = 0;
             int i = 0;
             bool ok = true;
-            for (int t = cl; t < ntiles && ok; t += ncl, ++i) {
+            for (int t = cl; t < nitems && ok; t += ncl, ++i) {
+                const int nk = item(t).nk;
                 const int a = i & 1;
                 // accumulator a was last used by tile i - 2: wait for its epilogue
                 if (i >= 2 && !mbar_wait_bounded(&ctl->tmem_empty[a], ((i >> 1) - 1) & 1, wait_ns, status)) {
@@ -405,7 +425,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 }
                 tc_fence_after();
                 const uint32_t dcol = tmem + ACC_COL + uint32_t(a) * BX;
-                for (int kt = 0; kt < KT; ++kt, ++g) {
+                for (int j = 0; j < nk; ++j, ++g) {
                     const int s = int(g % STAGES);
                     const uint32_t par = uint32_t(g / STAGES) & 1;
                     if (!mbar_wait_bounded(&ctl->full[s], par, wait_ns, status)) {
@@ -419,7 +439,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     const uint64_t bdesc = sw128_desc(stage_x(s));
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk)
-                        tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (kt | kk) != 0);
+                        tc_mma_f16(dcol, adesc + 2 * kk, bdesc + 2 * kk, IDESC, (j | kk) != 0);
                     tc_commit_mc(&ctl->empty[s], pair_mask);
                 }
                 if (ok) tc_commit(&ctl->tmem_full[a]);
@@ -432,21 +452,23 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         const uint32_t rsw = uint32_t(pr & 7);     // SWIZZLE_128B phase of this row
         const uint32_t rbase = uint32_t(pr >> 3) * 1024 + rsw * 128;
         int64_t gbase = 0;
-        for (int t = cl; t < ntiles; t += ncl, gbase += KT) {
-            const int nw = 2 * (t / MX) + rank;
+        for (int t = cl; t < nitems; t += ncl) {
+            const Item it = item(t);
+            const int nw = it.nw;
             const int row = nw * BW + pr;
             const bool rvalid = row < N;
             const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
-            const int kt0 = int(((dset - gbase) % DEC_SETS + DEC_SETS) % DEC_SETS);
+            const int j0 = int(((dset - gbase) % DEC_SETS + DEC_SETS) % DEC_SETS);
             // the scale of this thread's next stage, loaded one stage ahead
-            uint32_t dnext = (rvalid && kt0 < KT) ? ldg_u16(drow + (kt0 >> 1)) : 0u;
+            uint32_t dnext = (rvalid && j0 < it.nk) ? ldg_u16(drow + ((it.kbeg + j0) >> 1)) : 0u;
             bool stop = false;
-            for (int kt = kt0; kt < KT; kt += DEC_SETS) {
-                const int64_t g = gbase + kt;
+            for (int j = j0; j < it.nk; j += DEC_SETS) {
+                const int kt = it.kbeg + j;
+                const int64_t g = gbase + j;
                 const int cs = int(g % CSTAGES);
                 const int s = int(g % STAGES);
                 const uint32_t dbits = dnext;
-                if (rvalid && kt + DEC_SETS < KT) dnext = ldg_u16(drow + ((kt + DEC_SETS) >> 1));
+                if (rvalid && j + DEC_SETS < it.nk) dnext = ldg_u16(drow + ((kt + DEC_SETS) >> 1));
                 if (!mbar_wait_bounded(&ctl->codes_full[cs], uint32_t(g / CSTAGES) & 1, wait_ns,
                                        status)) {
                     *abort_flag = 1;
@@ -489,14 +511,20 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 fence_proxy_async_smem();
                 mbar_arrive(&ctl->full[s]);
             }
+            gbase += it.nk;
             if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
         }
     } else if (warp >= EPI_WARP0) {
         const int quarter = warp - EPI_WARP0;  // TMEM lanes 32*quarter .. +31 = output columns
         const uint32_t ebuf = ebase + uint32_t(quarter) * EPI_NB * EPI_BYTES;
         int i = 0, e = 0;
-        for (int t = cl; t < ntiles; t += ncl, ++i) {
-            const int mx = t % MX, nw = 2 * (t / MX) + rank;
+        for (int t = cl; t < nitems; t += ncl, ++i) {
+            const Item it = item(t);
+            const int mx = it.mx, nw = it.nw;
+            // a K slice of a split problem writes its partial sums, plainly
+            float *const dst = ksplit > 1 ? partial + int64_t(it.ks) * M * N : out;
+            const float *const res = ksplit > 1 ? nullptr : residual;
+            const int mode = ksplit > 1 ? EPI_DIRECT : epi_mode;
             const int a = i & 1;
             if (!mbar_wait_bounded(&ctl->tmem_full[a], (i >> 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -515,13 +543,13 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 }
                 const int row0 = mx * BX + c * 32;
                 if (row0 >= M || col0 >= N) continue;  // block wholly outside the output
-                if (epi_mode == EPI_DIRECT) {
+                if (mode == EPI_DIRECT) {
                     if (col >= N) continue;
                     const int nr = min(32, M - row0);  // rows of this block inside the output
-                    float *op = out + int64_t(row0) * N + col;
-                    if (residual) {
+                    float *op = dst + int64_t(row0) * N + col;
+                    if (res) {
                         // 16 residual loads in flight before their first use
-                        const float *rp = residual + int64_t(row0) * N + col;
+                        const float *rp = res + int64_t(row0) * N + col;
 #pragma unroll
                         for (int h = 0; h < 32; h += 16) {
                             float rv[16];
@@ -552,7 +580,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        if (epi_mode == EPI_TMA_ADD)
+                        if (mode == EPI_TMA_ADD)
                             tma_add_2d(&omap, col0, row0, buf);
                         else
                             tma_store_2d(&omap, col0, row0, buf);
@@ -586,6 +614,37 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
     cluster_sync();
 }
 
+// out = sum of the K-slice partials in slice order (+ residual): deterministic.
+__global__ void __launch_bounds__(256)
+ksplit_reduce_kernel(const float *__restrict__ part, int S, int64_t mn, const float *residual,
+                     float *out) {
+    const int64_t stride = int64_t(gridDim.x) * blockDim.x;
+    const int64_t i0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x;
+    if ((mn & 3) == 0) {
+        const int64_t n4 = mn / 4;
+        const float4 *p4 = reinterpret_cast<const float4 *>(part);
+        for (int64_t i = i0; i < n4; i += stride) {
+            float4 acc = __ldcs(p4 + i);
+            for (int s = 1; s < S; ++s) {
+                const float4 v = __ldcs(p4 + int64_t(s) * n4 + i);
+                acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+            }
+            if (residual) {
+                const float4 r = reinterpret_cast<const float4 *>(residual)[i];
+                acc.x += r.x; acc.y += r.y; acc.z += r.z; acc.w += r.w;
+            }
+            reinterpret_cast<float4 *>(out)[i] = acc;
+        }
+    } else {
+        for (int64_t i = i0; i < mn; i += stride) {
+            float acc = part[i];
+            for (int s = 1; s < S; ++s) acc += part[int64_t(s) * mn + i];
+            if (residual) acc += residual[i];
+            out[i] = acc;
+        }
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
@@ -613,7 +672,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
                               int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx) {
-    if (tc_ws_bytes(m, k) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+    if (tc_ws_bytes(m, n, k) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -634,9 +693,27 @@ cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *re
     return launch_tc_ws(w_soa, x, residual, out, m, n, k, scratch, ctx);
 }
 
-size_t tc_ws_bytes(int64_t m, int64_t k) {
+// K slices per output tile pair: enough work items for the 76 CTA pairs of a
+// 152-SM GB300 when the shape has fewer tile pairs, at least 4 stages each.
+// A function of the shape only (the workspace size must not depend on the device).
+int tc_ksplit(int64_t m, int64_t n, int64_t k) {
+    const int64_t pairs = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2);
+    int64_t s = pairs < 76 ? 76 / pairs : 1;
+    s = std::min<int64_t>(s, (k / BK) / 4);
+    s = std::min<int64_t>(s, 16);
+    return int(std::max<int64_t>(s, 1));
+}
+
+static size_t x_tile_bytes(int64_t m, int64_t k) {
     const int64_t mt = (m + BM - 1) / BM;
     return size_t(mt) * BM * size_t(k) * 2;
+}
+
+size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k) {
+    const size_t xb = x_tile_bytes(m, k);
+    const int s = tc_ksplit(m, n, k);
+    if (s == 1) return xb;
+    return ((xb + 255) & ~size_t(255)) + size_t(s) * size_t(m) * size_t(n) * 4;
 }
 
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
@@ -681,11 +758,21 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
                              static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     // clusters of two CTAs, each cluster a pair of neighbouring weight tiles
-    const int64_t ntiles = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2);
-    const int64_t grid = 2 * std::min<int64_t>(ntiles, ctx.num_sms / 2);
+    // (times the K slices of a split problem)
+    const int ksplit = tc_ksplit(m, n, k);
+    float *partial = ksplit > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
+                                                            ((x_tile_bytes(m, k) + 255) & ~size_t(255)))
+                                : nullptr;
+    const int64_t nitems = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2) * ksplit;
+    const int64_t grid = 2 * std::min<int64_t>(nitems, ctx.num_sms / 2);
     tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
         qmap, omap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
-        epi_mode, ctx.status, ctx.wait_ns);
+        epi_mode, ksplit, partial, ctx.status, ctx.wait_ns);
+    e = cudaPeekAtLastError();
+    if (e != cudaSuccess || ksplit == 1) return e;
+    const int64_t mn = m * n;
+    const int64_t rgrid = std::min<int64_t>((mn / 4 + 255) / 256 + 1, int64_t(ctx.num_sms) * 8);
+    ksplit_reduce_kernel<<<unsigned(rgrid), 256, 0, ctx.stream>>>(partial, ksplit, mn, residual, out);
     return cudaPeekAtLastError();
 }
 

@@ -48,7 +48,8 @@ cudaError_t launch_f32ref(const void *w_soa, const float *x, const float *residu
 cudaError_t launch_tc(const void *w_soa, const float *x, const float *residual, float *out,
                       int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
 // Workspace variant of the tensor-core kernel (x pre-converted to f16 tiles).
-size_t tc_ws_bytes(int64_t m, int64_t k);
+size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k);  // x tiles (+ split-K partials)
+int tc_ksplit(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx);
 // Same kernel pair with the library's fixed device scratch (no allocation).

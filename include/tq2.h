@@ -147,10 +147,12 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
 int tq2_gemm_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
                     int64_t m, int64_t n, int64_t k, void *stream);
 
-/* Workspace bytes that tq2_gemm_ws needs for this shape: the binary16 copy of
- * x, padded to a multiple of 128 rows (ceil(m/128)*128*k*2 bytes) when the
- * shape selects the tensor-core kernel, else 0.  Host only.  Returns 0 for
- * invalid shapes. */
+/* Workspace bytes that tq2_gemm_ws needs for this shape when it selects the
+ * tensor-core kernel, else 0: the binary16 copy of x, padded to a multiple of
+ * 128 rows (ceil(m/128)*128*k*2 bytes), plus, for shapes with too few output
+ * tiles to occupy the GPU, S f32 partial results of m*n elements (S K slices,
+ * a function of the shape only, summed afterwards in slice order).  Host only.
+ * Returns 0 for invalid shapes. */
 size_t tq2_gemm_workspace_bytes(int64_t m, int64_t n, int64_t k);
 
 /* tq2_gemm with a caller-owned device workspace (the library still
@@ -181,9 +183,9 @@ int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float 
  * (TQ2_NOALLOC_SCRATCH_BYTES, reserved on every device that loads the library
  * until the process exits) and then runs the same kernel as tq2_gemm_ws, with
  * the same results.  Other shapes use no scratch and behave like tq2_gemm.
- *   - Limit: shapes with ceil(m/128)*128*k*2 > TQ2_NOALLOC_SCRATCH_BYTES
- *     return TQ2_ERR_TOO_LARGE before any work (e.g. m = 4096 with k up to
- *     4096 fits; k = 12288 does not).
+ *   - Limit: shapes with tq2_gemm_workspace_bytes(m,n,k) >
+ *     TQ2_NOALLOC_SCRATCH_BYTES return TQ2_ERR_TOO_LARGE before any work
+ *     (e.g. m = 4096 with k up to 4096 fits; k = 12288 does not).
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - The first call on a device looks up the scratch array's device address
  *     (one-time set-up, with that device current); make that first call before
