@@ -74,6 +74,10 @@ def lib():
             L.tq2o_soa_to_aos.argtypes = [_p, _p, _i64, _i64]
             L.tq2o_threads.restype = ctypes.c_int
             L.tq2o_set_threads.argtypes = [ctypes.c_int]
+            L.tq2o_double_to_half.restype = ctypes.c_uint16
+            L.tq2o_double_to_half.argtypes = [ctypes.c_double]
+            L.tq2o_quantize.restype = ctypes.c_int
+            L.tq2o_quantize.argtypes = [_p, _i64, _i64, _p]
             _lib = L
     return _lib
 
@@ -161,3 +165,20 @@ def soa_to_aos(w_soa, n: int, k: int) -> np.ndarray:
     if lib().tq2o_soa_to_aos(_ptr(s), _ptr(out), n, k):
         raise ValueError("bad k")
     return out.reshape(n, k // 128, 34)
+
+
+def double_to_half(v: float) -> int:
+    """binary16 bits of v, round to nearest even (the oracle's own conversion)."""
+    return int(lib().tq2o_double_to_half(float(v)))
+
+
+def quantize(w, n: int, k: int) -> np.ndarray:
+    """Encoder: f32 weights [n, k] -> uint8 AoS blocks [n, k/128, 34] (absmean
+    scale per 128-weight block, binary16 round to nearest even, codes
+    clamp(rint(w / d), -1, 1) + 1 in binary32)."""
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    assert w.size == n * k
+    out = np.zeros((n, k // 128 if k > 0 else 0, 34), dtype=np.uint8)
+    if lib().tq2o_quantize(_ptr(w), n, k, _ptr(out)) == -1:
+        raise ValueError(f"tq2o_quantize: k={k} is not a positive multiple of 128")
+    return out

@@ -26,6 +26,11 @@
  *    the d plane [N][K/128] binary16 values; block (n,b) keeps its qs bytes at
  *    (n*(K/128)+b)*32 and its two d bytes at N*K/4 + (n*(K/128)+b)*2.
  *
+ *  - the encoder (f32 weights -> blocks) is this library's reading, because
+ *    the pages never show how the blocks are produced (they are read from a
+ *    GGUF file): the absmean rule of ternary weights, with every step that
+ *    decides a code fixed (see tq2o_quantize below).
+ *
  * Everything is computed in IEEE double; the binary16 scale is decoded from
  * its bits by hand (no compiler half type).  Rows of the output are spread
  * over OpenMP threads when the build has OpenMP; the arithmetic per element is
@@ -186,6 +191,74 @@ int tq2o_soa_to_aos(const uint8_t *soa, uint8_t *aos, int64_t n, int64_t k) {
         for (int j = 0; j < TQ2O_QS_BYTES; ++j) blk[j] = qs_plane[i * TQ2O_QS_BYTES + j];
         blk[TQ2O_QS_BYTES + 0] = d_plane[i * 2 + 0];
         blk[TQ2O_QS_BYTES + 1] = d_plane[i * 2 + 1];
+    }
+    return 0;
+}
+
+/* double -> IEEE binary16 bits, round to nearest even, by hand: values at or
+ * above 65520 (halfway past the largest finite 65504) become Inf; magnitudes at
+ * or below 2^-25 become (signed) zero; subnormals keep the 2^-24 step. */
+uint16_t tq2o_double_to_half(double v) {
+    uint16_t sign = signbit(v) ? 0x8000 : 0;
+    double a = fabs(v);
+    if (isnan(v)) return 0x7e00;
+    if (a >= 65520.0) return (uint16_t)(sign | 0x7c00);
+    if (a < ldexp(1.0, -14)) {
+        /* subnormal range: integer multiple of 2^-24 (1024 carries into the
+         * smallest normal, which is the right encoding) */
+        double f = nearbyint(ldexp(a, 24));
+        return (uint16_t)(sign | (uint16_t)f);
+    }
+    int ex;
+    frexp(a, &ex); /* a = m * 2^ex, m in [0.5, 1): the unbiased exponent is ex - 1 */
+    int e = ex - 1;
+    double r = nearbyint(ldexp(a, 10 - e)); /* in [1024, 2048] */
+    if (r >= 2048.0) {
+        r = 1024.0;
+        e += 1;
+    }
+    if (e > 15) return (uint16_t)(sign | 0x7c00);
+    return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(r - 1024.0));
+}
+
+/* Encoder: f32 weights w[n][k] (row-major) -> AoS blocks [n][k/128] of 34
+ * bytes.  For each 128-weight block (the absmean rule of ternary weights):
+ *   gamma = (sum_{j=0..127} |w_j|) / 128, the sum in double in index order;
+ *   d     = binary16(gamma), round to nearest even;
+ *   q_j   = rint(w_j / (float)d) in binary32 (IEEE division, ties to even),
+ *           clamped to [-1, 1]; code c_j = q_j + 1 (weight j at bits
+ *           2*(j%4) of qs[j/4]).
+ * A zero or non-finite d gives code 1 (weight 0) everywhere.  Returns -1 for
+ * a k that is not a positive multiple of 128. */
+int tq2o_quantize(const float *w, int64_t n, int64_t k, uint8_t *aos) {
+    if (k <= 0 || k % TQ2O_BLOCK_W) return -1;
+    const int64_t nb = k / TQ2O_BLOCK_W;
+    int64_t r;
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (r = 0; r < n; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            const float *wb = w + r * k + b * TQ2O_BLOCK_W;
+            double s = 0.0;
+            for (int j = 0; j < TQ2O_BLOCK_W; ++j) s += fabs((double)wb[j]);
+            const uint16_t dh = tq2o_double_to_half(s / 128.0);
+            const double dd = tq2o_half_to_double(dh);
+            const int live = dd > 0.0 && isfinite(dd);
+            const float df = (float)dd; /* exact: a binary16 value */
+            uint8_t *blk = aos + (r * nb + b) * TQ2O_BLOCK_BYTES;
+            memset(blk, 0, TQ2O_QS_BYTES);
+            for (int j = 0; j < TQ2O_BLOCK_W; ++j) {
+                int c = 1;
+                if (live) {
+                    const float q = rintf(wb[j] / df);
+                    c = q >= 1.0f ? 2 : (q <= -1.0f ? 0 : 1);
+                }
+                blk[j / 4] |= (uint8_t)(c << (2 * (j % 4)));
+            }
+            blk[TQ2O_QS_BYTES + 0] = (uint8_t)(dh & 0xff);
+            blk[TQ2O_QS_BYTES + 1] = (uint8_t)(dh >> 8);
+        }
     }
     return 0;
 }

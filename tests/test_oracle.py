@@ -285,3 +285,100 @@ def test_generator_distributions():
     q = tq2_synth.dit(3072)
     col_absmax = np.abs(q.x).max(axis=0)
     assert (col_absmax > 10).sum() == round(0.01 * 3072)
+
+
+# ---------------------------------------------------------------------------
+# Encoder (f32 -> blocks): this library's absmean reading, pinned to closed
+# forms and to numpy's own binary16 conversion.
+
+
+def _codes(blk):
+    """The 128 codes of one 34-byte block."""
+    b = np.asarray(blk, dtype=np.uint8)
+    return np.array([(b[j // 4] >> (2 * (j % 4))) & 3 for j in range(128)])
+
+
+def _d_bits(blk):
+    return int(blk[32]) | (int(blk[33]) << 8)
+
+
+def test_double_to_half_matches_numpy():
+    rng = np.random.default_rng(5)
+    vals = np.concatenate([
+        rng.standard_normal(20000) * 10.0 ** rng.uniform(-9, 5, 20000),
+        [0.0, -0.0, 1.0, -1.0, 65504.0, 65519.999, 65520.0, 1e30, -1e30,
+         2.0 ** -24, 2.0 ** -25, 2.0 ** -25 * 1.0000001, 3 * 2.0 ** -26, 2.0 ** -14,
+         2.0 ** -14 - 2.0 ** -25, 1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 2049.0, 2051.0]])
+    for v in vals:
+        want = int(np.array([v], dtype=np.float64).astype(np.float16).view(np.uint16)[0])
+        assert oracle.double_to_half(v) == want, (v, hex(want))
+
+
+def test_quantize_constant_block():
+    # gamma = |a|; a exactly representable: w / d = +-1 -> codes 2 (positive), 0 (negative)
+    for a in (1.0, 0.375, -2.5, 2.0 ** -10):
+        blk = oracle.quantize(np.full((1, 128), a, np.float32), 1, 128)[0, 0]
+        assert oracle.half_to_double(_d_bits(blk)) == abs(a)
+        assert np.all(_codes(blk) == (2 if a > 0 else 0))
+
+
+def test_quantize_alternating_and_spike():
+    w = np.tile(np.array([0.75, -0.75], np.float32), 64).reshape(1, 128)
+    blk = oracle.quantize(w, 1, 128)[0, 0]
+    assert oracle.half_to_double(_d_bits(blk)) == 0.75
+    assert np.array_equal(_codes(blk), np.tile([2, 0], 64))
+    # a single spike: gamma = 3/128 (exact in binary16); the spike clips to +1, zeros stay 0
+    w = np.zeros((1, 128), np.float32)
+    w[0, 5] = 3.0
+    blk = oracle.quantize(w, 1, 128)[0, 0]
+    assert oracle.half_to_double(_d_bits(blk)) == 3.0 / 128
+    want = np.ones(128, int)
+    want[5] = 2
+    assert np.array_equal(_codes(blk), want)
+
+
+def test_quantize_ties_round_to_even():
+    # 64 x 1.5 and 64 x 0.5: gamma = 1 exactly; rint(1.5) = 2 -> clipped to +1,
+    # rint(0.5) = 0 (ties to even), rint(-0.5) = -0 -> code 1
+    w = np.array([1.5] * 64 + [0.5] * 32 + [-0.5] * 32, np.float32).reshape(1, 128)
+    blk = oracle.quantize(w, 1, 128)[0, 0]
+    assert _d_bits(blk) == 0x3C00
+    assert np.array_equal(_codes(blk), np.array([2] * 64 + [1] * 64))
+
+
+def test_quantize_zero_and_huge_blocks():
+    blk = oracle.quantize(np.zeros((1, 128), np.float32), 1, 128)[0, 0]
+    assert _d_bits(blk) == 0 and np.all(_codes(blk) == 1)
+    # gamma above the binary16 range: d = Inf, every code 1
+    blk = oracle.quantize(np.full((1, 128), 1e6, np.float32), 1, 128)[0, 0]
+    assert _d_bits(blk) == 0x7C00 and np.all(_codes(blk) == 1)
+
+
+def test_quantize_scaling_and_layout():
+    rng = np.random.default_rng(11)
+    n, k = 3, 384
+    w = rng.standard_normal((n, k)).astype(np.float32)
+    a = oracle.quantize(w, n, k)
+    b = oracle.quantize(w * np.float32(4.0), n, k)
+    for r in range(n):
+        for blk in range(k // 128):
+            assert np.array_equal(_codes(a[r, blk]), _codes(b[r, blk]))
+            assert oracle.half_to_double(_d_bits(b[r, blk])) == 4 * oracle.half_to_double(_d_bits(a[r, blk]))
+            # each block is quantised on its own
+            one = oracle.quantize(w[r:r + 1, blk * 128:(blk + 1) * 128], 1, 128)[0, 0]
+            assert np.array_equal(one, a[r, blk])
+    # reconstruction: |w - (c-1) d| <= d/2 where |w| <= 1.5 d, else the clip error |w| - d
+    wd = oracle.dequant(a, n, k)
+    for r in range(n):
+        for blk in range(k // 128):
+            d = oracle.half_to_double(_d_bits(a[r, blk]))
+            seg = slice(blk * 128, (blk + 1) * 128)
+            err = np.abs(w[r, seg].astype(np.float64) - wd[r, seg])
+            bound = np.where(np.abs(w[r, seg]) <= 1.5 * d, 0.5 * d * (1 + 1e-6),
+                             np.abs(w[r, seg]) - d + 1e-12)
+            assert np.all(err <= bound)
+
+
+def test_quantize_bad_k():
+    with pytest.raises(ValueError):
+        oracle.quantize(np.zeros((1, 100), np.float32), 1, 100)
