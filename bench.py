@@ -505,6 +505,14 @@ def run_suite(args, local):
                      "max_err_over_sum_abs_xw": worst, "min_row_cos": cmin,
                      "parity_rows": "2 sampled rows per layer",
                      "oracle_s_full_extrapolated": round(t_or5, 1)})
+    # the encoder (f32 -> blocks) on the largest DiT weight: f32 bytes read per second
+    n, k = 12288, 3072
+    wf = torch.randn((n, k), device=device) * 0.02
+    aos = torch.empty(tq2.tq2_soa_bytes(n, k), dtype=torch.uint8, device=device)
+    t = timed(lambda i: tq2.tq2_quantize_f32(wf, aos, n, k), 10)
+    rows_out.append({"config": "encoder f32 -> blocks (12288 x 3072)", "us_per_call": round(t * 1e6, 2),
+                     "f32_GBps": round(n * k * 4 / t / 1e9, 1),
+                     "bytes_GBps": round((n * k * 4 + tq2.tq2_soa_bytes(n, k)) / t / 1e9, 1)})
     return {"suite": rows_out, "oracle_threads": oracle.threads()}
 
 

@@ -169,6 +169,19 @@ int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k
     return finish(tq2::launch_reformat(w_aos, w_soa, n, k, ctx));
 }
 
+int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *stream) {
+    if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
+    if (n < 0 || n > (int64_t(1) << 40) / k) return TQ2_ERR_INVALID_ARG;
+    if (n == 0) return TQ2_OK;
+    if (!w || !w_aos) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(w) || !aligned16(w_aos)) return TQ2_ERR_MISALIGNED;
+    if (overlaps(w, size_t(n) * size_t(k) * 4, w_aos, tq2_soa_bytes(n, k))) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_quantize(w, w_aos, n, k, ctx));
+}
+
 int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *residual,
                   float *out, int64_t m, int64_t n, int64_t k, void *stream) {
     bool noop = false;

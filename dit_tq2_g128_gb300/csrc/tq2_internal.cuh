@@ -37,6 +37,7 @@ inline SoaView soa_view(const void *w_soa, int64_t n, int64_t k) {
 
 // ---------------------------------------------------------------------------
 // Kernel launchers (one per .cu file).  All return cudaError_t of the launch.
+cudaError_t launch_quantize(const float *w, void *w_aos, int64_t n, int64_t k, const LaunchCtx &ctx);
 cudaError_t launch_reformat(const void *w_aos, void *w_soa, int64_t n, int64_t k,
                             const LaunchCtx &ctx);
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,

@@ -102,6 +102,22 @@ const char *tq2_status_string(int status);
  */
 int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k, void *stream);
 
+/* Encoder: f32 weights -> TQ2_0_g128 blocks.  (No counterpart on the pages:
+ * their blocks come ready-made from a GGUF file, and they never show how
+ * blocks are produced.  This library reads it as the absmean rule of ternary
+ * weights, with every step that decides a code fixed, so that the bytes are
+ * reproducible exactly.)  For each block of 128 weights of a row:
+ *   gamma = (sum_j |w_j|) / 128, summed in double in index order;
+ *   d     = binary16(gamma), round to nearest even (Inf above 65504);
+ *   code  = clamp(rint(w_j / d), -1, 1) + 1, the quotient in binary32 (IEEE
+ *           division, ties to even); a zero or non-finite d gives code 1.
+ *   w     : device f32 [n, k] row-major, 16-byte aligned, finite
+ *   w_aos : device, n*(k/128)*34 bytes, AoS [N][K/128] blocks, 16-byte
+ *           aligned, must not overlap w (relayout with
+ *           tq2_reformat_aos_to_soa for the matmul entry points)
+ * Errors: TQ2_ERR_BAD_K, TQ2_ERR_INVALID_ARG, TQ2_ERR_MISALIGNED. */
+int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *stream);
+
 /* M = 1 decode GEMV: out[n] = sum_k x[k] * dequant(W)[n,k] (+ residual[n]).
  * The decode-path GEMV `gemv_tq2_g128_v1` of the "oxibonsai-kernels 0.1.5 ...
  * pipelines.rs" page; the operation is the contract above with M = 1.

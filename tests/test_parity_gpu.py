@@ -1,7 +1,7 @@
 """GPU parity: every CUDA entry point against the CPU oracle, through the C ABI.
 
 Bars (per element, Sigma|xw| computed by the oracle in f64):
-  * reformat: bit-exact;
+  * reformat and encoder: bit-exact;
   * f32 kernels (GEMV, small-M, f32ref): |out - ref| <= 1e-5 * Sigma|xw| + 2^-23 |residual|;
   * tensor-core kernel: |out - ref| <= 4e-3 * Sigma|xw| + 2^-23 |residual|, and the
     cosine between each output row and the oracle's row >= 0.9999.
@@ -388,3 +388,64 @@ def test_wait_timeout_ws_kernel(tq2):
     assert st == tq2.TQ2_ERR_TIMEOUT
     check(run_ws(tq2, w, p), p, TOL_TC, cos=True, what="ws after timeout")
     assert tq2.tq2_device_status() == tq2.TQ2_OK
+
+
+# ---------------------------------------------------------------------------
+# encoder (f32 -> blocks): bit-exact against the oracle
+
+
+def _encode(tq2, w, n, k):
+    wd = torch.from_numpy(np.ascontiguousarray(w, dtype=np.float32)).cuda()
+    out = torch.full((tq2.tq2_soa_bytes(n, k),), 0xAB, dtype=torch.uint8, device="cuda")
+    tq2.tq2_quantize_f32(wd, out, n, k)
+    torch.cuda.synchronize()
+    return out.cpu().numpy().reshape(n, k // 128, 34)
+
+
+@pytest.mark.parametrize("n,k,dist", [(1, 128, "normal"), (7, 384, "normal"), (33, 1024, "uniform"),
+                                      (256, 4096, "normal"), (1000, 128, "mixed"),
+                                      (64, 2048, "heavy"), (3, 12288, "normal")])
+def test_quantize_bit_exact(tq2, n, k, dist):
+    rng = np.random.default_rng(7 * n + k)
+    if dist == "normal":
+        w = rng.standard_normal((n, k)) * 0.02
+    elif dist == "uniform":
+        w = rng.uniform(-1.0, 1.0, (n, k))
+    elif dist == "heavy":
+        w = rng.standard_cauchy((n, k))
+    else:  # zeros, tiny and large blocks side by side
+        w = rng.standard_normal((n, k))
+        w[::3] = 0.0
+        w[1::7] *= 1e-7
+        w[2::11] *= 3e4
+    w = w.astype(np.float32)
+    assert np.array_equal(_encode(tq2, w, n, k), oracle.quantize(w, n, k))
+
+
+def test_quantize_special_blocks(tq2):
+    blocks = [np.zeros(128), np.full(128, 1e6), np.array([1.5] * 64 + [0.5] * 32 + [-0.5] * 32),
+              np.full(128, 3e-8), np.array([-0.0] * 128), np.tile([0.75, -0.75], 64),
+              np.r_[np.full(1, 3.0), np.zeros(127)], np.linspace(-2.0, 2.0, 128)]
+    w = np.stack(blocks).astype(np.float32).reshape(1, -1)
+    n, k = 1, w.size
+    assert np.array_equal(_encode(tq2, w, n, k), oracle.quantize(w, n, k))
+
+
+def test_quantize_then_matmul(tq2):
+    rng = np.random.default_rng(21)
+    m, n, k = 64, 300, 1024
+    w = (rng.standard_normal((n, k)) * 0.05).astype(np.float32)
+    aos = _encode(tq2, w, n, k)
+    p = tq2_synth.make_problem(m, n, k, seed=4)
+    p.w_aos[:] = aos
+    check(run(tq2, tq2.TQ2_KERNEL_AUTO, upload(tq2, p), p), p, TOL_TC, cos=True, what="encode + gemm")
+
+
+def test_quantize_empty_and_errors(tq2):
+    w = torch.zeros((2, 256), device="cuda")
+    out = torch.zeros(tq2.tq2_soa_bytes(2, 256), dtype=torch.uint8, device="cuda")
+    tq2.tq2_quantize_f32(w, out, 0, 256)  # no-op
+    with pytest.raises(tq2.TQ2Error):
+        tq2.tq2_quantize_f32(w, out, 2, 100)
+    with pytest.raises(tq2.TQ2Error):
+        tq2.tq2_quantize_f32(w, out.data_ptr() + 1, 2, 256)
