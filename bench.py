@@ -308,7 +308,7 @@ def run_ours(args, world, rank, local, pg):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 in/out; x as 23-bit fixed point per 64-weight segment, int32 (dp4a) ternary dot products, f32 scale and sum",
+        "dtype": "f32 in/out; x as 23-bit fixed point per 32-weight slice, int32 (dp4a) ternary dot products, f32 scale and sum",
         "data": "synthetic (seeded numpy: x~N(0,1), codes P(0)=0.4 P(+-1)=0.3, d=f16(|N(0,0.02)|+1e-4))",
         "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288,
                    "weight_bytes": wbytes, "kernel": "tq2_gemv",

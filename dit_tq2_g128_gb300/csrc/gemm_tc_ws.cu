@@ -645,7 +645,12 @@ ksplit_reduce_kernel(const float *__restrict__ part, int S, int64_t mn, const fl
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+std::mutex g_noalloc_mu;
+uint8_t *g_noalloc_ptr[64];  // device address of the scratch array, per device
+
+}  // namespace
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
     std::call_once(once, [] {
@@ -658,11 +663,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     });
     return fn;
 }
-
-std::mutex g_noalloc_mu;
-uint8_t *g_noalloc_ptr[64];  // device address of the scratch array, per device
-
-}  // namespace
 
 // Fixed scratch of the allocation-free entry point (tq2_gemm_noalloc): the
 // binary16 activation tiles live here instead of in a caller workspace.  Being
@@ -720,7 +720,7 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx) {
     if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return cudaErrorInvalidValue;
     const SoaView v = soa_view(w_soa, n, k);
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap qmap;
     const cuuint64_t gdim[2] = {cuuint64_t(k / 4), cuuint64_t(n)};

@@ -229,38 +229,40 @@ cudaError_t launch_tpl(const void *w_soa, const float *x, const float *residual,
 }
 
 
-constexpr int kGvChunk = 2048;  // weights per warp-chunk (32 lanes x 64)
+constexpr int kGvLaneW = 32;                 // weights per lane: a quarter of a 128-weight block
+constexpr int kGvChunk = 32 * kGvLaneW;      // weights per warp-chunk (1024)
+constexpr int kGvMaxConsumers = 12;          // consumer warps per CTA (three per scheduler)
+constexpr int kGvMaxThreads = 32 * (kGvMaxConsumers + 1);  // + the producer warp
 
 // ---------------------------------------------------------------------------
-// M = 1 decode GEMV (K <= 16384): bulk-copy streaming + integer dot products.
+// M = 1 decode GEMV (K <= 12288): bulk-copy streaming + integer dot products.
 //
 // Memory side.  One CTA per SM owns a contiguous row range, i.e. a contiguous
-// range of the qs plane.  One producer thread streams it into a shared-memory
-// ring with cp.async.bulk (four rows per stage, completion counted on an
-// mbarrier), so the bytes in flight do not depend on per-thread load slots.
+// range of the qs plane.  The producer warp streams it into a shared-memory
+// ring with cp.async.bulk (four rows per stage, with their block scales;
+// completion counted on an mbarrier), so the bytes in flight do not depend on
+// per-thread load slots.  Before waiting for the preceding kernel of the
+// stream it prefetches all of it into L2.
 //
-// Arithmetic.  x is quantised once per CTA, per 64-weight segment, to a signed
-// fixed-point integer X = rint(x * 2^22 / s) with s = max |x| of the segment
-// (|X| <= 2^22), held as three 8-bit limbs (top limb signed).  For one 32-bit
-// code word (16 weights, code i at bits 2i), (w >> 2t) & 0x03030303 gathers
-// the codes of weights t, t+4, t+8, t+12 into four bytes, and dp4a multiplies
-// them with the matching limb bytes and accumulates exactly in int32.  Per row
-// and segment, sum_i (c_i - 1) X_i = sum c*X - sum X is exact; one conversion
-// to f32 and one multiply by s * 2^-22 * d finish the segment.  Per weight this
-// is 3/4 dp4a + 7/16 shift/logic operations instead of the 2 operations of an
-// exact-f32 decode.  The only error is the quantisation of x: per element at
-// most 2^-22 * s (s the segment's max |x|: half a step of 2^-22 * s plus the
-// rounding of the reciprocal); all sums are exact until the final f32 sum over
-// segments.
-// Consumer warps take (row, 2048-weight chunk) items round-robin: each lane
-// owns one 64-weight segment of the chunk, reads its 16 code bytes from the
-// ring and its segment's limbs from shared memory, and the row's 32 lane
-// partials are reduced with shuffles.  Per-(row, chunk) partials meet in
-// shared memory and are summed per row at the end (plus the residual).
-
-constexpr int kSegWords = 52;  // 48 limb words per segment, padded (conflict-free 16-byte reads)
-constexpr int kGvThreads = 512;    // two CTAs per SM (registers, threads and shared memory)
-constexpr int kGvMaxSegs = 256;    // 64-weight segments of x: K <= 16384
+// Arithmetic.  A row is cut into 1024-weight chunks; consumer warp w owns chunk
+// w % C of every row of the stages it takes, and lane l of it the 32 weights
+// [1024 c + 32 l, +32), i.e. a fixed slice of x.  Each lane quantises its own
+// slice once, to a signed fixed-point integer X = rint(x * 2^22 / s) with s =
+// max |x| over the slice (|X| <= 2^22), held in registers as three 8-bit limbs
+// (top limb signed): no shared-memory table and no block-wide barrier between
+// the quantisation and the dot products.  For one 32-bit code word (16
+// weights, code i at bits 2i), (w >> 2t) & 0x03030303 gathers the codes of
+// weights t, t+4, t+8, t+12 into four bytes, and dp4a multiplies them with the
+// matching limb bytes and accumulates exactly in int32.  Per row and slice,
+// sum_i (c_i - 1) X_i = sum c*X - sum X is exact; one conversion to f32 and one
+// multiply by s * 2^-22 * d finish the slice.  Per weight this is 3/4 dp4a +
+// 7/16 shift/logic operations instead of the 2 operations of an exact-f32
+// decode.  The error is the quantisation of x (per element at most 2^-22 * s:
+// half a step plus the rounding of the reciprocal), the rounding of the
+// slice's integer sum to f32 (|sum| <= 2^27) and the f32 sums over slices.
+// The row's 32 lane partials of a chunk are reduced with shuffles;
+// per-(row, chunk) partials meet in shared memory and are summed per row at
+// the end (plus the residual).
 
 __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint32_t bytes,
                                             uint64_t *bar) {
@@ -273,6 +275,15 @@ __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint3
 
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d_gv(uint32_t dst, const CUtensorMap *map, int cx, int cy,
+                                               uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(cx), "r"(cy), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx_gv(uint64_t *bar, uint32_t bytes) {
@@ -294,10 +305,11 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 }
 
 struct GvsParams {
-    int n, k, C;       // rows, K, 2048-weight chunks per row
+    int n, k, C;       // rows, K, 1024-weight chunks per row
     int rbase, rextra; // CTA b owns rbase (+1 if b < rextra) rows starting at b*rbase + min(b, rextra)
-    // shared-memory offsets (bytes), computed on the host
-    uint32_t off_limbs, off_scale, off_sum, off_d, off_partial, off_bar;
+    int xbox_rows, nxbox;  // x arrives as nxbox tensor boxes of xbox_rows 128-byte rows
+    // shared-memory offsets (bytes, from the 1024-aligned base), computed on the host
+    uint32_t off_ring, off_partial, off_bar;
     int rs;            // rows per stage
     int ns;            // ring slots
     int consumers;     // consumer warps = groups * C
@@ -305,36 +317,38 @@ struct GvsParams {
     int rows_cta;      // max rows of a CTA (partial buffer size)
 };
 
-template <int RS>  // rows per stage
-__global__ void __launch_bounds__(kGvThreads, 2)
-gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dpl,
-                   const float *__restrict__ x, const float *residual, float *out, GvsParams P,
+// RS: rows per stage; DBULK: the rows' block scales travel with their stage in
+// the ring (K a multiple of 1024: 16-byte multiples), else they are read from
+// global memory
+template <int RS, bool DBULK>
+__global__ void __launch_bounds__(kGvMaxThreads, 2)
+gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__restrict__ qs,
+                   const __half *__restrict__ dpl, const float *residual, float *out, GvsParams P,
                    unsigned int *status, uint64_t wait_ns) {
-    extern __shared__ __align__(128) uint8_t gvs_smem[];
+    extern __shared__ __align__(128) uint8_t gvs_raw[];
+    // the 128-byte swizzle of the x tile repeats every 1024 bytes: align the base
+    uint8_t *gvs_smem = gvs_raw + ((1024u - (smem_u32(gvs_raw) & 1023u)) & 1023u);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = P.k, C = P.C;
     const int64_t kq = k / 4, kb = k / kBlockW;
-    const int nseg = C * 32;                 // 64-weight segments incl. padding past K
-    const int consumers = P.consumers;       // warps 0 .. consumers-1
+    const int consumers = P.consumers;           // warps 0 .. consumers-1
     const int pwarp = int(blockDim.x >> 5) - 1;  // the producer: the last warp
     const int b = int(blockIdx.x);
     const int R0 = b * P.rbase + min(b, P.rextra);
     const int rows = P.rbase + (b < P.rextra ? 1 : 0);
-    const int nstages = (rows + P.rs - 1) / P.rs;
-    const bool dbulk = (kb % 8) == 0;  // row scales travel with their stage (16-byte multiples)
-    const uint32_t code_bytes = uint32_t(P.rs * kq);
-    const uint32_t stage_bytes = code_bytes + (dbulk ? uint32_t(P.rs * kb * 2) : 0u);
+    const int nstages = (rows + RS - 1) / RS;
+    constexpr bool dbulk = DBULK;
+    const uint32_t code_bytes = uint32_t(RS * kq);
+    const uint32_t stage_bytes = code_bytes + (dbulk ? uint32_t(RS * kb * 2) : 0u);
 
-    // shared memory: [ring][limbs][seg scale][seg sum X][d rows][partials][barriers]
-    uint8_t *ring = gvs_smem;
-    uint32_t *limbs = reinterpret_cast<uint32_t *>(gvs_smem + P.off_limbs);
-    float *sscale = reinterpret_cast<float *>(gvs_smem + P.off_scale);
-    int *ssum = reinterpret_cast<int *>(gvs_smem + P.off_sum);
-    __half *dsm = reinterpret_cast<__half *>(gvs_smem + P.off_d);
+    // shared memory: [x][ring][partials][barriers][abort flag]
+    const float *xs = reinterpret_cast<const float *>(gvs_smem);
+    uint8_t *ring = gvs_smem + P.off_ring;
     float *partial = reinterpret_cast<float *>(gvs_smem + P.off_partial);
     uint64_t *full = reinterpret_cast<uint64_t *>(gvs_smem + P.off_bar);
     uint64_t *empty = full + P.ns;
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + P.ns);
+    uint64_t *xbar = empty + P.ns;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(xbar + 1);
     const uint32_t ring_addr = smem_u32(ring);
 
     // barriers: the lanes of warp 0 initialise them in parallel
@@ -343,226 +357,200 @@ gemv_stream_kernel(const uint8_t *__restrict__ qs, const __half *__restrict__ dp
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 32 * C);
         }
-        if (lane == 0) *abort_flag = 0;
+        if (lane == 0) {
+            mbar_init(xbar, 1);
+            *abort_flag = 0;
+        }
         fence_proxy_async_smem();   // the inits are visible to the copy engine
     }
     __syncthreads();
-    // ---- producer warp, part 1: the first ring-full of stages needs no slot to
-    // free up; its 32 lanes issue those copies in parallel
     const bool producer = warp == pwarp && lane == 0;
     const uint8_t *src = qs + int64_t(R0) * kq;
     const __half *dsrc_rows = dpl + int64_t(R0) * kb;
     auto issue = [&](int st) {
         const int slot = st % P.ns;
-        const int r = min(P.rs, rows - st * P.rs);
+        const int r = min(RS, rows - st * RS);
         const uint32_t bytes = uint32_t(r * kq);
         const uint32_t dbytes = dbulk ? uint32_t(r * kb * 2) : 0u;
         const uint32_t dst = ring_addr + uint32_t(slot) * stage_bytes;
         mbar_expect_tx_gv(&full[slot], bytes + dbytes);
         bulk_g2s_gv(dst, src + int64_t(st) * code_bytes, bytes, &full[slot]);
         if (dbytes)
-            bulk_g2s_gv(dst + code_bytes, dsrc_rows + int64_t(st) * P.rs * kb, dbytes, &full[slot]);
+            bulk_g2s_gv(dst + code_bytes, dsrc_rows + int64_t(st) * RS * kb, dbytes, &full[slot]);
     };
     // The weights go to L2 before waiting for the preceding kernel.  A
     // prefetch cannot leave stale data behind (L2 is the point of coherence,
     // and the copies below read through it after the wait).
     if (warp == pwarp) {
         for (int st = lane; st < nstages; st += 32) {
-            const int r = min(P.rs, rows - st * P.rs);
+            const int r = min(RS, rows - st * RS);
             bulk_prefetch_l2(src + int64_t(st) * code_bytes, uint32_t(r * kq));
-            if (dbulk) bulk_prefetch_l2(dsrc_rows + int64_t(st) * P.rs * kb, uint32_t(r * kb * 2));
+            if (dbulk) bulk_prefetch_l2(dsrc_rows + int64_t(st) * RS * kb, uint32_t(r * kb * 2));
         }
     }
     // Everything a preceding kernel may have written (x, the weights, out and
     // the residual) is touched only after this.
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int first = min(nstages, P.ns);
-    if (warp == pwarp)
-        for (int st = lane; st < first; st += 32) issue(st);
-    // ---- everyone: quantise x per 64-weight segment.  Item (segment, word q,
-    // group t) loads the four consecutive elements 16q + 4t + m (m = 0..3) in
-    // one 16-byte read; 16 items per segment find its max |x| with shuffles.
-    // A 4 x 4 byte transpose among the four items of word q then leaves item
-    // (q, t) with the limb words whose byte m holds weight 16q + 4m + t, the
-    // order in which the dot products unpack the codes.  Items are taken three
-    // passes at a time, loads first.  The producer warp takes no items (it is
-    // busy issuing the copies).
-    const int nthr = nseg * 16;  // a multiple of 512: warp-uniform bounds
-    const int nq = int(blockDim.x) - 32;  // item threads (a multiple of 32)
-#pragma unroll 1
-    for (int p0 = 0; warp != pwarp && p0 * nq < nthr; p0 += 3) {  // warp-uniform
-        float4 xv[3];
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp) {
-            const int qi = int(threadIdx.x) + (p0 + pp) * nq;
-            const int kk = (qi >> 4) * 64 + 16 * ((qi >> 2) & 3) + 4 * (qi & 3);
-            xv[pp] = (qi < nthr && kk < k) ? __ldg(reinterpret_cast<const float4 *>(x + kk))
-                                           : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        // the three items' shuffle chains are interleaved step by step
-        float m[3], xe[3][4];
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp) {
-            xe[pp][0] = xv[pp].x; xe[pp][1] = xv[pp].y; xe[pp][2] = xv[pp].z; xe[pp][3] = xv[pp].w;
-            m[pp] = fmaxf(fmaxf(fabsf(xe[pp][0]), fabsf(xe[pp][1])), fmaxf(fabsf(xe[pp][2]), fabsf(xe[pp][3])));
-        }
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-            for (int pp = 0; pp < 3; ++pp) m[pp] = fmaxf(m[pp], __shfl_xor_sync(0xffffffffu, m[pp], o));
-        uint32_t r[3][3];  // item pp, limb l: weight 16q + 4t + mm in byte mm
-        int sx[3];
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp) {
-            // 2^22 / s: the correctly rounded reciprocal times 2^22 (exact
-            // scaling), i.e. the correctly rounded quotient
-            const float inv = m[pp] > 0.f ? __frcp_rn(m[pp]) * 4194304.0f : 0.f;
-            r[pp][0] = r[pp][1] = r[pp][2] = 0;
-            sx[pp] = 0;
-#pragma unroll
-            for (int mm = 0; mm < 4; ++mm) {
-                // |X| <= 2^22 (the rounded reciprocal may overshoot by half an ulp)
-                const int X = max(-4194304, min(4194304, __float2int_rn(xe[pp][mm] * inv)));
-                sx[pp] += X;
-                r[pp][0] |= uint32_t(X & 0xFF) << (8 * mm);
-                r[pp][1] |= uint32_t((X >> 8) & 0xFF) << (8 * mm);
-                r[pp][2] |= uint32_t((X >> 16) & 0xFF) << (8 * mm);
-            }
-        }
-#pragma unroll
-        for (int o = 8; o >= 1; o >>= 1)
-#pragma unroll
-            for (int pp = 0; pp < 3; ++pp) sx[pp] += __shfl_xor_sync(0xffffffffu, sx[pp], o);
-        // transpose: item t gathers byte t of the four items' words of word q
-        const int qt = int(threadIdx.x) & 3;
-        uint32_t h[3][3];
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp)
-#pragma unroll
-            for (int l = 0; l < 3; ++l) {
-                const uint32_t o1 = __shfl_xor_sync(0xffffffffu, r[pp][l], 1);
-                h[pp][l] = (qt & 1) ? __byte_perm(r[pp][l], o1, 0x3715) : __byte_perm(r[pp][l], o1, 0x6240);
-            }
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp)
-#pragma unroll
-            for (int l = 0; l < 3; ++l) {
-                const uint32_t o2 = __shfl_xor_sync(0xffffffffu, h[pp][l], 2);
-                r[pp][l] = (qt & 2) ? __byte_perm(h[pp][l], o2, 0x3276) : __byte_perm(h[pp][l], o2, 0x5410);
-            }
-#pragma unroll
-        for (int pp = 0; pp < 3; ++pp) {
-            const int qi = int(threadIdx.x) + (p0 + pp) * nq;
-            if (qi < nthr) {
-                const int qseg = qi >> 4, qq = (qi >> 2) & 3;
-                uint32_t *lw = limbs + qseg * kSegWords + (qq * 4 + qt) * 3;
-                lw[0] = r[pp][0];
-                lw[1] = r[pp][1];
-                lw[2] = r[pp][2];
-                if ((qi & 15) == 0) {
-                    sscale[qseg] = m[pp] * (1.0f / 4194304.0f);  // s * 2^-22
-                    ssum[qseg] = sx[pp];
-                }
-            }
-        }
-    }
-    if (!dbulk) {
-        const unsigned short *dsrc = reinterpret_cast<const unsigned short *>(dpl + int64_t(R0) * kb);
-        unsigned short *ddst = reinterpret_cast<unsigned short *>(dsm);
-        for (int64_t i = threadIdx.x; i < int64_t(rows) * kb; i += blockDim.x) ddst[i] = dsrc[i];
-    }
-    __syncthreads();
-
-    // Programmatic dependent launch: once this CTA holds x and has its
-    // weight copies in flight, the next kernel of the stream may start
-    // launching.  Two CTAs of this kernel fit on one SM, so the next call's
-    // set-up and weight prefetch overlap this call's arithmetic (which needs
-    // no memory bandwidth); the next call reads nothing a predecessor may
-    // write before its own griddepcontrol.wait.
+    // Programmatic dependent launch: the next kernel of the stream may start
+    // launching now.  Two CTAs of this kernel fit on one SM, so the next
+    // call's set-up and weight prefetch overlap this call's arithmetic (which
+    // needs no memory bandwidth); the next call reads nothing a predecessor
+    // may write before its own griddepcontrol.wait.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    if (producer) {
-        // ---- producer, part 2: refill slots as the consumers release them
-        for (int st = P.ns; st < nstages; ++st) {
-            const int slot = st % P.ns, u = st / P.ns;
-            if (!mbar_wait_bounded(&empty[slot], (u - 1) & 1, wait_ns, status)) {
-                *abort_flag = 1;
-                break;
-            }
-            if (*abort_flag) break;
-            issue(st);
+    if (warp == pwarp) {
+        // x first: one tensor copy per box of 128-byte rows (32 elements), each
+        // row's 16-byte pieces permuted by the 128-byte swizzle (piece i of row
+        // r lands at piece i ^ (r % 8)), so that the consumers' reads below are
+        // free of bank conflicts.  Rows past K arrive as zeros.
+        if (lane == 0) {
+            mbar_expect_tx_gv(xbar, uint32_t(P.nxbox * P.xbox_rows * 128));
+            for (int bx = 0; bx < P.nxbox; ++bx)
+                tma_load_2d_gv(smem_u32(gvs_smem) + uint32_t(bx * P.xbox_rows * 128), &xmap, 0,
+                               bx * P.xbox_rows, xbar);
         }
-        // every copy issued must land before the CTA exits: the last round of each slot
-        const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
-        for (int st = max(0, nstages - P.ns); st < nstages; ++st)
-            mbar_wait_bounded(&full[st % P.ns], (st / P.ns) & 1, drain, status);
-    }
-    if (warp < consumers) {
-        // Warp w takes chunk w % C of the stages st = g, g + groups, ... (g = w / C).
-        // The ring size is a multiple of `groups`, so every slot is only ever
-        // touched by one group, in stage order: no warp can wait on a slot's
-        // next round before the group released the current one.
+        // the first ring-full of stages needs no slot to free up: the 32 lanes
+        // issue those copies in parallel; lane 0 then refills slots as the
+        // consumers release them
+        const int first = min(nstages, P.ns);
+        for (int st = lane; st < first; st += 32) issue(st);
+        if (producer) {
+            for (int st = P.ns; st < nstages; ++st) {
+                const int slot = st % P.ns, u = st / P.ns;
+                if (!mbar_wait_bounded(&empty[slot], (u - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                issue(st);
+            }
+            // every copy issued must land before the CTA exits: the last round of each slot
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            for (int st = max(0, nstages - P.ns); st < nstages; ++st)
+                mbar_wait_bounded(&full[st % P.ns], (st / P.ns) & 1, drain, status);
+        }
+    } else if (warp < consumers) {
+        // Warp w takes chunk c = w % C of the stages st = g, g + groups, ...
+        // (g = w / C).  The ring size is a multiple of `groups`, so every slot
+        // is only ever touched by one group, in stage order: no warp can wait
+        // on a slot's next round before the group released the current one.
         const int g = warp / C, c = warp % C;
-        const int seg = c * 32 + lane;
-        const int kw0 = seg * 64;
+        const int kw0 = c * kGvChunk + lane * kGvLaneW;
         const bool active = kw0 < k;
         const int kw_rd = active ? kw0 : 0;
+        // ---- quantise this lane's 32 elements of x into three limbs.
+        // L[q][t][l] holds in byte i limb l of X[16q + t + 4i], the order in
+        // which a code word unpacks (bytes of (w >> 2t) & 0x03030303).
+        uint32_t L[2][4][3];
+        int sx = 0;
+        float sc;
+        if (!mbar_wait_bounded(xbar, 0, wait_ns, status)) *abort_flag = 1;
+        {
+            float xv[kGvLaneW];
+            const int xrow = kw_rd / kGvLaneW;  // this lane's 128-byte row of the x tile
+#pragma unroll
+            for (int i = 0; i < kGvLaneW / 4; ++i) {
+                const float4 v = active ? *reinterpret_cast<const float4 *>(xs + xrow * 32 + ((i ^ (xrow & 7)) << 2))
+                                        : make_float4(0.f, 0.f, 0.f, 0.f);
+                xv[4 * i + 0] = v.x;
+                xv[4 * i + 1] = v.y;
+                xv[4 * i + 2] = v.z;
+                xv[4 * i + 3] = v.w;
+            }
+            float s = 0.f;
+#pragma unroll
+            for (int j = 0; j < kGvLaneW; ++j) s = fmaxf(s, fabsf(xv[j]));
+            // 2^22 / s: the correctly rounded reciprocal times 2^22 (exact scaling)
+            const float inv = s > 0.f ? __frcp_rn(s) * 4194304.0f : 0.f;
+            // X = x * inv rounded to the nearest integer (ties to even) by one
+            // fused multiply-add onto 1.5 * 2^23: the sum lies in [2^23, 2^24),
+            // where the binary32 spacing is 1, so the low mantissa bits hold
+            // X + 2^22.  |x * inv| <= 2^22 + 2^-2 (the reciprocal is within half
+            // an ulp), so |X| <= 2^22 without a clamp.
+            int X[kGvLaneW];
+#pragma unroll
+            for (int j = 0; j < kGvLaneW; ++j) {
+                X[j] = __float_as_int(__fmaf_rn(xv[j], inv, 12582912.0f)) - 0x4B400000;
+                sx += X[j];
+            }
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t x0 = uint32_t(X[16 * q + t]), x1 = uint32_t(X[16 * q + t + 4]);
+                    const uint32_t x2 = uint32_t(X[16 * q + t + 8]), x3 = uint32_t(X[16 * q + t + 12]);
+                    const uint32_t p01 = __byte_perm(x0, x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1
+                    const uint32_t p23 = __byte_perm(x2, x3, 0x5140);
+                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);        // byte 0 of x0..x3
+                    L[q][t][1] = __byte_perm(p01, p23, 0x7632);        // byte 1
+                    const uint32_t h01 = __byte_perm(x0, x1, 0x0062);  // x0.b2 x1.b2
+                    const uint32_t h23 = __byte_perm(x2, x3, 0x0062);
+                    L[q][t][2] = __byte_perm(h01, h23, 0x5410);        // byte 2 (signed)
+                }
+            sc = s * (1.0f / 4194304.0f);  // s * 2^-22
+        }
+        // loop-invariant 32-bit shared-memory offsets of this lane's data in a
+        // slot: code bytes of row u at code_off + u * kq, the row's block scale
+        // at d_off + u * kb * 2
+        const uint32_t kq32 = uint32_t(kq), kb2 = uint32_t(kb) * 2;
+        const uint32_t code_off = uint32_t(kw_rd / 4);
+        const uint32_t d_off = code_bytes + uint32_t(kw_rd / kBlockW) * 2;
+        const int64_t dcol = kw_rd / kBlockW;
+        int slot = g, ph = 0;  // ring slot and phase of stage st, advanced incrementally
         for (int st = g; st < nstages; st += P.groups) {
-            const int slot = st % P.ns, u = st / P.ns;
-            if (!mbar_wait_bounded(&full[slot], u & 1, wait_ns, status)) {
+            if (!mbar_wait_bounded(&full[slot], uint32_t(ph), wait_ns, status)) {
                 *abort_flag = 1;
                 break;
             }
             if (*abort_flag) break;
-            const int r0 = st * P.rs;                 // first row (CTA-relative) of the stage
-            const int nv = min(P.rs, rows - r0);      // warp-uniform, >= 1
-            const uint8_t *base = ring + size_t(slot) * stage_bytes + kw_rd / 4;
-            const __half *sd = dbulk ? reinterpret_cast<const __half *>(ring + size_t(slot) * stage_bytes + code_bytes)
-                                     : dsm + int64_t(r0) * kb;  // this stage's row scales
-            // each lane's 16 code bytes of a row in one conflict-free 16-byte read
-            uint4 cw[RS];
+            const int r0 = st * RS;             // first row (CTA-relative) of the stage
+            const int nv = min(RS, rows - r0);  // warp-uniform, >= 1
+            const uint8_t *sb = ring + uint32_t(slot) * stage_bytes;
+            // Each lane's 8 code bytes of a row in one 8-byte read (a warp reads
+            // 256 contiguous bytes: conflict-free) and the row's block scale.
+            // All RS rows of the slot are read: rows past nv (the CTA's last
+            // stage) hold stale bytes of the slot and their results are dropped.
+            uint2 cw[RS];
+            float d[RS];
 #pragma unroll
-            for (int uu = 0; uu < RS; ++uu)
-                cw[uu] = *reinterpret_cast<const uint4 *>(base + size_t(uu < nv ? uu : nv - 1) * kq);
-            int a0[RS], a1[RS], a2[RS];
-#pragma unroll
-            for (int uu = 0; uu < RS; ++uu) a0[uu] = a1[uu] = a2[uu] = 0;
-            const uint4 *lw = reinterpret_cast<const uint4 *>(limbs + seg * kSegWords);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                // limb words (q, t, l) for t = 0..3, l = 0..2: 12 words
-                const uint4 L0 = lw[3 * q + 0], L1 = lw[3 * q + 1], L2 = lw[3 * q + 2];
-                const uint32_t lv[12] = {L0.x, L0.y, L0.z, L0.w, L1.x, L1.y, L1.z, L1.w,
-                                         L2.x, L2.y, L2.z, L2.w};
-#pragma unroll
-                for (int uu = 0; uu < RS; ++uu) {
-                    const uint32_t wq = q == 0 ? cw[uu].x : q == 1 ? cw[uu].y : q == 2 ? cw[uu].z : cw[uu].w;
-#pragma unroll
-                    for (int t = 0; t < 4; ++t) {
-                        const uint32_t v = (wq >> (2 * t)) & 0x03030303u;
-                        a0[uu] = dp4a_uu(v, lv[3 * t + 0], a0[uu]);
-                        a1[uu] = dp4a_uu(v, lv[3 * t + 1], a1[uu]);
-                        a2[uu] = dp4a_us(v, lv[3 * t + 2], a2[uu]);
-                    }
-                }
+            for (int uu = 0; uu < RS; ++uu) {
+                cw[uu] = *reinterpret_cast<const uint2 *>(sb + code_off + uint32_t(uu) * kq32);
+                d[uu] = dbulk ? __half2float(*reinterpret_cast<const __half *>(sb + d_off + uint32_t(uu) * kb2))
+                              : (uu < nv ? __half2float(__ushort_as_half(ldg_u16(dsrc_rows + int64_t(r0 + uu) * kb + dcol)))
+                                         : 0.f);
             }
             // every lane has read its codes: release this chunk's share of the slot
             mbar_arrive(&empty[slot]);
-            const float sc = active ? sscale[seg] : 0.f;
-            const int sx = active ? ssum[seg] : 0;
-            float v[RS];
+            // the rows' 3 * RS accumulator chains advance together
+            int a0[RS], a1[RS], a2[RS];
 #pragma unroll
-            for (int uu = 0; uu < RS; ++uu) {
-                const int ur = uu < nv ? uu : nv - 1;
-                const int tot = a2[uu] * 65536 + a1[uu] * 256 + a0[uu] - sx;
-                const float d = __half2float(sd[int64_t(ur) * kb + kw_rd / kBlockW]);
-                v[uu] = float(tot) * (sc * d);
+            for (int uu = 0; uu < RS; ++uu) a0[uu] = a1[uu] = a2[uu] = 0;
+#pragma unroll
+            for (int q = 0; q < 2; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t)
+#pragma unroll
+                    for (int uu = 0; uu < RS; ++uu) {
+                        const uint32_t wq = q == 0 ? cw[uu].x : cw[uu].y;
+                        const uint32_t cv = (wq >> (2 * t)) & 0x03030303u;
+                        a0[uu] = dp4a_uu(cv, L[q][t][0], a0[uu]);
+                        a1[uu] = dp4a_uu(cv, L[q][t][1], a1[uu]);
+                        a2[uu] = dp4a_us(cv, L[q][t][2], a2[uu]);
+                    }
+            constexpr int V = RS <= 2 ? 2 : RS <= 4 ? 4 : 8;  // reduction width (power of two)
+            float v[V];
+#pragma unroll
+            for (int uu = 0; uu < V; ++uu) {
+                const int tot = uu < RS ? (a2[uu] << 16) + (a1[uu] << 8) + a0[uu] - sx : 0;
+                v[uu] = uu < RS ? float(tot) * (sc * d[uu]) : 0.f;
             }
-            butterfly<RS>(v, lane);
-            constexpr int G = 32 / RS;
+            butterfly<V>(v, lane);
+            constexpr int G = 32 / V;
             if (lane % G == 0) {
                 const int uu = lane / G;
-                if (uu < nv) partial[(r0 + uu) * C + c] = v[0];
+                if (uu < RS && uu < nv) partial[(r0 + uu) * C + c] = v[0];
             }
+            slot += P.groups;
+            if (slot >= P.ns) slot -= P.ns, ph ^= 1;
         }
     }
     __syncthreads();
@@ -581,32 +569,46 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
                                float *out, int64_t n, int64_t k, const LaunchCtx &ctx) {
     const int C = int((k + kGvChunk - 1) / kGvChunk);
     const int64_t kq = k / 4, kb = k / kBlockW;
-    if (C > 30) return cudaErrorNotSupported;
+    if (C > kGvMaxConsumers) return cudaErrorNotSupported;
     GvsParams P;
     P.n = int(n);
     P.k = int(k);
     P.C = C;
-    P.rs = 4;
-    const int threads = kGvThreads;  // consumer warps, the producer warp, one spare
-    P.groups = std::max(1, (threads / 32 - 2) / C);  // consumer warp groups of C warps (one per chunk)
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + P.rs - 1) / P.rs));
+    P.groups = std::max(1, kGvMaxConsumers / C);  // consumer warp groups of C warps (one per chunk)
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + 7) / 8));
     P.rbase = int(n / grid);
     P.rextra = int(n % grid);
     P.rows_cta = P.rbase + (P.rextra ? 1 : 0);
-    const int nseg = C * 32;
+    // Rows per stage: a group's time is (its stages) x (RS rows + a per-stage
+    // cost of about two rows); pick the RS in [2, 8] that minimises it for the
+    // CTA's row count (ties: more rows per stage).
+    {
+        int best = 8;
+        long best_cost = LONG_MAX;
+        for (int rs = 8; rs >= 2; --rs) {
+            const long nst_rs = (P.rows_cta + rs - 1) / rs;
+            const long cost = ((nst_rs + P.groups - 1) / P.groups) * (rs + 2);
+            if (cost < best_cost) best_cost = cost, best = rs;
+        }
+        P.rs = best;
+    }
     const bool dbulk = (kb % 8) == 0;  // scales travel with their stage in the ring
     const size_t stage_bytes = size_t(P.rs) * kq + (dbulk ? size_t(P.rs) * kb * 2 : 0);
-    const size_t dsm_bytes = dbulk ? 0 : size_t((int64_t(P.rows_cta) * kb + 7) & ~int64_t(7)) * 2;
-    const size_t lwords = size_t(nseg) * kSegWords;
-    if (nseg > kGvMaxSegs) return cudaErrorNotSupported;
-    const size_t fixed = lwords * 4 + size_t(nseg) * 8 + dsm_bytes +
-                         size_t((P.rows_cta * C + 1) & ~1) * 4;
-    const size_t budget = 108 * 1024;  // two CTAs per SM
-    if (fixed + stage_bytes + 64 * 16 + 32 > budget) return cudaErrorNotSupported;
+    const size_t partial_bytes = size_t((P.rows_cta * C + 1) & ~1) * 4;
+    // x as a tensor of K/32 rows of 128 bytes, in boxes of at most 256 rows
+    // (a multiple of 8 rows: every box starts on a 1024-byte swizzle atom)
+    const int xrows = int(k / kGvLaneW);
+    P.nxbox = (xrows + 255) / 256;
+    P.xbox_rows = (((xrows + P.nxbox - 1) / P.nxbox) + 7) & ~7;
+    const size_t x_bytes = size_t(P.nxbox) * P.xbox_rows * 128;
+    // two CTAs per SM: 2 * (this + 1 KB reserved per CTA) within 228 KB
+    const size_t budget = 112 * 1024;
+    const size_t fixed = 1024 + x_bytes + partial_bytes + 64 * 16 + 32;
+    if (fixed + stage_bytes > budget) return cudaErrorNotSupported;
     // ring: enough slots for all of a CTA's stages if shared memory allows (no
     // refill round trips), as a multiple of the group count
     const int nst = (P.rows_cta + P.rs - 1) / P.rs;
-    const int max_slots = int(std::min<size_t>(64, (budget - fixed - 64 * 16 - 32) / stage_bytes));
+    const int max_slots = int(std::min<size_t>(64, (budget - fixed) / stage_bytes));
     int ns = std::min(max_slots, ((nst + P.groups - 1) / P.groups) * P.groups);
     ns = (ns / P.groups) * P.groups;
     if (ns < P.groups) {  // fewer slots than groups: shrink the groups
@@ -615,18 +617,40 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     }
     P.ns = ns;
     P.consumers = P.groups * C;
-    P.off_limbs = uint32_t(size_t(ns) * stage_bytes);
-    P.off_scale = uint32_t(P.off_limbs + lwords * 4);
-    P.off_sum = uint32_t(P.off_scale + size_t(nseg) * 4);
-    P.off_d = uint32_t(P.off_sum + size_t(nseg) * 4);
-    P.off_partial = uint32_t(P.off_d + dsm_bytes);
-    P.off_bar = uint32_t(P.off_partial + size_t((P.rows_cta * C + 1) & ~1) * 4);
-    const size_t smem = size_t(P.off_bar) + size_t(2 * ns) * 8 + 16;
-    cudaError_t e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    P.off_ring = uint32_t(x_bytes);
+    P.off_partial = uint32_t(x_bytes + size_t(ns) * stage_bytes);
+    P.off_bar = uint32_t((P.off_partial + partial_bytes + 7) & ~size_t(7));
+    const size_t smem = 1024 + size_t(P.off_bar) + size_t(2 * ns + 1) * 8 + 16;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap xmap;
+    {
+        const cuuint64_t gdim[2] = {cuuint64_t(kGvLaneW), cuuint64_t(xrows)};
+        const cuuint64_t gstride[1] = {cuuint64_t(kGvLaneW) * 4};
+        const cuuint32_t box[2] = {cuuint32_t(kGvLaneW), cuuint32_t(P.xbox_rows)};
+        const cuuint32_t estride[2] = {1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float *>(x), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    const int threads = 32 * (P.consumers + 1);  // consumer warps and the producer warp
+    void (*kern)(const CUtensorMap, const uint8_t *, const __half *, const float *, float *, GvsParams,
+                 unsigned int *, uint64_t) = nullptr;
+    switch (P.rs) {
+        case 2: kern = dbulk ? gemv_stream_kernel<2, true> : gemv_stream_kernel<2, false>; break;
+        case 3: kern = dbulk ? gemv_stream_kernel<3, true> : gemv_stream_kernel<3, false>; break;
+        case 4: kern = dbulk ? gemv_stream_kernel<4, true> : gemv_stream_kernel<4, false>; break;
+        case 5: kern = dbulk ? gemv_stream_kernel<5, true> : gemv_stream_kernel<5, false>; break;
+        case 6: kern = dbulk ? gemv_stream_kernel<6, true> : gemv_stream_kernel<6, false>; break;
+        case 7: kern = dbulk ? gemv_stream_kernel<7, true> : gemv_stream_kernel<7, false>; break;
+        default: kern = dbulk ? gemv_stream_kernel<8, true> : gemv_stream_kernel<8, false>; break;
+    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // the largest shared-memory carve-out, so that two CTAs fit on an SM
-    e = cudaFuncSetAttribute(gemv_stream_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     const SoaView v = soa_view(w_soa, n, k);
     // programmatic dependent launch (see the kernel): the launch may begin
@@ -641,13 +665,13 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemv_stream_kernel<4>, v.qs, v.d, x, residual, out, P, ctx.status,
+    return cudaLaunchKernelEx(&cfg, kern, xmap, v.qs, v.d, residual, out, P, ctx.status,
                               ctx.wait_ns);
 }
 
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
                         int64_t n, int64_t k, const LaunchCtx &ctx) {
-    if (k <= 16384 && n <= INT32_MAX) {
+    if (k <= int64_t(kGvMaxConsumers) * kGvChunk && n <= INT32_MAX) {
         cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, ctx);
         if (e != cudaErrorNotSupported) return e;
         (void)cudaGetLastError();

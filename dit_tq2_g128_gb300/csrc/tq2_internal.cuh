@@ -4,6 +4,8 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -57,6 +59,9 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
 constexpr size_t kNoAllocScratchBytes = size_t(TQ2_NOALLOC_SCRATCH_BYTES);
 cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
                               int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
+
+// The driver's cuTensorMapEncodeTiled (null if the driver lacks it).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // Largest M the small-M CUDA-core kernel handles.
 constexpr int64_t kSkinnyMaxM = 16;

@@ -125,13 +125,13 @@ int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *st
  *   x        : device f32 [k], finite
  *   residual : device f32 [n], or NULL
  *   out      : device f32 [n]
- * Arithmetic (k <= 16384): x is quantised per 64-weight segment to a signed
- * fixed-point integer relative to the segment's largest |x| (23 bits:
- * |x - xq| <= 2^-22 * max|x_segment|); the ternary dot products are then
- * exact integer sums, scaled by max|x_segment| * 2^-22 * d and summed in f32.
- * Per element: |error| <= sum over segments of 2^-22 * max|x_seg| * sum_seg |w|
- * plus f32 rounding of the final sum.  For k > 16384: exact f32 products and
- * f32 accumulation. */
+ * Arithmetic (k <= 12288): x is quantised per 32-weight slice to a signed
+ * fixed-point integer relative to the slice's largest |x| (23 bits:
+ * |x - xq| <= 2^-22 * max|x_slice|); the ternary dot products are then exact
+ * integer sums, scaled by max|x_slice| * 2^-22 * d and summed in f32.
+ * Per element: |error| <= sum over slices of 2^-22 * max|x_slice| * sum_slice |w|
+ * plus f32 rounding of the slice sums and of the final sum.  For k > 12288:
+ * exact f32 products and f32 accumulation. */
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t n, int64_t k, void *stream);
 
