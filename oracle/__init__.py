@@ -16,7 +16,10 @@ closed forms (all +1, all 0, all -1, alternating signs, every single-code
 position); the contraction against ``numpy.matmul`` of the dequantised matrix;
 invariants (linearity, negation, exact doubling under d*2, row-wise equals
 batched, residual passthrough) and the SoA layout on a hand-built example plus
-the AoS->SoA->AoS round trip.
+the AoS->SoA->AoS round trip.  The gate/up SwiGLU (``swiglu``) is pinned by
+the closed form silu(ln 3) = 0.75 ln 3, the odd identity silu(z) - silu(-z) = z
+(flipping every gate code), zero gate or up rows, exact linearity in the up
+rows and the limits silu(z) -> z and -> 0.
 """
 
 from __future__ import annotations
@@ -182,3 +185,31 @@ def quantize(w, n: int, k: int) -> np.ndarray:
     if lib().tq2o_quantize(_ptr(w), n, k, _ptr(out)) == -1:
         raise ValueError(f"tq2o_quantize: k={k} is not a positive multiple of 128")
     return out
+
+
+def silu(z):
+    """SiLU in float64: z * sigmoid(z) = z / (1 + exp(-z)) (the element-wise
+    activation the pages dispatch as ``silu_f32``, "oxibonsai-kernels 0.1.5
+    src/gpu_backend/metal_graph/pipelines.rs", FLUX.2 VAE primitives)."""
+    z = np.asarray(z, dtype=np.float64)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu(w_aos, x, *, f: int, k: int, rows=None):
+    """Fused gate/up projection with the SwiGLU activation, float64.
+
+    The TQ2 analogue of the pages' ``fused_gate_up_swiglu_q1`` /
+    ``fused_gate_up_swiglu_gemm_q1`` pipelines ("oxibonsai-kernels 0.1.5
+    src/gpu_backend/metal_graph/pipelines.rs", decode and prefill fields),
+    which the pages name without a listing.  Reading: the weight holds 2f rows,
+    the gate projection in rows [0, f) and the up projection in rows [f, 2f);
+    for each input row, g = x . W_gate^T, u = x . W_up^T and
+    h = silu(g) * u, f values.
+
+    Returns (h, g, u, absdot_g, absdot_u), each [len(rows) or M, f]; the
+    absdot arrays are sum_k |x w| of the gate and up rows (the tolerance scales).
+    """
+    out, absdot = matmul(w_aos, x, n=2 * f, k=k, rows=rows)
+    g, u = out[:, :f], out[:, f:]
+    return silu(g) * u, g, u, absdot[:, :f], absdot[:, f:]

@@ -383,3 +383,85 @@ def test_quantize_scaling_and_layout():
 def test_quantize_bad_k():
     with pytest.raises(ValueError):
         oracle.quantize(np.zeros((1, 100), np.float32), 1, 100)
+
+
+# --------------------------------------------------------------------------
+# gate/up SwiGLU
+
+HALF_1 = 0x3C00  # 1.0
+
+
+def _one_hot_block(pos, d_bits, code=2):
+    """A block whose weight `pos` has code `code` and every other weight code 1 (zero)."""
+    qs = np.full(32, 0x55, dtype=np.uint8)
+    byte, shift = pos // 4, 2 * (pos % 4)
+    qs[byte] = np.uint8(((int(qs[byte]) & ~(3 << shift)) & 0xFF) | (code << shift))
+    return block(qs, d_bits)
+
+
+def test_silu_closed_form_ln3():
+    # sigmoid(ln 3) = 3/4
+    z = np.log(3.0)
+    assert abs(float(oracle.silu(z)) - 0.75 * z) < 1e-15
+    assert abs(float(oracle.silu(-z)) - (-0.25 * z)) < 1e-15
+
+
+def test_swiglu_hand_built_ln3():
+    # f = 1, k = 128: gate row selects x[0] (d = 1), up row selects x[1] (d = 1)
+    w = weight([_one_hot_block(0, HALF_1), _one_hot_block(1, HALF_1)], 2, 128)
+    x = np.zeros((1, 128), dtype=np.float32)
+    x[0, 0] = np.float32(np.log(3.0))
+    x[0, 1] = 2.5
+    h, g, u, _, _ = oracle.swiglu(w, x, f=1, k=128)
+    assert g[0, 0] == float(np.float32(np.log(3.0))) and u[0, 0] == 2.5
+    # silu(z) for z within 2^-24 relative of ln 3: 0.75 * ln 3 * 2.5 to ~1e-7
+    assert abs(h[0, 0] - 0.75 * np.log(3.0) * 2.5) < 1e-7 * abs(h[0, 0])
+
+
+def test_swiglu_odd_identity_pins_gate_and_up_roles():
+    # flipping every gate code (c -> 2 - c) negates g exactly; since
+    # silu(z) - silu(-z) = z, h(W) - h(W') = g * u.  Swapped gate/up roles or a
+    # different activation break this.
+    f, k = 24, 384
+    p = tq2_synth.make_problem(3, 2 * f, k, seed=11)
+    w = np.array(p.w_aos, copy=True).reshape(2 * f, k // 128, 34)
+    w_flip = w.copy()
+    qs = w_flip[:f, :, :32]
+    c = np.stack([(qs >> (2 * t)) & 3 for t in range(4)], axis=-1)
+    c = 2 - c
+    w_flip[:f, :, :32] = (c[..., 0] | (c[..., 1] << 2) | (c[..., 2] << 4) | (c[..., 3] << 6)).astype(np.uint8)
+    h, g, u, sg, su = oracle.swiglu(w, p.x, f=f, k=k)
+    h2, g2, u2, _, _ = oracle.swiglu(w_flip, p.x, f=f, k=k)
+    assert np.array_equal(g2, -g) and np.array_equal(u2, u)
+    assert np.allclose(h - h2, g * u, rtol=1e-12, atol=1e-12 * np.max(np.abs(g * u)))
+
+
+def test_swiglu_zero_rows_and_linearity_in_up():
+    f, k = 8, 256
+    p = tq2_synth.make_problem(2, 2 * f, k, seed=12)
+    w = np.array(p.w_aos, copy=True).reshape(2 * f, k // 128, 34)
+    z_up = w.copy()
+    z_up[f:, :, :32] = 0x55
+    assert np.array_equal(oracle.swiglu(z_up, p.x, f=f, k=k)[0], np.zeros((2, f)))
+    z_gate = w.copy()
+    z_gate[:f, :, :32] = 0x55
+    assert np.array_equal(np.abs(oracle.swiglu(z_gate, p.x, f=f, k=k)[0]), np.zeros((2, f)))
+    # doubling every up scale (exact in binary16) doubles h exactly
+    dbl = w.copy()
+    d = dbl[f:, :, 32].astype(np.uint16) | (dbl[f:, :, 33].astype(np.uint16) << 8)
+    d2 = (d.view(np.float16).astype(np.float32) * 2).astype(np.float16).view(np.uint16)
+    dbl[f:, :, 32] = (d2 & 0xFF).astype(np.uint8)
+    dbl[f:, :, 33] = (d2 >> 8).astype(np.uint8)
+    h = oracle.swiglu(w, p.x, f=f, k=k)[0]
+    assert np.array_equal(oracle.swiglu(dbl, p.x, f=f, k=k)[0], 2 * h)
+
+
+def test_swiglu_limits():
+    # gate = +-40 (x = 40, d = 1): h = 40 u (sigmoid(40) = 1 - 4e-18) and |h| < 1e-15 |u|
+    w = weight([_one_hot_block(0, HALF_1), _one_hot_block(1, HALF_1)], 2, 128)
+    x = np.zeros((2, 128), dtype=np.float32)
+    x[:, 1] = 3.0
+    x[0, 0], x[1, 0] = 40.0, -40.0
+    h = oracle.swiglu(w, x, f=1, k=128)[0]
+    assert abs(h[0, 0] - 120.0) < 1e-12
+    assert abs(h[1, 0]) < 1e-15 * 3.0
