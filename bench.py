@@ -482,14 +482,49 @@ def run_suite(args, local):
         torch.cuda.empty_cache()
         return rec, t
 
+    def one_swiglu(name, p, f, steps, sample_rows):
+        """Fused gate/up + SwiGLU (2f weight rows, out [m, f]); error reported
+        relative to the bound's scale 1.1*S_g*|u| + |silu(g)|*S_u (S = sum|xw|)."""
+        wbytes = tq2.tq2_soa_bytes(p.n, p.k)
+        per = wbytes + p.m * p.k * 4 + p.m * f * 4
+        c = max(2, -(-2 * l2 // per) + 1) if per < l2 else 1
+        w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
+        ws = [w0] + [w0.clone() for _ in range(c - 1)]
+        x = torch.from_numpy(p.x).to(device)
+        outs = [torch.empty((p.m, f), dtype=torch.float32, device=device) for _ in range(c)]
+        t = timed(lambda i: tq2.tq2_gate_up_swiglu(ws[i % c], x, outs[i % c], p.m, f, p.k), steps)
+        tq2.tq2_gate_up_swiglu(ws[0], x, outs[0], p.m, f, p.k)
+        torch.cuda.synchronize()
+        assert tq2.tq2_device_status() == tq2.TQ2_OK
+        rows = sample(p.m, sample_rows) if p.m > sample_rows else np.arange(p.m)
+        t0 = time.perf_counter()
+        h, g, u, sg, su = oracle.swiglu(p.w_aos, p.x, f=f, k=p.k, rows=rows)
+        t_or = time.perf_counter() - t0
+        got = outs[0].cpu().numpy().astype(np.float64)[rows]
+        scale = 1.1 * sg * np.abs(u) + np.abs(oracle.silu(g)) * su
+        rel = float(np.max(np.abs(got - h) / np.maximum(scale, 1e-30)))
+        rec = {"config": name, "m": p.m, "f": f, "k": p.k, "entry": "tq2_gate_up_swiglu",
+               "us_per_call": round(t * 1e6, 2), "weight_GBps": round(wbytes / t / 1e9, 1),
+               "TFLOPs": round(2.0 * p.m * p.n * p.k / t / 1e12, 2),
+               "max_err_over_bound_scale": rel, "parity_rows": int(rows.size),
+               "oracle_s_full_extrapolated": round(t_or * p.m / rows.size, 3),
+               "l2": f"{c} rotating weight copies" if c > 1 else "inputs larger than L2"}
+        del ws, outs, x, w0
+        torch.cuda.empty_cache()
+        return rec
+
     rows_out.append(one("1 small", tq2_synth.small(), "gemm", 50, 8)[0])
     rows_out.append(one("2a decode gate/up", tq2_synth.decode_gate_up(), "gemv", 200, 1)[0])
     rows_out.append(one("2b decode down + residual", tq2_synth.decode_down(), "gemv", 200, 1)[0])
+    # the same gate/up weight with the activation fused (out: 6144 values)
+    rows_out.append(one_swiglu("2a fused gate/up + SwiGLU", tq2_synth.decode_gate_up(), 6144, 200, 1))
     for m in tq2_synth.SKINNY_MS:
         rows_out.append(one(f"3 skinny m={m}", tq2_synth.skinny(m), "gemv" if m == 1 else "gemm",
                             100, 16)[0])
     for n in tq2_synth.DIT_NS:
         rows_out.append(one(f"4 dit n={n}", tq2_synth.dit(n), "gemm", 10, 16)[0])
+    # a DiT-sized fused gate/up: M=1536, 2f = 12288 rows, K=3072 (config 4's x and weights)
+    rows_out.append(one_swiglu("4 fused gate/up + SwiGLU m=1536 f=6144", tq2_synth.dit(12288), 6144, 10, 16))
     # config 5: the 100 layers one after another (each timed on its own, summed)
     tot_t, tot_f, worst, cmin, t_or5 = 0.0, 0.0, 0.0, 1.0, 0.0
     for li in range(len(tq2_synth.DIT_FORWARD_SHAPES)):

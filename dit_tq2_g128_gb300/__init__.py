@@ -44,7 +44,7 @@ EXPORTS = (
     "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
-    "tq2_gemm_noalloc", "tq2_quantize_f32",
+    "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu",
 )
 
 
@@ -89,6 +89,8 @@ def _load():
     L.tq2_gemm_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
     L.tq2_quantize_f32.restype = i32
     L.tq2_quantize_f32.argtypes = [vp, vp, i64, i64, vp]
+    L.tq2_gate_up_swiglu.restype = i32
+    L.tq2_gate_up_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gemm_noalloc.restype = i32
     L.tq2_gemm_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     return L
@@ -159,6 +161,11 @@ def tq2_reformat_aos_to_soa(w_aos, w_soa, n: int, k: int, stream=None) -> None:
 
 def tq2_quantize_f32(w, w_aos, n: int, k: int, stream=None) -> None:
     _check(lib.tq2_quantize_f32(_ptr(w), _ptr(w_aos), n, k, _stream(stream)), "tq2_quantize_f32")
+
+
+def tq2_gate_up_swiglu(w_soa, x, out, m: int, f: int, k: int, stream=None) -> None:
+    _check(lib.tq2_gate_up_swiglu(_ptr(w_soa), _ptr(x), _ptr(out), m, f, k, _stream(stream)),
+           "tq2_gate_up_swiglu")
 
 
 def tq2_gemv(w_soa, x, residual, out, n: int, k: int, stream=None) -> None:

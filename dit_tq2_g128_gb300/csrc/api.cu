@@ -263,6 +263,49 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
     return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
 }
 
+int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                       int64_t k, void *stream) {
+    if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
+    if (f < 0 || f > (int64_t(1) << 39)) return TQ2_ERR_INVALID_ARG;
+    bool noop = false;
+    int st = check_shape(m, 2 * f, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    if (!w_soa || !x || !out) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(w_soa) || !aligned16(x) || !aligned16(out)) return TQ2_ERR_MISALIGNED;
+    const size_t wb = size_t(2 * f) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
+    const size_t xb = size_t(m) * size_t(k) * 4, ob = size_t(m) * size_t(f) * 4;
+    if (overlaps(out, ob, x, xb) || overlaps(out, ob, w_soa, wb)) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    cudaError_t e = cudaErrorNotSupported;
+    if (m == 1) {
+        e = tq2::launch_gemv_swiglu(w_soa, x, out, f, k, ctx);
+    } else if (f % 16 == 0) {
+        void *ws = nullptr;
+        if (cudaMallocAsync(&ws, tq2::tc_swiglu_ws_bytes(m, k), ctx.stream) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return TQ2_ERR_CUDA;
+        }
+        e = tq2::launch_tc_swiglu(w_soa, x, out, m, f, k, ws, ctx);
+        const cudaError_t fr = cudaFreeAsync(ws, ctx.stream);
+        if (e == cudaSuccess) e = fr;
+    }
+    if (e != cudaErrorNotSupported) return finish(e);
+    (void)cudaGetLastError();
+    // Shapes outside the fused kernels: the plain product into a stream-ordered
+    // temporary [m, 2f], then the element-wise activation.
+    void *gu = nullptr;
+    if (cudaMallocAsync(&gu, size_t(m) * size_t(2 * f) * 4, ctx.stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TQ2_ERR_CUDA;
+    }
+    st = tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, nullptr, static_cast<float *>(gu), m, 2 * f, k, stream);
+    if (st == TQ2_OK) st = finish(tq2::launch_swiglu_rows(static_cast<const float *>(gu), out, m, f, ctx));
+    const cudaError_t fr = cudaFreeAsync(gu, ctx.stream);
+    return st != TQ2_OK ? st : finish(fr);
+}
+
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out, int64_t n,
              int64_t k, void *stream) {
     return tq2_gemm_with(TQ2_KERNEL_GEMV, w_soa, x, residual, out, 1, n, k, stream);

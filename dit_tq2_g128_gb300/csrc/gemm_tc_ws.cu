@@ -70,7 +70,14 @@ constexpr int NUM_EPI = 128;
 constexpr int EPI_NB = 1;                // staging buffers per epilogue warp
 constexpr int EPI_BYTES = 32 * 32 * 4;   // one 32 x 32 f32 block
 // Epilogue modes chosen by the host.
-constexpr int EPI_DIRECT = 0, EPI_TMA_STORE = 1, EPI_TMA_ADD = 2;
+// EPI_SWIGLU: fused gate/up projection.  The N = 2F weight rows hold the gate
+// projection in rows [0, F) and the up projection in rows [F, 2F); weight tile
+// nw is assembled from features 64 nw .. 64 nw + 63 as four groups of 16 gate
+// rows each followed by the matching 16 up rows (tile row 32 q + r: gate of
+// feature 64 nw + 16 q + r for r < 16, its up row for r >= 16).  Each epilogue
+// warp then holds g and u of 16 features in its lanes r and r + 16 and writes
+// out[m, f] = silu(g) * u (out has F columns).
+constexpr int EPI_DIRECT = 0, EPI_TMA_STORE = 1, EPI_TMA_ADD = 2, EPI_SWIGLU = 3;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;          // two f32 accumulators of BX columns
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16, both
@@ -146,6 +153,15 @@ __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+
+__device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int c0, int c1, int c2,
+                                       int c3, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
 }
 
 __device__ __forceinline__ void tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y,
@@ -371,7 +387,10 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     if (*abort_flag) { ok = false; break; }
                     if (codes) {
                         mbar_expect_tx(&ctl->codes_full[s], C_BYTES);
-                        tma_2d(stage_c(s), &qmap, kt * (BK / 4), nw * BW, &ctl->codes_full[s]);
+                        if (epi_mode == EPI_SWIGLU)  // 4 feature groups x {gate, up} x 16 rows
+                            tma_4d(stage_c(s), &qmap, kt * (BK / 4), 0, 0, nw * 4, &ctl->codes_full[s]);
+                        else
+                            tma_2d(stage_c(s), &qmap, kt * (BK / 4), nw * BW, &ctl->codes_full[s]);
                     } else {
                         // lane 0 arrives with the byte count of both halves; the
                         // CTA of rank h copies half h into both CTAs.  A half
@@ -455,8 +474,13 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         for (int t = cl; t < nitems; t += ncl) {
             const Item it = item(t);
             const int nw = it.nw;
-            const int row = nw * BW + pr;
-            const bool rvalid = row < N;
+            int row = nw * BW + pr;
+            bool rvalid = row < N;
+            if (epi_mode == EPI_SWIGLU) {  // tile row pr: feature 64 nw + 16 (pr / 32) + pr % 16
+                const int feat = nw * (BW / 2) + (pr >> 5) * 16 + (pr & 15);
+                rvalid = feat < N / 2;
+                row = feat + ((pr >> 4) & 1) * (N / 2);
+            }
             const __half *drow = dpl + int64_t(rvalid ? row : 0) * kb;
             const int j0 = int(((dset - gbase) % DEC_SETS + DEC_SETS) % DEC_SETS);
             // the scale of this thread's next stage, loaded one stage ahead
@@ -524,7 +548,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             // a K slice of a split problem writes its partial sums, plainly
             float *const dst = ksplit > 1 ? partial + int64_t(it.ks) * M * N : out;
             const float *const res = ksplit > 1 ? nullptr : residual;
-            const int mode = ksplit > 1 ? EPI_DIRECT : epi_mode;
+            const int mode = ksplit > 1 ? EPI_DIRECT : epi_mode;  // (never split with swiglu)
             const int a = i & 1;
             if (!mbar_wait_bounded(&ctl->tmem_full[a], (i >> 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
@@ -542,6 +566,30 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     mbar_arrive(&ctl->tmem_empty[a]);
                 }
                 const int row0 = mx * BX + c * 32;
+                if (mode == EPI_SWIGLU) {
+                    // lanes r and r + 16 hold g and u of feature 64 nw + 16 quarter + r
+                    const int F = N / 2;
+                    const int feat = nw * (BW / 2) + quarter * 16 + (lane & 15);
+                    const int nr = row0 < M ? min(32, M - row0) : 0;
+                    float *op = out + int64_t(row0) * F + feat;
+                    // the pair splits the block's 32 rows: lane r takes rows 0..15,
+                    // lane r + 16 rows 16..31 (each swaps the other half with its
+                    // partner), so that each lane evaluates 16 activations.
+                    // Fast exp and division here (relative error ~1e-6, far inside
+                    // the f16 path's bound): the activation shares the issue slots
+                    // of the SM with the weight decoders.
+                    const bool lo = lane < 16;
+#pragma unroll
+                    for (int jj = 0; jj < 16; ++jj) {
+                        const float a0 = __shfl_xor_sync(0xffffffffu, __uint_as_float(r[jj]), 16);
+                        const float a1 = __shfl_xor_sync(0xffffffffu, __uint_as_float(r[jj + 16]), 16);
+                        const float g = lo ? __uint_as_float(r[jj]) : a1;
+                        const float u = lo ? a0 : __uint_as_float(r[jj + 16]);
+                        const int j = lo ? jj : jj + 16;
+                        if (feat < F && j < nr) op[int64_t(j) * F] = __fdividef(g, 1.0f + __expf(-g)) * u;
+                    }
+                    continue;
+                }
                 if (row0 >= M || col0 >= N) continue;  // block wholly outside the output
                 if (mode == EPI_DIRECT) {
                     if (col >= N) continue;
@@ -716,28 +764,56 @@ size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k) {
     return ((xb + 255) & ~size_t(255)) + size_t(s) * size_t(m) * size_t(n) * 4;
 }
 
+size_t tc_swiglu_ws_bytes(int64_t m, int64_t k) { return x_tile_bytes(m, k); }
+
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx) {
+    return launch_tc_ws_mode(w_soa, x, residual, out, m, n, k, ws, false, ctx);
+}
+
+cudaError_t launch_tc_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                             int64_t k, void *ws, const LaunchCtx &ctx) {
+    if (f % 16) return cudaErrorNotSupported;  // whole 16-row groups in the 4-D view
+    return launch_tc_ws_mode(w_soa, x, nullptr, out, m, 2 * f, k, ws, true, ctx);
+}
+
+cudaError_t launch_tc_ws_mode(const void *w_soa, const float *x, const float *residual, float *out,
+                              int64_t m, int64_t n, int64_t k, void *ws, bool swiglu,
+                              const LaunchCtx &ctx) {
     if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return cudaErrorInvalidValue;
     const SoaView v = soa_view(w_soa, n, k);
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap qmap;
-    const cuuint64_t gdim[2] = {cuuint64_t(k / 4), cuuint64_t(n)};
-    const cuuint64_t gstride[1] = {cuuint64_t(k / 4)};
-    const cuuint32_t box[2] = {BK / 4, BW};
-    const cuuint32_t estride[2] = {1, 1};
-    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(v.qs), gdim, gstride, box,
-            estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    const cuuint32_t estride[4] = {1, 1, 1, 1};
+    if (swiglu) {
+        // codes viewed as [F/16 groups][2: gate, up][16 rows][K/4 bytes]
+        // (innermost first below); one box = 4 groups x 2 halves x 16 rows x 16 bytes
+        const int64_t f = n / 2;
+        const cuuint64_t gdim[4] = {cuuint64_t(k / 4), 16, 2, cuuint64_t(f / 16)};
+        const cuuint64_t gstride[3] = {cuuint64_t(k / 4), cuuint64_t(f) * cuuint64_t(k / 4),
+                                       16 * cuuint64_t(k / 4)};
+        const cuuint32_t box[4] = {BK / 4, 16, 2, 4};
+        if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<uint8_t *>(v.qs), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
+        const cuuint64_t gdim[2] = {cuuint64_t(k / 4), cuuint64_t(n)};
+        const cuuint64_t gstride[1] = {cuuint64_t(k / 4)};
+        const cuuint32_t box[2] = {BK / 4, BW};
+        if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(v.qs), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     // Output tensor map for the TMA epilogue: needs a 16-byte row pitch (n % 4
     // == 0; the base is 16-byte aligned by the API's checks) and either no
     // residual or an in-place residual (reduce-add into out).
-    int epi_mode = EPI_DIRECT;
+    int epi_mode = swiglu ? EPI_SWIGLU : EPI_DIRECT;
     CUtensorMap omap;
     std::memset(&omap, 0, sizeof(omap));
-    if (n % 4 == 0 && (residual == nullptr || residual == out)) {
+    if (!swiglu && n % 4 == 0 && (residual == nullptr || residual == out)) {
         const cuuint64_t odim[2] = {cuuint64_t(n), cuuint64_t(m)};
         const cuuint64_t ostride[1] = {cuuint64_t(n) * 4};
         const cuuint32_t obox[2] = {32, 32};
@@ -759,7 +835,7 @@ cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residua
     if (e != cudaSuccess) return e;
     // clusters of two CTAs, each cluster a pair of neighbouring weight tiles
     // (times the K slices of a split problem)
-    const int ksplit = tc_ksplit(m, n, k);
+    const int ksplit = swiglu ? 1 : tc_ksplit(m, n, k);
     float *partial = ksplit > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
                                                             ((x_tile_bytes(m, k) + 255) & ~size_t(255)))
                                 : nullptr;

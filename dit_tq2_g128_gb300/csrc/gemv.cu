@@ -306,7 +306,9 @@ __device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
 
 struct GvsParams {
     int n, k, C;       // rows, K, 1024-weight chunks per row
-    int rbase, rextra; // CTA b owns rbase (+1 if b < rextra) rows starting at b*rbase + min(b, rextra)
+    int rbase, rextra; // CTA b owns rbase (+1 if b < rextra) rows (features, with swiglu)
+                       // starting at b*rbase + min(b, rextra)
+    int swiglu, f;     // fused gate/up: rows [0, f) gate, [f, 2f) up; out[i] = silu(g_i) * u_i
     int xbox_rows, nxbox;  // x arrives as nxbox tensor boxes of xbox_rows 128-byte rows
     // shared-memory offsets (bytes, from the 1024-aligned base), computed on the host
     uint32_t off_ring, off_partial, off_bar;
@@ -334,8 +336,12 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     const int consumers = P.consumers;           // warps 0 .. consumers-1
     const int pwarp = int(blockDim.x >> 5) - 1;  // the producer: the last warp
     const int b = int(blockIdx.x);
-    const int R0 = b * P.rbase + min(b, P.rextra);
-    const int rows = P.rbase + (b < P.rextra ? 1 : 0);
+    const int R0 = b * P.rbase + min(b, P.rextra);  // first row (first feature, with swiglu)
+    const int nf = P.rbase + (b < P.rextra ? 1 : 0);
+    // The CTA's row list: rows R0 .. R0+nf-1, or with swiglu the gate rows
+    // R0 .. R0+nf-1 followed by the matching up rows f+R0 .. f+R0+nf-1.
+    const int rows = P.swiglu ? 2 * nf : nf;
+    auto real_row = [&](int i) { return (P.swiglu && i >= nf) ? P.f + R0 + (i - nf) : R0 + i; };
     const int nstages = (rows + RS - 1) / RS;
     constexpr bool dbulk = DBULK;
     const uint32_t code_bytes = uint32_t(RS * kq);
@@ -365,27 +371,41 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     }
     __syncthreads();
     const bool producer = warp == pwarp && lane == 0;
-    const uint8_t *src = qs + int64_t(R0) * kq;
-    const __half *dsrc_rows = dpl + int64_t(R0) * kb;
+    // A stage's rows are consecutive in the list; they are consecutive weight
+    // rows except where a swiglu stage crosses from the gate to the up rows:
+    // there the stage is copied (or prefetched) as two pieces.
+    auto pieces = [&](int st, auto &&fn) {
+        const int lo = st * RS, hi = min(lo + RS, rows);
+        if (P.swiglu && lo < nf && hi > nf) {
+            fn(lo, nf - lo, 0);
+            fn(nf, hi - nf, nf - lo);
+        } else {
+            fn(lo, hi - lo, 0);
+        }
+    };
     auto issue = [&](int st) {
         const int slot = st % P.ns;
         const int r = min(RS, rows - st * RS);
-        const uint32_t bytes = uint32_t(r * kq);
-        const uint32_t dbytes = dbulk ? uint32_t(r * kb * 2) : 0u;
         const uint32_t dst = ring_addr + uint32_t(slot) * stage_bytes;
-        mbar_expect_tx_gv(&full[slot], bytes + dbytes);
-        bulk_g2s_gv(dst, src + int64_t(st) * code_bytes, bytes, &full[slot]);
-        if (dbytes)
-            bulk_g2s_gv(dst + code_bytes, dsrc_rows + int64_t(st) * RS * kb, dbytes, &full[slot]);
+        mbar_expect_tx_gv(&full[slot], uint32_t(r) * (uint32_t(kq) + (dbulk ? uint32_t(kb * 2) : 0u)));
+        pieces(st, [&](int i0, int cnt, int off) {
+            const int64_t row = real_row(i0);
+            bulk_g2s_gv(dst + uint32_t(off) * uint32_t(kq), qs + row * kq, uint32_t(cnt * kq), &full[slot]);
+            if (dbulk)
+                bulk_g2s_gv(dst + code_bytes + uint32_t(off) * uint32_t(kb * 2), dpl + row * kb,
+                            uint32_t(cnt * kb * 2), &full[slot]);
+        });
     };
     // The weights go to L2 before waiting for the preceding kernel.  A
     // prefetch cannot leave stale data behind (L2 is the point of coherence,
     // and the copies below read through it after the wait).
     if (warp == pwarp) {
         for (int st = lane; st < nstages; st += 32) {
-            const int r = min(RS, rows - st * RS);
-            bulk_prefetch_l2(src + int64_t(st) * code_bytes, uint32_t(r * kq));
-            if (dbulk) bulk_prefetch_l2(dsrc_rows + int64_t(st) * RS * kb, uint32_t(r * kb * 2));
+            pieces(st, [&](int i0, int cnt, int) {
+                const int64_t row = real_row(i0);
+                bulk_prefetch_l2(qs + row * kq, uint32_t(cnt * kq));
+                if (dbulk) bulk_prefetch_l2(dpl + row * kb, uint32_t(cnt * kb * 2));
+            });
         }
     }
     // Everything a preceding kernel may have written (x, the weights, out and
@@ -515,7 +535,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             for (int uu = 0; uu < RS; ++uu) {
                 cw[uu] = *reinterpret_cast<const uint2 *>(sb + code_off + uint32_t(uu) * kq32);
                 d[uu] = dbulk ? __half2float(*reinterpret_cast<const __half *>(sb + d_off + uint32_t(uu) * kb2))
-                              : (uu < nv ? __half2float(__ushort_as_half(ldg_u16(dsrc_rows + int64_t(r0 + uu) * kb + dcol)))
+                              : (uu < nv ? __half2float(__ushort_as_half(ldg_u16(dpl + int64_t(real_row(r0 + uu)) * kb + dcol)))
                                          : 0.f);
             }
             // every lane has read its codes: release this chunk's share of the slot
@@ -555,6 +575,15 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     }
     __syncthreads();
     if (*abort_flag) return;
+    if (P.swiglu) {
+        for (int i = threadIdx.x; i < nf; i += blockDim.x) {
+            float g = 0.f, u = 0.f;
+            for (int cc = 0; cc < C; ++cc) g += partial[i * C + cc];
+            for (int cc = 0; cc < C; ++cc) u += partial[(nf + i) * C + cc];
+            out[R0 + i] = g / (1.0f + expf(-g)) * u;  // silu(g) * u
+        }
+        return;
+    }
     for (int i = threadIdx.x; i < rows; i += blockDim.x) {
         float sum = 0.f;
         for (int cc = 0; cc < C; ++cc) sum += partial[i * C + cc];
@@ -565,8 +594,9 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
 
 }  // namespace
 
+// swiglu: n = 2f weight rows (gate then up), out has f elements, no residual.
 cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *residual,
-                               float *out, int64_t n, int64_t k, const LaunchCtx &ctx) {
+                               float *out, int64_t n, int64_t k, bool swiglu, const LaunchCtx &ctx) {
     const int C = int((k + kGvChunk - 1) / kGvChunk);
     const int64_t kq = k / 4, kb = k / kBlockW;
     if (C > kGvMaxConsumers) return cudaErrorNotSupported;
@@ -574,11 +604,15 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.n = int(n);
     P.k = int(k);
     P.C = C;
+    P.swiglu = swiglu ? 1 : 0;
+    P.f = int(n / 2);
     P.groups = std::max(1, kGvMaxConsumers / C);  // consumer warp groups of C warps (one per chunk)
+    // the CTAs split the rows (with swiglu: the features, two rows each)
+    const int64_t units = swiglu ? n / 2 : n;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + 7) / 8));
-    P.rbase = int(n / grid);
-    P.rextra = int(n % grid);
-    P.rows_cta = P.rbase + (P.rextra ? 1 : 0);
+    P.rbase = int(units / grid);
+    P.rextra = int(units % grid);
+    P.rows_cta = (P.rbase + (P.rextra ? 1 : 0)) * (swiglu ? 2 : 1);
     // Rows per stage: a group's time is (its stages) x (RS rows + a per-stage
     // cost of about two rows); pick the RS in [2, 8] that minimises it for the
     // CTA's row count (ties: more rows per stage).
@@ -669,15 +703,41 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
                               ctx.wait_ns);
 }
 
+cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,
+                               const LaunchCtx &ctx) {
+    if (k > int64_t(kGvMaxConsumers) * kGvChunk || 2 * f > INT32_MAX) return cudaErrorNotSupported;
+    return launch_gemv_stream(w_soa, x, nullptr, out, 2 * f, k, true, ctx);
+}
+
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
                         int64_t n, int64_t k, const LaunchCtx &ctx) {
     if (k <= int64_t(kGvMaxConsumers) * kGvChunk && n <= INT32_MAX) {
-        cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, ctx);
+        cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, false, ctx);
         if (e != cudaErrorNotSupported) return e;
         (void)cudaGetLastError();
     }
     // very long rows: the chunk-looping small-M kernel (exact f32)
     return launch_tpl<1, 2>(w_soa, x, residual, out, 1, n, k, ctx);
+}
+
+namespace {
+__global__ void __launch_bounds__(256) swiglu_rows_kernel(const float *__restrict__ gu, float *__restrict__ out,
+                                                          int64_t m, int64_t f) {
+    const int64_t total = m * f, stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < total; i += stride) {
+        const int64_t r = i / f, j = i - r * f;
+        const float g = gu[r * 2 * f + j], u = gu[r * 2 * f + f + j];
+        out[i] = g / (1.0f + expf(-g)) * u;
+    }
+}
+}  // namespace
+
+cudaError_t launch_swiglu_rows(const float *gu, float *out, int64_t m, int64_t f, const LaunchCtx &ctx) {
+    const int64_t total = m * f;
+    if (total == 0) return cudaSuccess;
+    const int64_t grid = std::min<int64_t>((total + 255) / 256, int64_t(ctx.num_sms) * 8);
+    swiglu_rows_kernel<<<unsigned(grid), 256, 0, ctx.stream>>>(gu, out, m, f);
+    return cudaPeekAtLastError();
 }
 
 cudaError_t launch_skinny(const void *w_soa, const float *x, const float *residual, float *out,

@@ -44,6 +44,15 @@ cudaError_t launch_reformat(const void *w_aos, void *w_soa, int64_t n, int64_t k
                             const LaunchCtx &ctx);
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
                         int64_t n, int64_t k, const LaunchCtx &ctx);
+// Fused gate/up + SwiGLU (weight rows [0, f) gate, [f, 2f) up; out [m, f]).
+// cudaErrorNotSupported: shape outside the fused kernels (the caller falls back).
+cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,
+                               const LaunchCtx &ctx);
+cudaError_t launch_tc_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                             int64_t k, void *ws, const LaunchCtx &ctx);
+size_t tc_swiglu_ws_bytes(int64_t m, int64_t k);
+// out[i, j] = silu(gu[i, j]) * gu[i, f + j] for a row-major gu [m, 2f].
+cudaError_t launch_swiglu_rows(const float *gu, float *out, int64_t m, int64_t f, const LaunchCtx &ctx);
 cudaError_t launch_skinny(const void *w_soa, const float *x, const float *residual, float *out,
                           int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
 cudaError_t launch_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
@@ -55,6 +64,9 @@ size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k);  // x tiles (+ split-K part
 int tc_ksplit(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx);
+cudaError_t launch_tc_ws_mode(const void *w_soa, const float *x, const float *residual, float *out,
+                              int64_t m, int64_t n, int64_t k, void *ws, bool swiglu,
+                              const LaunchCtx &ctx);
 // Same kernel pair with the library's fixed device scratch (no allocation).
 constexpr size_t kNoAllocScratchBytes = size_t(TQ2_NOALLOC_SCRATCH_BYTES);
 cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,

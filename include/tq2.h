@@ -157,6 +157,36 @@ int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *ou
 int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t m, int64_t n, int64_t k, void *stream);
 
+/* Fused gate/up projection with the SwiGLU activation: the TQ2 analogue of
+ * the pages' `fused_gate_up_swiglu_q1` (decode) and
+ * `fused_gate_up_swiglu_gemm_q1` (prefill) pipelines ("oxibonsai-kernels
+ * 0.1.5 src/gpu_backend/metal_graph/pipelines.rs", fused-kernel fields), which
+ * the pages name without a listing.  The weight holds 2f rows: the gate
+ * projection in rows [0, f), the up projection in rows [f, 2f).  For each
+ * input row i and feature j:
+ *   g = sum_k x[i,k] W[j,k],  u = sum_k x[i,k] W[f+j,k],
+ *   out[i,j] = silu(g) * u,  silu(z) = z / (1 + exp(-z)).
+ *   w_soa : device SoA weight of n = 2f rows (from tq2_reformat_aos_to_soa)
+ *   x     : device f32 [m, k] row-major
+ *   out   : device f32 [m, f] row-major (may not overlap x or w_soa)
+ * Arithmetic: m = 1 runs the GEMV (x quantised per 32-weight slice, exact
+ * integer dot products; see tq2_gemv) for k <= 12288; m >= 2 runs the
+ * tensor-core kernel (x rounded to binary16; see tq2_gemm) with the activation
+ * in its epilogue when f % 16 == 0.  Other shapes compute the plain product
+ * into a temporary [m, 2f] and apply the activation in a second kernel.  g and
+ * u are never written to memory on the fused paths.  The activation is
+ * evaluated in f32: with expf and IEEE division on the GEMV and unfused paths,
+ * with the fast exp2-based exponential and division (relative error about
+ * 1e-6) in the tensor-core epilogue.
+ * Memory: m >= 2 (and the unfused shapes) take a temporary from the device's
+ * default memory pool, ordered on `stream` (as tq2_gemm).
+ * Errors: TQ2_ERR_BAD_K, TQ2_ERR_INVALID_ARG (negative m or f, NULL pointers,
+ * out overlapping x or w_soa), TQ2_ERR_MISALIGNED (pointers not 16-byte
+ * aligned), TQ2_ERR_CUDA (launch or temporary allocation failure).  m = 0 or
+ * f = 0 is a no-op. */
+int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                       int64_t k, void *stream);
+
 /* Same operation as tq2_gemm, computed by the exact-f32 CUDA-core tiled
  * kernel (the role of the pages' non-matrix-unit `gemm_tq2_g128_v8_tiled`,
  * kept for tolerance checks). */

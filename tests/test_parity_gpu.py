@@ -450,3 +450,80 @@ def test_quantize_empty_and_errors(tq2):
         tq2.tq2_quantize_f32(w, out, 2, 100)
     with pytest.raises(tq2.TQ2Error):
         tq2.tq2_quantize_f32(w, out.data_ptr() + 1, 2, 256)
+
+
+# ---------------------------------------------------------------------------
+# fused gate/up + SwiGLU
+
+def run_swiglu(tq2, w, p, f):
+    x = torch.from_numpy(p.x).cuda()
+    out = torch.full((p.m, f), float("nan"), dtype=torch.float32, device="cuda")
+    tq2.tq2_gate_up_swiglu(w, x, out, p.m, f, p.k)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def check_swiglu(got, p, f, rel, *, rows=None, cos=False, what=""):
+    """|h - ref| <= 1.1 tg (|u| + tu) + |silu(g)| tu + 2^-22 |h|: the products'
+    bound rel * Sigma|xw| (tg, tu) carried through silu (|silu'| <= 1.1) and
+    the product, plus f32 rounding of the activation."""
+    h, g, u, sg, su = oracle.swiglu(p.w_aos, p.x, f=f, k=p.k, rows=rows)
+    got = np.asarray(got, dtype=np.float64).reshape(-1, f)
+    got = got if rows is None else got[rows]
+    tg, tu = rel * sg, rel * su
+    bound = 1.1 * tg * (np.abs(u) + tu) + np.abs(oracle.silu(g)) * tu + 2.0 ** -22 * np.abs(h) + 1e-30
+    err = np.abs(got - h)
+    worst = float(np.max(err / bound)) if err.size else 0.0
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    assert np.all(err <= bound), f"{what}: max err/bound {worst:.3g}"
+    if cos:
+        num = np.sum(got * h, axis=1)
+        den = np.linalg.norm(got, axis=1) * np.linalg.norm(h, axis=1)
+        c = np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)
+        assert np.all(c >= COS_MIN), f"{what}: min row cosine {c.min()}"
+    return worst
+
+
+@pytest.mark.parametrize("f,k", [(6144, 4096), (1, 128), (7, 1152), (100, 3072), (2048, 12288),
+                                 (33, 16384)])
+def test_swiglu_decode(tq2, f, k):
+    # m = 1: fused into the GEMV for k <= 12288 (the 6144 x 4096 case is the
+    # decode fused gate/up shape, 2f = 12288 rows); k = 16384 takes the
+    # unfused path (exact-f32 product, then the activation)
+    p = tq2_synth.make_problem(1, 2 * f, k, seed=f + k, code_probs=(0.3, 0.4, 0.3))
+    w = upload(tq2, p)
+    check_swiglu(run_swiglu(tq2, w, p, f), p, f, TOL_F32, what=f"swiglu m=1 f={f} k={k}")
+
+
+@pytest.mark.parametrize("m,f,k", [(8, 512, 1024), (2, 64, 256), (129, 48, 640), (300, 1024, 3072),
+                                   (64, 6144, 4096), (5, 40, 384), (20, 1000, 1152), (3, 7, 128)])
+def test_swiglu_batched(tq2, m, f, k):
+    # m >= 2: the tensor-core kernel with the activation in its epilogue when
+    # f % 16 == 0 (40, 1000 and 7 take the unfused path)
+    p = tq2_synth.make_problem(m, 2 * f, k, seed=m * 31 + f)
+    w = upload(tq2, p)
+    check_swiglu(run_swiglu(tq2, w, p, f), p, f, TOL_TC, cos=True, what=f"swiglu m={m} f={f} k={k}")
+
+
+def test_swiglu_dit_shape_sampled(tq2):
+    # prefill-sized: m = 1536, 2f = 12288 rows, k = 3072; sampled rows
+    m, f, k = 1536, 6144, 3072
+    p = tq2_synth.make_problem(m, 2 * f, k, seed=77, d_sigma=0.01, outlier_frac=0.01)
+    w = upload(tq2, p)
+    got = run_swiglu(tq2, w, p, f)
+    check_swiglu(got, p, f, TOL_TC, rows=sample_rows(m), cos=True, what="swiglu dit shape")
+
+
+def test_swiglu_empty_and_errors(tq2):
+    x = torch.zeros(4, 128, device="cuda")
+    out = torch.zeros(4, 8, device="cuda")
+    w = torch.zeros(int(tq2.tq2_soa_bytes(16, 128)), dtype=torch.uint8, device="cuda")
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), out.data_ptr(), 0, 8, 128, None) == tq2.TQ2_OK
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), out.data_ptr(), 4, 0, 128, None) == tq2.TQ2_OK
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), out.data_ptr(), 4, 8, 100, None) == tq2.TQ2_ERR_BAD_K
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), out.data_ptr(), -1, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr() + 4, out.data_ptr(), 4, 8, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert tq2.lib.tq2_gate_up_swiglu(None, x.data_ptr(), out.data_ptr(), 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    # out overlapping x
+    assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), x.data_ptr(), 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    torch.cuda.synchronize()
