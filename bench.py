@@ -513,6 +513,57 @@ def run_suite(args, local):
         torch.cuda.empty_cache()
         return rec
 
+    def host_act16(a):
+        """binary16 activation layout made on the host (numpy rounding, then
+        element i of each 16-group at 2i or 2(i-8)+1)."""
+        a16 = np.asarray(a, dtype=np.float32).astype(np.float16)
+        kk = a16.shape[1]
+        i = np.arange(kk) % 16
+        pos = (np.arange(kk) - i) + np.where(i < 8, 2 * i, 2 * (i - 8) + 1)
+        out = np.empty_like(a16)
+        out[:, pos] = a16
+        return out, a16.astype(np.float32)
+
+    def one_act16(name, p, steps, sample_rows):
+        """tq2_gemm_act16: binary16 activations in and out; error against the oracle
+        on the binary16 input values, relative to sum|xw| after removing the
+        result's own rounding (2^-11 |ref|)."""
+        wbytes = tq2.tq2_soa_bytes(p.n, p.k)
+        per = wbytes + p.m * p.k * 2 + p.m * p.n * 2
+        c = max(2, -(-2 * l2 // per) + 1) if per < l2 else 1
+        w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
+        ws = [w0] + [w0.clone() for _ in range(c - 1)]
+        x16, x32 = host_act16(p.x)
+        r16, r32 = host_act16(p.residual) if p.residual is not None else (None, None)
+        xd = torch.from_numpy(x16).to(device)
+        rd = None if r16 is None else torch.from_numpy(r16).to(device)
+        outs = [torch.empty((p.m, p.n), dtype=torch.float16, device=device) for _ in range(c)]
+        t = timed(lambda i: tq2.tq2_gemm_act16(ws[i % c], xd, rd, outs[i % c], p.m, p.n, p.k), steps)
+        tq2.tq2_gemm_act16(ws[0], xd, rd, outs[0], p.m, p.n, p.k)
+        torch.cuda.synchronize()
+        assert tq2.tq2_device_status() == tq2.TQ2_OK
+        rows = sample(p.m, sample_rows) if p.m > sample_rows else np.arange(p.m)
+        t0 = time.perf_counter()
+        ref, scale = oracle.matmul(p.w_aos, x32, r32, n=p.n, k=p.k, rows=rows)
+        t_or = time.perf_counter() - t0
+        got16 = outs[0].cpu().numpy()
+        i = np.arange(p.n) % 16
+        pos = (np.arange(p.n) - i) + np.where(i < 8, 2 * i, 2 * (i - 8) + 1)
+        got = got16[:, pos].astype(np.float64)[rows]
+        err = np.maximum(np.abs(got - ref) - 2.0 ** -11 * np.abs(ref), 0.0)
+        rel = float(np.max(err / np.maximum(scale, 1e-30)))
+        num = np.sum(got * ref, axis=1)
+        den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+        cos = float(np.min(np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)))
+        rec = {"config": name, "m": p.m, "n": p.n, "k": p.k, "entry": "tq2_gemm_act16",
+               "us_per_call": round(t * 1e6, 2), "TFLOPs": round(2.0 * p.m * p.n * p.k / t / 1e12, 2),
+               "max_err_over_sum_abs_xw": rel, "min_row_cos": cos, "parity_rows": int(rows.size),
+               "oracle_s_full_extrapolated": round(t_or * p.m / rows.size, 3),
+               "l2": f"{c} rotating weight copies" if c > 1 else "inputs larger than L2"}
+        del ws, outs, xd, rd, w0
+        torch.cuda.empty_cache()
+        return rec, t
+
     rows_out.append(one("1 small", tq2_synth.small(), "gemm", 50, 8)[0])
     rows_out.append(one("2a decode gate/up", tq2_synth.decode_gate_up(), "gemv", 200, 1)[0])
     rows_out.append(one("2b decode down + residual", tq2_synth.decode_down(), "gemv", 200, 1)[0])
@@ -540,6 +591,21 @@ def run_suite(args, local):
                      "max_err_over_sum_abs_xw": worst, "min_row_cos": cmin,
                      "parity_rows": "2 sampled rows per layer",
                      "oracle_s_full_extrapolated": round(t_or5, 1)})
+    # configs 4 and 5 with binary16 activations in and out (no pre-pass, half the output bytes)
+    for n in tq2_synth.DIT_NS:
+        rows_out.append(one_act16(f"4 dit n={n} act16", tq2_synth.dit(n), 10, 16)[0])
+    tot_t, tot_f, worst, cmin = 0.0, 0.0, 0.0, 1.0
+    for li in range(len(tq2_synth.DIT_FORWARD_SHAPES)):
+        p = tq2_synth.dit_forward_layer(li)
+        rec, t = one_act16(f"5 layer {li} act16", p, 3, 2)
+        tot_t += t
+        tot_f += 2.0 * p.m * p.n * p.k
+        worst = max(worst, rec["max_err_over_sum_abs_xw"])
+        cmin = min(cmin, rec["min_row_cos"])
+    rows_out.append({"config": "5 dit forward act16 (100 layers, M=4096, binary16 activations)",
+                     "entry": "tq2_gemm_act16", "us_total": round(tot_t * 1e6, 1),
+                     "TFLOPs": round(tot_f / tot_t / 1e12, 2), "max_err_over_sum_abs_xw": worst,
+                     "min_row_cos": cmin, "parity_rows": "2 sampled rows per layer"})
     # the encoder (f32 -> blocks) on the largest DiT weight: f32 bytes read per second
     n, k = 12288, 3072
     wf = torch.randn((n, k), device=device) * 0.02

@@ -44,7 +44,8 @@ EXPORTS = (
     "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
-    "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu",
+    "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu", "tq2_act16_from_f32",
+    "tq2_act16_to_f32", "tq2_gemm_act16",
 )
 
 
@@ -89,6 +90,12 @@ def _load():
     L.tq2_gemm_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp, ctypes.c_size_t, vp]
     L.tq2_quantize_f32.restype = i32
     L.tq2_quantize_f32.argtypes = [vp, vp, i64, i64, vp]
+    L.tq2_act16_from_f32.restype = i32
+    L.tq2_act16_from_f32.argtypes = [vp, vp, i64, i64, vp]
+    L.tq2_act16_to_f32.restype = i32
+    L.tq2_act16_to_f32.argtypes = [vp, vp, i64, i64, vp]
+    L.tq2_gemm_act16.restype = i32
+    L.tq2_gemm_act16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gate_up_swiglu.restype = i32
     L.tq2_gate_up_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gemm_noalloc.restype = i32
@@ -161,6 +168,19 @@ def tq2_reformat_aos_to_soa(w_aos, w_soa, n: int, k: int, stream=None) -> None:
 
 def tq2_quantize_f32(w, w_aos, n: int, k: int, stream=None) -> None:
     _check(lib.tq2_quantize_f32(_ptr(w), _ptr(w_aos), n, k, _stream(stream)), "tq2_quantize_f32")
+
+
+def tq2_act16_from_f32(x, x16, m: int, k: int, stream=None) -> None:
+    _check(lib.tq2_act16_from_f32(_ptr(x), _ptr(x16), m, k, _stream(stream)), "tq2_act16_from_f32")
+
+
+def tq2_act16_to_f32(x16, x, m: int, k: int, stream=None) -> None:
+    _check(lib.tq2_act16_to_f32(_ptr(x16), _ptr(x), m, k, _stream(stream)), "tq2_act16_to_f32")
+
+
+def tq2_gemm_act16(w_soa, x16, residual16, out16, m: int, n: int, k: int, stream=None) -> None:
+    _check(lib.tq2_gemm_act16(_ptr(w_soa), _ptr(x16), _ptr(residual16), _ptr(out16), m, n, k,
+                              _stream(stream)), "tq2_gemm_act16")
 
 
 def tq2_gate_up_swiglu(w_soa, x, out, m: int, f: int, k: int, stream=None) -> None:

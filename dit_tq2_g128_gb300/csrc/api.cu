@@ -306,6 +306,62 @@ int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m,
     return st != TQ2_OK ? st : finish(fr);
 }
 
+int tq2_act16_from_f32(const float *x, void *x16, int64_t m, int64_t k, void *stream) {
+    if (k <= 0 || k % 16 || m < 0 || (m && k > (int64_t(1) << 40) / m)) return TQ2_ERR_INVALID_ARG;
+    if (m == 0) return TQ2_OK;
+    if (!x || !x16) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x16)) return TQ2_ERR_MISALIGNED;
+    if (overlaps(x, size_t(m) * size_t(k) * 4, x16, size_t(m) * size_t(k) * 2)) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_act16_from_f32(x, static_cast<__half *>(x16), m, k, ctx));
+}
+
+int tq2_act16_to_f32(const void *x16, float *x, int64_t m, int64_t k, void *stream) {
+    if (k <= 0 || k % 16 || m < 0 || (m && k > (int64_t(1) << 40) / m)) return TQ2_ERR_INVALID_ARG;
+    if (m == 0) return TQ2_OK;
+    if (!x || !x16) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x16)) return TQ2_ERR_MISALIGNED;
+    if (overlaps(x, size_t(m) * size_t(k) * 4, x16, size_t(m) * size_t(k) * 2)) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_act16_to_f32(static_cast<const __half *>(x16), x, m, k, ctx));
+}
+
+int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, void *out16, int64_t m,
+                   int64_t n, int64_t k, void *stream) {
+    bool noop = false;
+    int st = check_shape(m, n, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    if (n % 16) return TQ2_ERR_INVALID_ARG;
+    if (!w_soa || !x16 || !out16) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(w_soa) || !aligned16(x16) || !aligned16(out16) || (residual16 && !aligned16(residual16)))
+        return TQ2_ERR_MISALIGNED;
+    const size_t wb = size_t(n) * size_t(k / tq2::kBlockW) * tq2::kBlockBytes;
+    const size_t xb = size_t(m) * size_t(k) * 2, ob = size_t(m) * size_t(n) * 2;
+    if (overlaps(out16, ob, x16, xb) || overlaps(out16, ob, w_soa, wb)) return TQ2_ERR_INVALID_ARG;
+    if (residual16 && residual16 != out16 && overlaps(out16, ob, residual16, ob)) return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    const size_t need = tq2::tc_act16_ws_bytes(m, n, k);
+    void *ws = nullptr;
+    if (need && cudaMallocAsync(&ws, need, ctx.stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TQ2_ERR_CUDA;
+    }
+    cudaError_t e = tq2::launch_tc_act16(w_soa, static_cast<const __half *>(x16),
+                                         static_cast<const __half *>(residual16), static_cast<__half *>(out16),
+                                         m, n, k, ws, ctx);
+    if (ws) {
+        const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
+        if (e == cudaSuccess) e = f;
+    }
+    return finish(e);
+}
+
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out, int64_t n,
              int64_t k, void *stream) {
     return tq2_gemm_with(TQ2_KERNEL_GEMV, w_soa, x, residual, out, 1, n, k, stream);

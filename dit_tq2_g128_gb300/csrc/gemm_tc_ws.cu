@@ -77,7 +77,15 @@ constexpr int EPI_BYTES = 32 * 32 * 4;   // one 32 x 32 f32 block
 // feature 64 nw + 16 q + r for r < 16, its up row for r >= 16).  Each epilogue
 // warp then holds g and u of 16 features in its lanes r and r + 16 and writes
 // out[m, f] = silu(g) * u (out has F columns).
-constexpr int EPI_DIRECT = 0, EPI_TMA_STORE = 1, EPI_TMA_ADD = 2, EPI_SWIGLU = 3;
+// EPI_ACT16: binary16 activations in and out (the library's activation
+// layout: row-major, element i of every 16-element group stored at position
+// 2i for i < 8 and 2(i-8)+1 for i >= 8, the k order of the decoded weights).
+// x tiles then arrive by tensor copy with no pre-pass, and the output, in the
+// same layout, is the next layer's input.
+constexpr int EPI_DIRECT = 0, EPI_TMA_STORE = 1, EPI_TMA_ADD = 2, EPI_SWIGLU = 3, EPI_ACT16 = 4;
+
+// Position of element i (0..15) of a 16-element group in the activation layout.
+__host__ __device__ __forceinline__ constexpr int act16_pos(int i) { return i < 8 ? 2 * i : 2 * (i - 8) + 1; }
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t ACC_COL = 0;          // two f32 accumulators of BX columns
 // Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A and B f16, both
@@ -161,6 +169,16 @@ __device__ __forceinline__ void tma_4d(uint32_t dst, const CUtensorMap *map, int
         "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Tensor copy delivered to the same offset in every CTA of `mask`.
+__device__ __forceinline__ void tma_2d_mc(uint32_t dst, const CUtensorMap *map, int x, int y,
+                                          uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar)), "h"(mask)
         : "memory");
 }
 
@@ -282,8 +300,9 @@ x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, 
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
-             const __half *__restrict__ dpl, const uint8_t *__restrict__ xtiles, const float *residual,
-             float *out, int M, int N, int K, int epi_mode, int ksplit, float *partial,
+             const __grid_constant__ CUtensorMap xmap, const __half *__restrict__ dpl,
+             const uint8_t *__restrict__ xtiles, const float *residual, float *out, const __half *res16,
+             __half *out16, int M, int N, int K, int epi_mode, int ksplit, float *partial,
              unsigned int *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -399,10 +418,15 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                         // without the arrival).
                         if (lane == 0) {
                             mbar_expect_tx(&ctl->full[s], uint32_t(nmt) * A_BYTES);
-                            if (rank < nmt)
-                                bulk_g2s_mc(stage_x(s) + uint32_t(rank) * A_BYTES,
-                                            xtiles + (int64_t(mt0 + rank) * KT + kt) * A_BYTES, A_BYTES,
-                                            &ctl->full[s], pair_mask);
+                            if (rank < nmt) {
+                                if (epi_mode == EPI_ACT16)  // 128 rows x 64 k of the activation tensor
+                                    tma_2d_mc(stage_x(s) + uint32_t(rank) * A_BYTES, &xmap, kt * BK,
+                                              (mt0 + rank) * BM, &ctl->full[s], pair_mask);
+                                else
+                                    bulk_g2s_mc(stage_x(s) + uint32_t(rank) * A_BYTES,
+                                                xtiles + (int64_t(mt0 + rank) * KT + kt) * A_BYTES, A_BYTES,
+                                                &ctl->full[s], pair_mask);
+                            }
                         }
                     }
                     last_round[s] = u;
@@ -550,6 +574,27 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             const float *const res = ksplit > 1 ? nullptr : residual;
             const int mode = ksplit > 1 ? EPI_DIRECT : epi_mode;  // (never split with swiglu)
             const int a = i & 1;
+            {
+                // The residual this warp adds (its 32 columns of the tile's 256
+                // rows) goes to L2 while the tile's MMAs run: the epilogue's
+                // loads then wait on L2, not on DRAM.
+                const int pcol = nw * BW + quarter * 32;
+                if (pcol < N && (mode == EPI_DIRECT || mode == EPI_ACT16)) {
+                    const bool h16 = mode == EPI_ACT16;
+                    const char *rb = h16 ? reinterpret_cast<const char *>(res16) : reinterpret_cast<const char *>(res);
+                    if (rb) {
+                        const int esz = h16 ? 2 : 4;
+                        const int ncol = min(32, N - pcol);
+                        for (int rr = lane; rr < BX; rr += 32) {
+                            const int row = mx * BX + rr;
+                            if (row >= M) break;
+                            const char *p0 = rb + (int64_t(row) * N + pcol) * esz;
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(p0));
+                            asm volatile("prefetch.global.L2 [%0];" ::"l"(p0 + ncol * esz - 1));
+                        }
+                    }
+                }
+            }
             if (!mbar_wait_bounded(&ctl->tmem_full[a], (i >> 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
             tc_fence_after();
@@ -591,6 +636,33 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     continue;
                 }
                 if (row0 >= M || col0 >= N) continue;  // block wholly outside the output
+                if (mode == EPI_ACT16) {
+                    // binary16 out (and residual) at the activation-layout position of col
+                    if (col >= N) continue;
+                    const int nr = min(32, M - row0);
+                    const int64_t pc = (col & ~15) | act16_pos(col & 15);
+                    __half *op = out16 + int64_t(row0) * N + pc;
+                    const __half *rp = res16 ? res16 + int64_t(row0) * N + pc : nullptr;
+                    if (rp) {
+                        // eight residual loads in flight before their first use
+#pragma unroll
+                        for (int h = 0; h < 32; h += 8) {
+                            float rv[8];
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                rv[j] = h + j < nr ? __half2float(rp[int64_t(h + j) * N]) : 0.f;
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                if (h + j < nr)
+                                    op[int64_t(h + j) * N] = __float2half_rn(__uint_as_float(r[h + j]) + rv[j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (j < nr) op[int64_t(j) * N] = __float2half_rn(__uint_as_float(r[j]));
+                    }
+                    continue;
+                }
                 if (mode == EPI_DIRECT) {
                     if (col >= N) continue;
                     const int nr = min(32, M - row0);  // rows of this block inside the output
@@ -660,6 +732,22 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
     // The peer may still arrive on this CTA's barriers until its own MMAs
     // have drained: leave together.
     cluster_sync();
+}
+
+// Activation-layout variant of the reduction: binary16 out (and residual) at
+// the layout position of each column.
+__global__ void __launch_bounds__(256)
+ksplit_reduce_act16_kernel(const float *__restrict__ part, int S, int64_t m, int64_t n,
+                           const __half *res16, __half *out16) {
+    const int64_t mn = m * n, stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t i = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; i < mn; i += stride) {
+        float acc = part[i];
+        for (int s = 1; s < S; ++s) acc += part[int64_t(s) * mn + i];
+        const int64_t r = i / n, c = i - r * n;
+        const int64_t o = r * n + ((c & ~int64_t(15)) | act16_pos(int(c & 15)));
+        if (res16) acc += __half2float(res16[o]);
+        out16[o] = __float2half_rn(acc);
+    }
 }
 
 // out = sum of the K-slice partials in slice order (+ residual): deterministic.
@@ -766,21 +854,36 @@ size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k) {
 
 size_t tc_swiglu_ws_bytes(int64_t m, int64_t k) { return x_tile_bytes(m, k); }
 
+// Activation-layout GEMM: the workspace holds only split-K partials (x needs no tiles).
+size_t tc_act16_ws_bytes(int64_t m, int64_t n, int64_t k) {
+    const int s = tc_ksplit(m, n, k);
+    return s == 1 ? 0 : size_t(s) * size_t(m) * size_t(n) * 4;
+}
+
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx) {
-    return launch_tc_ws_mode(w_soa, x, residual, out, m, n, k, ws, false, ctx);
+    TcIo io{x, residual, out, nullptr, nullptr, nullptr};
+    return launch_tc_ws_mode(w_soa, io, m, n, k, ws, TC_PLAIN, ctx);
 }
 
 cudaError_t launch_tc_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
                              int64_t k, void *ws, const LaunchCtx &ctx) {
     if (f % 16) return cudaErrorNotSupported;  // whole 16-row groups in the 4-D view
-    return launch_tc_ws_mode(w_soa, x, nullptr, out, m, 2 * f, k, ws, true, ctx);
+    TcIo io{x, nullptr, out, nullptr, nullptr, nullptr};
+    return launch_tc_ws_mode(w_soa, io, m, 2 * f, k, ws, TC_SWIGLU, ctx);
 }
 
-cudaError_t launch_tc_ws_mode(const void *w_soa, const float *x, const float *residual, float *out,
-                              int64_t m, int64_t n, int64_t k, void *ws, bool swiglu,
-                              const LaunchCtx &ctx) {
+cudaError_t launch_tc_act16(const void *w_soa, const __half *x16, const __half *res16, __half *out16,
+                            int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx) {
+    if (n % 16) return cudaErrorInvalidValue;  // whole 16-element groups in the output layout
+    TcIo io{nullptr, nullptr, nullptr, x16, res16, out16};
+    return launch_tc_ws_mode(w_soa, io, m, n, k, ws, TC_ACT16, ctx);
+}
+
+cudaError_t launch_tc_ws_mode(const void *w_soa, const TcIo &io, int64_t m, int64_t n, int64_t k,
+                              void *ws, int variant, const LaunchCtx &ctx) {
     if (m > INT32_MAX || n > INT32_MAX || k > INT32_MAX) return cudaErrorInvalidValue;
+    const bool swiglu = variant == TC_SWIGLU, act16 = variant == TC_ACT16;
     const SoaView v = soa_view(w_soa, n, k);
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
@@ -807,48 +910,70 @@ cudaError_t launch_tc_ws_mode(const void *w_soa, const float *x, const float *re
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
+    // binary16 activations: 128-row x 64-k boxes of x with the 128-byte swizzle,
+    // the layout of the MMA's B operand (rows past m arrive as zeros)
+    CUtensorMap xmap;
+    std::memset(&xmap, 0, sizeof(xmap));
+    if (act16) {
+        const cuuint64_t xdim[2] = {cuuint64_t(k), cuuint64_t(m)};
+        const cuuint64_t xstride[1] = {cuuint64_t(k) * 2};
+        const cuuint32_t xbox[2] = {BK, BM};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<__half *>(io.x16), xdim, xstride, xbox,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
     // Output tensor map for the TMA epilogue: needs a 16-byte row pitch (n % 4
     // == 0; the base is 16-byte aligned by the API's checks) and either no
     // residual or an in-place residual (reduce-add into out).
-    int epi_mode = swiglu ? EPI_SWIGLU : EPI_DIRECT;
+    int epi_mode = swiglu ? EPI_SWIGLU : act16 ? EPI_ACT16 : EPI_DIRECT;
     CUtensorMap omap;
     std::memset(&omap, 0, sizeof(omap));
-    if (!swiglu && n % 4 == 0 && (residual == nullptr || residual == out)) {
+    if (variant == TC_PLAIN && n % 4 == 0 && (io.residual == nullptr || io.residual == io.out)) {
         const cuuint64_t odim[2] = {cuuint64_t(n), cuuint64_t(m)};
         const cuuint64_t ostride[1] = {cuuint64_t(n) * 4};
         const cuuint32_t obox[2] = {32, 32};
-        if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, out, odim, ostride, obox, estride,
+        if (enc(&omap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, io.out, odim, ostride, obox, estride,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                 CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
-            epi_mode = residual ? EPI_TMA_ADD : EPI_TMA_STORE;
+            epi_mode = io.residual ? EPI_TMA_ADD : EPI_TMA_STORE;
     }
-    // pre-pass
-    const int MT = int((m + BM - 1) / BM);
-    const int64_t items = int64_t(MT) * BM * (k / 16);
-    const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
-    x_to_tiles_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(x, static_cast<uint8_t *>(ws), int(m),
-                                                               int(k), MT);
-    cudaError_t e = cudaPeekAtLastError();
-    if (e != cudaSuccess) return e;
+    cudaError_t e;
+    if (!act16) {
+        // pre-pass: f32 x -> binary16 MMA tiles in the workspace
+        const int MT = int((m + BM - 1) / BM);
+        const int64_t items = int64_t(MT) * BM * (k / 16);
+        const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
+        x_to_tiles_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(io.x, static_cast<uint8_t *>(ws), int(m),
+                                                                   int(k), MT);
+        e = cudaPeekAtLastError();
+        if (e != cudaSuccess) return e;
+    }
     e = cudaFuncSetAttribute(tc_ws_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(SMEM_BYTES));
     if (e != cudaSuccess) return e;
     // clusters of two CTAs, each cluster a pair of neighbouring weight tiles
     // (times the K slices of a split problem)
     const int ksplit = swiglu ? 1 : tc_ksplit(m, n, k);
-    float *partial = ksplit > 1 ? reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
-                                                            ((x_tile_bytes(m, k) + 255) & ~size_t(255)))
-                                : nullptr;
+    float *partial = nullptr;
+    if (ksplit > 1)
+        partial = act16 ? static_cast<float *>(ws)
+                        : reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
+                                                    ((x_tile_bytes(m, k) + 255) & ~size_t(255)));
     const int64_t nitems = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2) * ksplit;
     const int64_t grid = 2 * std::min<int64_t>(nitems, ctx.num_sms / 2);
     tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
-        qmap, omap, v.d, static_cast<const uint8_t *>(ws), residual, out, int(m), int(n), int(k),
-        epi_mode, ksplit, partial, ctx.status, ctx.wait_ns);
+        qmap, omap, xmap, v.d, static_cast<const uint8_t *>(ws), io.residual, io.out, io.res16, io.out16,
+        int(m), int(n), int(k), epi_mode, ksplit, partial, ctx.status, ctx.wait_ns);
     e = cudaPeekAtLastError();
     if (e != cudaSuccess || ksplit == 1) return e;
     const int64_t mn = m * n;
     const int64_t rgrid = std::min<int64_t>((mn / 4 + 255) / 256 + 1, int64_t(ctx.num_sms) * 8);
-    ksplit_reduce_kernel<<<unsigned(rgrid), 256, 0, ctx.stream>>>(partial, ksplit, mn, residual, out);
+    if (act16)
+        ksplit_reduce_act16_kernel<<<unsigned(rgrid), 256, 0, ctx.stream>>>(partial, ksplit, m, n, io.res16,
+                                                                            io.out16);
+    else
+        ksplit_reduce_kernel<<<unsigned(rgrid), 256, 0, ctx.stream>>>(partial, ksplit, mn, io.residual, io.out);
     return cudaPeekAtLastError();
 }
 

@@ -64,9 +64,26 @@ size_t tc_ws_bytes(int64_t m, int64_t n, int64_t k);  // x tiles (+ split-K part
 int tc_ksplit(int64_t m, int64_t n, int64_t k);
 cudaError_t launch_tc_ws(const void *w_soa, const float *x, const float *residual, float *out,
                          int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx);
-cudaError_t launch_tc_ws_mode(const void *w_soa, const float *x, const float *residual, float *out,
-                              int64_t m, int64_t n, int64_t k, void *ws, bool swiglu,
-                              const LaunchCtx &ctx);
+// Operands of the tensor-core kernel: f32 x/residual/out, or binary16
+// activations in the library's activation layout (x16/res16/out16).
+struct TcIo {
+    const float *x;
+    const float *residual;
+    float *out;
+    const __half *x16;
+    const __half *res16;
+    __half *out16;
+};
+constexpr int TC_PLAIN = 0, TC_SWIGLU = 1, TC_ACT16 = 2;
+cudaError_t launch_tc_ws_mode(const void *w_soa, const TcIo &io, int64_t m, int64_t n, int64_t k,
+                              void *ws, int variant, const LaunchCtx &ctx);
+// Binary16 activations in and out (out n % 16 == 0); ws: tc_act16_ws_bytes (may be 0).
+size_t tc_act16_ws_bytes(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_tc_act16(const void *w_soa, const __half *x16, const __half *res16, __half *out16,
+                            int64_t m, int64_t n, int64_t k, void *ws, const LaunchCtx &ctx);
+// f32 [m, k] <-> binary16 activation layout (k % 16 == 0)
+cudaError_t launch_act16_from_f32(const float *x, __half *x16, int64_t m, int64_t k, const LaunchCtx &ctx);
+cudaError_t launch_act16_to_f32(const __half *x16, float *x, int64_t m, int64_t k, const LaunchCtx &ctx);
 // Same kernel pair with the library's fixed device scratch (no allocation).
 constexpr size_t kNoAllocScratchBytes = size_t(TQ2_NOALLOC_SCRATCH_BYTES);
 cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,

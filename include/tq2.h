@@ -187,6 +187,35 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
 int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
                        int64_t k, void *stream);
 
+/* Binary16 activation layout (activation-resident chaining of layers): a
+ * row-major [m][k] array of binary16 in which element i (0..15) of every
+ * 16-element group of a row is stored at position 2i for i < 8 and 2(i-8)+1
+ * for i >= 8 (the k order in which the tensor-core kernel decodes weights).
+ * tq2_gemm_act16 reads x and writes out in this layout, so the output of one
+ * layer is the next layer's input with no f32 round trip and no conversion
+ * pass.  Converters (k % 16 == 0; pointers 16-byte aligned, not overlapping):
+ * from f32 rounds to nearest even (|x| >= 65520 becomes Inf), to f32 is exact.
+ * Errors: TQ2_ERR_INVALID_ARG (k not a positive multiple of 16, m < 0, NULL,
+ * overlap), TQ2_ERR_MISALIGNED, TQ2_ERR_CUDA. */
+int tq2_act16_from_f32(const float *x, void *x16, int64_t m, int64_t k, void *stream);
+int tq2_act16_to_f32(const void *x16, float *x, int64_t m, int64_t k, void *stream);
+
+/* out16[m, n] = x16[m, k] . dequant(W)^T (+ residual16), binary16 activations
+ * in the layout above (the pages' DiT linears, "oxibonsai-image 0.2.2
+ * src/gpu.rs" contract, with the activations kept in binary16 between layers:
+ * only activations cross between kernels).  The tensor-core kernel multiplies
+ * the exactly representable binary16 weights with x16 (no rounding of x),
+ * accumulates in f32, adds the residual in f32 and rounds the result once to
+ * binary16 (nearest even).  x tiles arrive by tensor copy: no pre-pass.
+ *   n must be a multiple of 16 (the output layout's groups); residual16 may be
+ *   NULL or equal to out16 (in place).
+ * Memory: shapes with too few output tiles for the GPU split K and take a
+ * temporary of S*m*n f32 from the device's default memory pool on `stream`.
+ * Errors: TQ2_ERR_BAD_K, TQ2_ERR_INVALID_ARG (n % 16 != 0, negative sizes,
+ * NULL, overlaps), TQ2_ERR_MISALIGNED, TQ2_ERR_CUDA.  m = 0 or n = 0: no-op. */
+int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, void *out16,
+                   int64_t m, int64_t n, int64_t k, void *stream);
+
 /* Same operation as tq2_gemm, computed by the exact-f32 CUDA-core tiled
  * kernel (the role of the pages' non-matrix-unit `gemm_tq2_g128_v8_tiled`,
  * kept for tolerance checks). */

@@ -527,3 +527,133 @@ def test_swiglu_empty_and_errors(tq2):
     # out overlapping x
     assert tq2.lib.tq2_gate_up_swiglu(w.data_ptr(), x.data_ptr(), x.data_ptr(), 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# binary16 activation layout and the activation-resident GEMM
+
+def act16_perm(k):
+    """Storage position of each element: element 16g + i at 16g + (2i if i < 8 else 2(i-8)+1)."""
+    i = np.arange(k) % 16
+    return (np.arange(k) - i) + np.where(i < 8, 2 * i, 2 * (i - 8) + 1)
+
+
+def to_act16(x):
+    """numpy reference of the layout: float16 (round to nearest even), elements permuted."""
+    with np.errstate(over="ignore"):
+        x16 = np.asarray(x, dtype=np.float32).astype(np.float16)
+    out = np.empty_like(x16)
+    out[:, act16_perm(x.shape[1])] = x16
+    return out
+
+
+def from_act16(y):
+    return y[:, act16_perm(y.shape[1])]
+
+
+@pytest.mark.parametrize("m,k", [(1, 16), (3, 48), (129, 1024), (7, 4096)])
+def test_act16_converters_bit_exact(tq2, m, k):
+    rng = np.random.default_rng(m + k)
+    x = (rng.standard_normal((m, k)) * rng.choice([1e-6, 1.0, 300.0], size=(m, k))).astype(np.float32)
+    x[0, 0] = 65519.0   # rounds to 65504
+    if k > 1:
+        x[0, 1] = 65520.0  # rounds to Inf
+    xd = torch.from_numpy(x).cuda()
+    y = torch.empty((m, k), dtype=torch.float16, device="cuda")
+    tq2.tq2_act16_from_f32(xd, y, m, k)
+    back = torch.empty((m, k), dtype=torch.float32, device="cuda")
+    tq2.tq2_act16_to_f32(y, back, m, k)
+    torch.cuda.synchronize()
+    ref = to_act16(x)
+    assert np.array_equal(y.cpu().numpy().view(np.uint16), ref.view(np.uint16))
+    assert np.array_equal(back.cpu().numpy(), from_act16(ref).astype(np.float32))
+
+
+def run_act16(tq2, w, x16_np, r16_np, m, n, k, *, inplace=False):
+    x16 = torch.from_numpy(x16_np).cuda()
+    if inplace:
+        out = torch.from_numpy(r16_np).cuda()
+        r = out
+    else:
+        out = torch.full((m, n), float("nan"), dtype=torch.float16, device="cuda")
+        r = None if r16_np is None else torch.from_numpy(r16_np).cuda()
+    tq2.tq2_gemm_act16(w, x16, r, out, m, n, k)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def check_act16(got16, p, x32, r32, *, rows=None, what=""):
+    """|out - ref| <= 4e-3 Sigma|xw| + 2^-11 |ref| (the f16 path's product bound and
+    the one rounding of the result to binary16; x16 values are inputs, exact)."""
+    ref, scale = oracle.matmul(p.w_aos, x32, r32, n=p.n, k=p.k, rows=rows)
+    got = from_act16(got16).astype(np.float64)
+    got = got if rows is None else got[rows]
+    bound = TOL_TC * scale + 2.0 ** -11 * np.abs(ref) + 2.0 ** -24
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), what
+    assert np.all(err <= bound), f"{what}: max err/bound {float(np.max(err / bound)):.3g}"
+    num = np.sum(got * ref, axis=1)
+    den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+    c = np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)
+    assert np.all(c >= COS_MIN), f"{what}: min row cosine {c.min()}"
+
+
+@pytest.mark.parametrize("m,n,k,res", [(8, 1024, 1024, False), (129, 256, 640, True), (300, 48, 128, False),
+                                       (64, 4096, 4096, True), (1, 16, 128, False), (1536, 3072, 3072, True)])
+def test_gemm_act16_parity(tq2, m, n, k, res):
+    # (64, 4096, 4096) splits K; (1536, 3072, 3072) is the DiT shape (sampled rows)
+    p = tq2_synth.make_problem(m, n, k, seed=m + n + k, residual=res)
+    x16 = to_act16(p.x)
+    r16 = to_act16(p.residual) if res else None
+    w = upload(tq2, p)
+    got = run_act16(tq2, w, x16, r16, m, n, k)
+    x32 = from_act16(x16).astype(np.float32)
+    r32 = from_act16(r16).astype(np.float32) if res else None
+    rows = sample_rows(m) if m > 256 else None
+    check_act16(got if rows is None else got, p, x32, r32, rows=rows, what=f"act16 {m}x{n}x{k}")
+    if res:  # in place: out16 = residual16 on entry
+        got2 = run_act16(tq2, w, x16, r16, m, n, k, inplace=True)
+        assert np.array_equal(got2.view(np.uint16), got.view(np.uint16))
+
+
+def test_gemm_act16_chain_two_layers(tq2):
+    # layer 1 (k0 -> k1) feeds layer 2 (k1 -> n2) in the activation layout on the
+    # GPU; the oracle runs the same chain with the intermediate rounded to binary16
+    # by numpy.  Layer 2's bound adds |W2| times layer 1's bound plus one binary16
+    # step of the intermediate (the two sides may round it one step apart).
+    m, k0, k1, n2 = 96, 1024, 2048, 512
+    p1 = tq2_synth.make_problem(m, k1, k0, seed=5)
+    p2 = tq2_synth.make_problem(m, n2, k1, seed=6)
+    w1, w2 = upload(tq2, p1), upload(tq2, p2)
+    x16 = torch.from_numpy(to_act16(p1.x)).cuda()
+    h16 = torch.empty((m, k1), dtype=torch.float16, device="cuda")
+    o16 = torch.empty((m, n2), dtype=torch.float16, device="cuda")
+    tq2.tq2_gemm_act16(w1, x16, None, h16, m, k1, k0)
+    tq2.tq2_gemm_act16(w2, h16, None, o16, m, n2, k1)
+    torch.cuda.synchronize()
+    x32 = from_act16(to_act16(p1.x)).astype(np.float32)
+    ref1, s1 = oracle.matmul(p1.w_aos, x32, n=k1, k=k0)
+    h = ref1.astype(np.float16)                       # the oracle's rounded intermediate
+    b1 = TOL_TC * s1 + 2.0 ** -11 * np.abs(ref1)      # layer 1's bound
+    step = np.abs(np.spacing(h.astype(np.float16))).astype(np.float64)
+    ref2, s2 = oracle.matmul(p2.w_aos, h.astype(np.float32), n=n2, k=k1)
+    W2 = np.abs(oracle.dequant(p2.w_aos, n2, k1))
+    bound = TOL_TC * s2 + 2.0 ** -11 * np.abs(ref2) + (b1 + step) @ W2.T + 2.0 ** -24
+    got = from_act16(o16.cpu().numpy()).astype(np.float64)
+    assert np.all(np.abs(got - ref2) <= bound)
+
+
+def test_act16_errors(tq2):
+    x = torch.zeros(4, 128, dtype=torch.float16, device="cuda")
+    o = torch.zeros(4, 40, dtype=torch.float16, device="cuda")
+    w = torch.zeros(int(tq2.tq2_soa_bytes(40, 128)), dtype=torch.uint8, device="cuda")
+    L = tq2.lib
+    assert L.tq2_gemm_act16(w.data_ptr(), x.data_ptr(), None, o.data_ptr(), 4, 40, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert L.tq2_gemm_act16(w.data_ptr(), x.data_ptr(), None, o.data_ptr(), 4, 32, 100, None) == tq2.TQ2_ERR_BAD_K
+    assert L.tq2_gemm_act16(w.data_ptr(), x.data_ptr(), None, o.data_ptr(), 0, 32, 128, None) == tq2.TQ2_OK
+    assert L.tq2_gemm_act16(w.data_ptr(), x.data_ptr() + 2, None, o.data_ptr(), 4, 32, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    f = torch.zeros(4, 24, device="cuda")
+    h = torch.zeros(4, 24, dtype=torch.float16, device="cuda")
+    assert L.tq2_act16_from_f32(f.data_ptr(), h.data_ptr(), 4, 24, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert L.tq2_act16_to_f32(h.data_ptr(), f.data_ptr(), 4, 24, None) == tq2.TQ2_ERR_INVALID_ARG
+    torch.cuda.synchronize()
