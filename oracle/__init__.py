@@ -19,7 +19,10 @@ batched, residual passthrough) and the SoA layout on a hand-built example plus
 the AoS->SoA->AoS round trip.  The gate/up SwiGLU (``swiglu``) is pinned by
 the closed form silu(ln 3) = 0.75 ln 3, the odd identity silu(z) - silu(-z) = z
 (flipping every gate code), zero gate or up rows, exact linearity in the up
-rows and the limits silu(z) -> z and -> 0.
+rows and the limits silu(z) -> z and -> 0.  The DiT joint attention
+(``attention``) is pinned by closed forms (identical keys give the mean of v,
+one key gives v, a two-key case is a logistic weight), a dominant key, and
+permutation equivariance over keys and queries.
 """
 
 from __future__ import annotations
@@ -213,3 +216,35 @@ def swiglu(w_aos, x, *, f: int, k: int, rows=None):
     out, absdot = matmul(w_aos, x, n=2 * f, k=k, rows=rows)
     g, u = out[:, :f], out[:, f:]
     return silu(g) * u, g, u, absdot[:, :f], absdot[:, f:]
+
+
+def attention(q, k, v, *, heads: int, seq: int, dim: int, rows=None):
+    """DiT joint multi-head attention, float64: the contract of the pages'
+    ``joint_attention_gpu`` ("oxibonsai-image 0.2.2 src/gpu.rs", its doc
+    comment; kernel ``joint_attention_flash_f32`` of "oxibonsai-kernels 0.1.5
+    src/gpu_backend/metal_graph/pipelines.rs", FLUX.2 DiT joint attention).
+
+    q, k, v: head-major [heads, seq, dim] (float32 inputs);
+    out[t, h*dim + d] = sum_j p[h, t, j] v[h, j, d] with
+    p[h, t, :] = softmax_j(q[h, t] . k[h, j] / sqrt(dim)) over all keys
+    (non-causal).  Token-major output [seq, heads*dim] (or the token rows
+    `rows`).  The softmax subtracts the row maximum before exponentiating.
+
+    Returns (out, absv): absv[t, h*dim + d] = sum_j p[h, t, j] |v[h, j, d]|, the
+    scale of the tolerance bounds.
+    """
+    q = np.asarray(q, dtype=np.float64).reshape(heads, seq, dim)
+    k = np.asarray(k, dtype=np.float64).reshape(heads, seq, dim)
+    v = np.asarray(v, dtype=np.float64).reshape(heads, seq, dim)
+    t = np.arange(seq) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.empty((t.size, heads * dim))
+    absv = np.empty((t.size, heads * dim))
+    scale = 1.0 / np.sqrt(dim)
+    for h in range(heads):
+        s = (q[h, t] @ k[h].T) * scale               # [rows, seq]
+        s -= s.max(axis=1, keepdims=True)
+        e = np.exp(s)
+        p = e / e.sum(axis=1, keepdims=True)
+        out[:, h * dim:(h + 1) * dim] = p @ v[h]
+        absv[:, h * dim:(h + 1) * dim] = p @ np.abs(v[h])
+    return out, absv

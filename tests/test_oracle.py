@@ -465,3 +465,67 @@ def test_swiglu_limits():
     h = oracle.swiglu(w, x, f=1, k=128)[0]
     assert abs(h[0, 0] - 120.0) < 1e-12
     assert abs(h[1, 0]) < 1e-15 * 3.0
+
+
+# --------------------------------------------------------------------------
+# DiT joint attention
+
+
+def test_attention_identical_keys_give_mean_of_v():
+    rng = np.random.default_rng(3)
+    h, n, d = 2, 7, 16
+    q = rng.standard_normal((h, n, d))
+    k = np.repeat(rng.standard_normal((h, 1, d)), n, axis=1)
+    v = rng.standard_normal((h, n, d))
+    out, _ = oracle.attention(q, k, v, heads=h, seq=n, dim=d)
+    for hh in range(h):
+        assert np.allclose(out[:, hh * d:(hh + 1) * d], v[hh].mean(axis=0)[None, :], rtol=0, atol=1e-14)
+
+
+def test_attention_single_key_and_token_major_layout():
+    rng = np.random.default_rng(4)
+    h, d = 3, 8
+    q, k, v = (rng.standard_normal((h, 1, d)) for _ in range(3))
+    out, _ = oracle.attention(q, k, v, heads=h, seq=1, dim=d)
+    assert np.array_equal(out[0], v[:, 0, :].reshape(-1))   # heads concatenated along features
+
+
+def test_attention_two_keys_logistic():
+    # dim 4, q = (a, 0, 0, 0), keys 0 and (b, 0, 0, 0): scores 0 and a b / 2, so
+    # the weight of key 1 is the logistic 1 / (1 + exp(-a b / 2))
+    a, b = 1.5, 0.8
+    q = np.array([[[a, 0, 0, 0]]])
+    k = np.array([[[0, 0, 0, 0], [b, 0, 0, 0]]], dtype=np.float64)
+    v = np.array([[[1.0, 2.0, 3.0, 4.0], [-5.0, 0.5, 7.0, 1.0]]])
+    q2 = np.concatenate([q, q], axis=1)  # two identical queries
+    out, _ = oracle.attention(q2, k, v, heads=1, seq=2, dim=4)
+    w1 = 1.0 / (1.0 + np.exp(-a * b / 2.0))
+    ref = (1 - w1) * v[0, 0] + w1 * v[0, 1]
+    assert np.allclose(out, ref[None, :], rtol=0, atol=1e-14)
+
+
+def test_attention_dominant_key():
+    rng = np.random.default_rng(5)
+    h, n, d = 1, 6, 8
+    q = np.zeros((h, n, d)); q[..., 0] = 1.0
+    k = rng.standard_normal((h, n, d)) * 0.1
+    k[0, 3, 0] = 200.0   # score 200/sqrt(8) above the rest: weight 1 - e^-70
+    v = rng.standard_normal((h, n, d))
+    out, _ = oracle.attention(q, k, v, heads=h, seq=n, dim=d)
+    assert np.allclose(out, v[0, 3][None, :], rtol=0, atol=1e-12)
+
+
+def test_attention_permutation_equivariance():
+    rng = np.random.default_rng(6)
+    h, n, d = 2, 9, 16
+    q, k, v = (rng.standard_normal((h, n, d)) for _ in range(3))
+    out, absv = oracle.attention(q, k, v, heads=h, seq=n, dim=d)
+    pk = rng.permutation(n)
+    out_k, _ = oracle.attention(q, k[:, pk], v[:, pk], heads=h, seq=n, dim=d)
+    assert np.allclose(out_k, out, rtol=0, atol=1e-13)
+    pq = rng.permutation(n)
+    out_q, _ = oracle.attention(q[:, pq], k, v, heads=h, seq=n, dim=d)
+    assert np.allclose(out_q, out[pq], rtol=0, atol=1e-13)
+    assert np.all(absv >= np.abs(out) - 1e-13)
+    sub, _ = oracle.attention(q, k, v, heads=h, seq=n, dim=d, rows=[4, 0])
+    assert np.array_equal(sub, out[[4, 0]])
