@@ -45,7 +45,7 @@ EXPORTS = (
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
     "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu", "tq2_act16_from_f32",
-    "tq2_act16_to_f32", "tq2_gemm_act16",
+    "tq2_act16_to_f32", "tq2_gemm_act16", "tq2_attention_f32",
 )
 
 
@@ -96,6 +96,8 @@ def _load():
     L.tq2_act16_to_f32.argtypes = [vp, vp, i64, i64, vp]
     L.tq2_gemm_act16.restype = i32
     L.tq2_gemm_act16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
+    L.tq2_attention_f32.restype = i32
+    L.tq2_attention_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gate_up_swiglu.restype = i32
     L.tq2_gate_up_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gemm_noalloc.restype = i32
@@ -181,6 +183,11 @@ def tq2_act16_to_f32(x16, x, m: int, k: int, stream=None) -> None:
 def tq2_gemm_act16(w_soa, x16, residual16, out16, m: int, n: int, k: int, stream=None) -> None:
     _check(lib.tq2_gemm_act16(_ptr(w_soa), _ptr(x16), _ptr(residual16), _ptr(out16), m, n, k,
                               _stream(stream)), "tq2_gemm_act16")
+
+
+def tq2_attention_f32(q, k, v, out, heads: int, seq: int, dim: int, stream=None) -> None:
+    _check(lib.tq2_attention_f32(_ptr(q), _ptr(k), _ptr(v), _ptr(out), heads, seq, dim, _stream(stream)),
+           "tq2_attention_f32")
 
 
 def tq2_gate_up_swiglu(w_soa, x, out, m: int, f: int, k: int, stream=None) -> None:

@@ -362,6 +362,30 @@ int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, v
     return finish(e);
 }
 
+int tq2_attention_f32(const float *q, const float *k, const float *v, float *out, int64_t heads,
+                      int64_t seq, int64_t dim, void *stream) {
+    if (heads < 0 || seq < 0 || (dim != 64 && dim != 128)) return TQ2_ERR_INVALID_ARG;
+    if (heads > 65535 || seq > (int64_t(1) << 24) || heads * ((seq + 127) / 128 * 128) > INT32_MAX)
+        return TQ2_ERR_INVALID_ARG;
+    if (heads == 0 || seq == 0) return TQ2_OK;
+    if (!q || !k || !v || !out) return TQ2_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out)) return TQ2_ERR_MISALIGNED;
+    const size_t nb = size_t(heads) * size_t(seq) * size_t(dim) * 4;
+    if (overlaps(out, nb, q, nb) || overlaps(out, nb, k, nb) || overlaps(out, nb, v, nb))
+        return TQ2_ERR_INVALID_ARG;
+    tq2::LaunchCtx ctx;
+    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    if (st != TQ2_OK) return st;
+    void *ws = nullptr;
+    if (cudaMallocAsync(&ws, tq2::attention_ws_bytes(heads, seq, dim), ctx.stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return TQ2_ERR_CUDA;
+    }
+    cudaError_t e = tq2::launch_attention(q, k, v, out, heads, seq, dim, ws, ctx);
+    const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
+    return finish(e != cudaSuccess ? e : f);
+}
+
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out, int64_t n,
              int64_t k, void *stream) {
     return tq2_gemm_with(TQ2_KERNEL_GEMV, w_soa, x, residual, out, 1, n, k, stream);

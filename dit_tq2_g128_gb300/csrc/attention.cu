@@ -1,0 +1,470 @@
+// DiT joint attention on the tcgen05 tensor cores (flash attention, one pass
+// over the keys with an online softmax).
+//
+// Contract of the pages' `joint_attention_gpu` ("oxibonsai-image 0.2.2
+// src/gpu.rs"; kernel `joint_attention_flash_f32` of "oxibonsai-kernels 0.1.5
+// src/gpu_backend/metal_graph/pipelines.rs", FLUX.2 DiT joint attention):
+// q, k, v head-major f32 [H, S, D]; out token-major f32 [S, H*D] (heads
+// concatenated along the features); scale 1/sqrt(D); non-causal softmax over
+// all S keys.
+//
+// Design (sm_103a):
+//  * Pre-pass: q -> binary16 pre-scaled by log2(e)/sqrt(D) (scores come out in
+//    log2 units for ex2), k -> binary16, v -> binary16 transposed per head
+//    ([H, D, Sp]); Sp = S rounded up to 128, padding zero.  All three are
+//    then K-major MMA operands loaded by tensor copies with the 128-byte
+//    swizzle.
+//  * One CTA per (head, 128 queries); keys in blocks of 128.  Warp 0 copies
+//    Q once and K, V^T tiles through two-stage rings; warp 1 issues the MMAs:
+//    S_j = Q K_j^T (M=128, N=128, K=D) into one of two TMEM score buffers,
+//    then O += P_{j-1} V_{j-1} (M=128, N=D, K=128) into the TMEM output, so
+//    the next scores are computed while the softmax works.  Warps 4-7 (one
+//    thread per query row = TMEM lane) read a score row, take the row maximum
+//    over the valid keys, write P = 2^(s - m) as binary16 into shared memory
+//    (the A operand of P V) and keep the running sum l.
+//  * Lazy rescale: the running maximum m changes (and O and l are rescaled by
+//    2^(m_old - m_new)) only when a block's maximum exceeds m by more than 8,
+//    so P <= 2^8 always fits binary16 and the rescale is rare.
+//  * Epilogue: out = O / l, f32.
+// Every wait is bounded; a timeout sets the device status word and the CTA
+// drains and exits.
+#include <algorithm>
+#include <cmath>
+#include <cstring>
+
+#include "tq2_internal.cuh"
+
+namespace tq2 {
+namespace {
+
+constexpr int AQ = 128;        // queries per CTA (MMA M)
+constexpr int AKB = 128;       // keys per block
+constexpr int ATHREADS = 256;  // warp 0 copies, warp 1 MMA + TMEM, warps 4-7 softmax
+constexpr int A_TMA = 0, A_MMA = 1, A_SM0 = 4;
+constexpr float kLazyLog2 = 8.0f;
+constexpr uint32_t ATMEM_COLS = 512;  // S buffers at 0 and 128, O at 256
+
+template <int D>
+struct AttnLayout {
+    static constexpr int SUB = 128 * 128;            // one swizzled 128-row x 64-element sub-tile
+    static constexpr int QB = AQ * D * 2;            // Q tile
+    static constexpr int KB = AKB * D * 2;           // one K tile
+    static constexpr int VB = D * AKB * 2;           // one V^T tile (D rows x 128 keys)
+    static constexpr int PB = AQ * AKB * 2;          // P tile
+    static constexpr int OFF_K = QB, OFF_V = OFF_K + 2 * KB, OFF_P = OFF_V + 2 * VB;
+    static constexpr int OFF_CTL = OFF_P + PB;
+    static constexpr int BYTES = OFF_CTL + 256 + 1024;  // barriers + alignment slack
+    // f32 accumulator D, binary16 A and B, both K-major; N >> 3 at bit 17, M >> 4 at bit 24
+    static constexpr uint32_t IDESC_S = (1u << 4) | (uint32_t(AKB >> 3) << 17) | (uint32_t(AQ >> 4) << 24);
+    static constexpr uint32_t IDESC_O = (1u << 4) | (uint32_t(D >> 3) << 17) | (uint32_t(AQ >> 4) << 24);
+};
+
+struct AttnCtl {
+    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2];
+    uint64_t p_full, pv_done, drain;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Shared-memory matrix descriptor of a K-major operand with the 128-byte
+// swizzle: rows 128 B apart, 8-row groups 1024 B apart.
+__device__ __forceinline__ uint64_t att_desc(uint32_t saddr) {
+    return uint64_t((saddr & 0x3FFFFu) >> 4) | (uint64_t(1) << 16) | (uint64_t(1024 >> 4) << 32) |
+           (uint64_t(1) << 46) | (uint64_t(2) << 61);
+}
+
+// Byte offset of 16-byte chunk j of row r in a swizzled sub-tile.
+__device__ __forceinline__ uint32_t att_sw_off(int r, int j) {
+    return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void att_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void att_tma_2d(uint32_t dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void att_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+          "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]),
+          "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]),
+          "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+
+__device__ __forceinline__ void att_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+        "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+        "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void att_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// 2^x by the hardware approximation (relative error about 2^-22; 2^-inf = 0)
+__device__ __forceinline__ float att_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <int D>
+__global__ void __launch_bounds__(ATHREADS, 1)
+attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
+                const __grid_constant__ CUtensorMap vmap, float *__restrict__ out, int H, int S, int Sp,
+                unsigned int *status, uint64_t wait_ns) {
+    using Lay = AttnLayout<D>;
+    extern __shared__ uint8_t att_raw[];
+    const uint32_t raw_addr = smem_u32(att_raw);
+    const uint32_t pad = (1024u - (raw_addr & 1023u)) & 1023u;
+    const uint32_t sbase = raw_addr + pad;
+    AttnCtl *ctl = reinterpret_cast<AttnCtl *>(att_raw + pad + Lay::OFF_CTL);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int qb = blockIdx.x, h = blockIdx.y;
+    const int nb = (S + AKB - 1) / AKB;  // key blocks
+    const uint32_t sQ = sbase, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V, sP = sbase + Lay::OFF_P;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&ctl->q_full, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ctl->k_full[b], 1);
+            mbar_init(&ctl->k_empty[b], 1);
+            mbar_init(&ctl->v_full[b], 1);
+            mbar_init(&ctl->v_empty[b], 1);
+            mbar_init(&ctl->s_full[b], 1);
+            mbar_init(&ctl->s_empty[b], 128);
+        }
+        mbar_init(&ctl->p_full, 128);
+        mbar_init(&ctl->pv_done, 1);
+        mbar_init(&ctl->drain, 1);
+        ctl->abort = 0;
+        fence_proxy_async_smem();
+    }
+    if (warp == A_MMA) {
+        tmem_alloc(&ctl->tmem_base, ATMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    volatile int *abort_flag = &ctl->abort;
+
+    if (warp == A_TMA) {
+        if (lane == 0) {
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+            asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+            att_expect_tx(&ctl->q_full, Lay::QB);
+            for (int sub = 0; sub < D / 64; ++sub)
+                att_tma_2d(sQ + sub * Lay::SUB, &qmap, sub * 64, h * Sp + qb * AQ, &ctl->q_full);
+            int issued = 0;
+            for (int j = 0; j < nb; ++j, ++issued) {
+                const int b = j & 1, u = j >> 1;
+                if (u > 0 && !mbar_wait_bounded(&ctl->k_empty[b], (u - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                att_expect_tx(&ctl->k_full[b], Lay::KB);
+                for (int sub = 0; sub < D / 64; ++sub)
+                    att_tma_2d(sK + b * Lay::KB + sub * Lay::SUB, &kmap, sub * 64, h * Sp + j * AKB, &ctl->k_full[b]);
+                if (u > 0 && !mbar_wait_bounded(&ctl->v_empty[b], (u - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                att_expect_tx(&ctl->v_full[b], Lay::VB);
+                for (int sub = 0; sub < AKB / 64; ++sub)
+                    att_tma_2d(sV + b * Lay::VB + sub * (D * 128), &vmap, j * AKB + sub * 64, h * D, &ctl->v_full[b]);
+            }
+            // every copy issued must land before the CTA exits: the last round of each slot
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            mbar_wait_bounded(&ctl->q_full, 0, drain, status);
+            for (int j = max(0, issued - 2); j < issued; ++j) {
+                mbar_wait_bounded(&ctl->k_full[j & 1], (j >> 1) & 1, drain, status);
+                mbar_wait_bounded(&ctl->v_full[j & 1], (j >> 1) & 1, drain, status);
+            }
+        }
+        __syncwarp();
+    } else if (warp == A_MMA) {
+        if (lane == 0) {
+            bool ok = mbar_wait_bounded(&ctl->q_full, 0, wait_ns, status);
+            if (!ok) *abort_flag = 1;
+            tc_fence_after();
+            for (int j = 0; j <= nb && ok; ++j) {
+                if (j < nb) {
+                    const int b = j & 1, u = j >> 1;
+                    if (!mbar_wait_bounded(&ctl->k_full[b], u & 1, wait_ns, status) ||
+                        (u > 0 && !mbar_wait_bounded(&ctl->s_empty[b], (u - 1) & 1, wait_ns, status))) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        tc_mma_f16(tmem + uint32_t(b * AKB),
+                                   att_desc(sQ + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
+                                   att_desc(sK + b * Lay::KB + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
+                                   Lay::IDESC_S, kk > 0);
+                    tc_commit(&ctl->s_full[b]);
+                    tc_commit(&ctl->k_empty[b]);
+                }
+                if (j > 0) {
+                    const int jj = j - 1, bb = jj & 1, uu = jj >> 1;
+                    if (!mbar_wait_bounded(&ctl->p_full, jj & 1, wait_ns, status) ||
+                        !mbar_wait_bounded(&ctl->v_full[bb], uu & 1, wait_ns, status)) {
+                        *abort_flag = 1;
+                        break;
+                    }
+                    if (*abort_flag) break;
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < AKB / 16; ++kk)
+                        tc_mma_f16(tmem + 2u * AKB, att_desc(sP + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
+                                   att_desc(sV + bb * Lay::VB + (kk >> 2) * (D * 128)) + 2 * (kk & 3),
+                                   Lay::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+                    tc_commit(&ctl->pv_done);
+                    tc_commit(&ctl->v_empty[bb]);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp >= A_SM0) {
+        const int quarter = warp - A_SM0;
+        const int r = quarter * 32 + lane;             // query row in the tile = TMEM lane
+        const uint32_t tl = uint32_t(quarter * 32) << 16;
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nb; ++j) {
+            const int b = j & 1, u = j >> 1;
+            if (!mbar_wait_bounded(&ctl->s_full[b], u & 1, wait_ns, status)) *abort_flag = 1;
+            if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t ts = tmem + tl + uint32_t(b * AKB);
+            const int kvalid = S - j * AKB;  // keys of this block below S
+            // pass 1: row maximum over the valid keys
+            float mx = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < AKB / 32; ++c) {
+                uint32_t v[32];
+                att_ld32(ts + uint32_t(c * 32), v);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (c * 32 + i < kvalid) mx = fmaxf(mx, __uint_as_float(v[i]));
+            }
+            const bool grow = j == 0 || mx > m + kLazyLog2;
+            const float mu = grow ? mx : m;
+            const float alpha = grow ? att_ex2(m - mu) : 1.f;
+            // pass 2: P = 2^(s - mu) in binary16, and the sum of the rounded values
+            uint32_t pk[AKB / 2];
+            float lsum = 0.f;
+#pragma unroll
+            for (int c = 0; c < AKB / 32; ++c) {
+                uint32_t v[32];
+                att_ld32(ts + uint32_t(c * 32), v);
+                tc_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    const float p0 = c * 32 + i < kvalid ? att_ex2(__uint_as_float(v[i]) - mu) : 0.f;
+                    const float p1 = c * 32 + i + 1 < kvalid ? att_ex2(__uint_as_float(v[i + 1]) - mu) : 0.f;
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    lsum += __low2float(hp) + __high2float(hp);
+                    pk[c * 16 + i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+            }
+            // this S buffer is read: the next-but-one block may overwrite it
+            tc_fence_before();
+            mbar_arrive(&ctl->s_empty[b]);
+            // P of the previous block has been consumed and O is stable
+            if (j > 0) {
+                if (!mbar_wait_bounded(&ctl->pv_done, (j - 1) & 1, wait_ns, status)) *abort_flag = 1;
+                if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, grow)) {
+                    // rescale this row of O (rows that keep m scale by 1)
+#pragma unroll 1
+                    for (int c = 0; c < D / 32; ++c) {
+                        uint32_t o[32];
+                        att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                        tc_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        att_st32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    }
+                    att_wait_st();
+                }
+            }
+            l = l * alpha + lsum;
+            m = mu;
+            // P row r: keys 64s + 8c .. +7 in 16-byte chunk c of sub-tile s
+#pragma unroll
+            for (int q = 0; q < AKB / 8; ++q) {
+                const uint32_t addr = sP + uint32_t((q >> 3) * Lay::SUB) + att_sw_off(r, q & 7);
+                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * q]),
+                             "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
+                             : "memory");
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&ctl->p_full);
+        }
+        if (ok) {
+            if (!mbar_wait_bounded(&ctl->pv_done, (nb - 1) & 1, wait_ns, status)) *abort_flag = 1;
+            if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+                tc_fence_after();
+                const float inv = 1.0f / l;
+                const int t = qb * AQ + r;
+                float *orow = out + int64_t(t) * H * D + int64_t(h) * D;
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    tc_wait_ld();
+                    if (t < S) {
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4)
+                            *reinterpret_cast<float4 *>(orow + c * 32 + i) =
+                                make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == A_MMA) {
+        if (lane == 0) {
+            // every issued MMA must be complete before TMEM is released
+            tc_commit(&ctl->drain);
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            mbar_wait_bounded(&ctl->drain, 0, drain, status);
+        }
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, ATMEM_COLS);
+    }
+}
+
+// q, k -> binary16 [H][Sp][D] (q times `scale`), zero rows past S; 8 elements per item.
+__global__ void __launch_bounds__(256)
+attn_prep_qk_kernel(const float *__restrict__ src, __half *__restrict__ dst, int H, int S, int Sp, int D,
+                    float scale) {
+    const int64_t items = int64_t(H) * Sp * (D / 8), stride = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
+        const int64_t row = it / (D / 8);  // h * Sp + s
+        const int g = int(it % (D / 8));
+        const int h = int(row / Sp), s = int(row % Sp);
+        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (s < S) {
+            const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t(h) * S + s) * D + g * 8);
+            const float4 a = __ldcs(p), c = __ldcs(p + 1);
+            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+        }
+        uint4 o;
+        __half2 t0 = __floats2half2_rn(f[0] * scale, f[1] * scale), t1 = __floats2half2_rn(f[2] * scale, f[3] * scale);
+        __half2 t2 = __floats2half2_rn(f[4] * scale, f[5] * scale), t3 = __floats2half2_rn(f[6] * scale, f[7] * scale);
+        o.x = *reinterpret_cast<uint32_t *>(&t0);
+        o.y = *reinterpret_cast<uint32_t *>(&t1);
+        o.z = *reinterpret_cast<uint32_t *>(&t2);
+        o.w = *reinterpret_cast<uint32_t *>(&t3);
+        *reinterpret_cast<uint4 *>(dst + row * D + g * 8) = o;
+    }
+}
+
+// v [H][S][D] -> binary16 v^T [H][D][Sp], zero keys past S: 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256)
+attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S, int Sp, int D) {
+    __shared__ float tile[32][33];
+    const int s0 = blockIdx.x * 32, d0 = blockIdx.y * 32, h = blockIdx.z;
+    for (int i = threadIdx.y; i < 32; i += 8) {
+        const int s = s0 + i;
+        tile[i][threadIdx.x] = s < S ? v[(int64_t(h) * S + s) * D + d0 + threadIdx.x] : 0.f;
+    }
+    __syncthreads();
+    for (int i = threadIdx.y; i < 32; i += 8)
+        vt[(int64_t(h) * D + d0 + i) * Sp + s0 + threadIdx.x] = __float2half_rn(tile[threadIdx.x][i]);
+}
+
+template <int D>
+cudaError_t launch_attention_d(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
+                               void *ws, const LaunchCtx &ctx) {
+    using Lay = AttnLayout<D>;
+    const int64_t Sp = (S + 127) / 128 * 128;
+    __half *qh = static_cast<__half *>(ws);
+    __half *kh = qh + H * Sp * D;
+    __half *vt = kh + H * Sp * D;
+    const float qscale = 1.4426950408889634f / sqrtf(float(D));  // log2(e) / sqrt(D)
+    const int64_t items = H * Sp * (D / 8);
+    const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
+    attn_prep_qk_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(q, qh, int(H), int(S), int(Sp), D, qscale);
+    attn_prep_qk_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(k, kh, int(H), int(S), int(Sp), D, 1.0f);
+    attn_prep_vt_kernel<<<dim3(unsigned(Sp / 32), unsigned(D / 32), unsigned(H)), dim3(32, 8), 0, ctx.stream>>>(
+        v, vt, int(S), int(Sp), D);
+    cudaError_t e = cudaPeekAtLastError();
+    if (e != cudaSuccess) return e;
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    CUtensorMap qmap, kmap, vmap;
+    const cuuint32_t estride[2] = {1, 1};
+    const cuuint64_t qkdim[2] = {cuuint64_t(D), cuuint64_t(H * Sp)};
+    const cuuint64_t qkstride[1] = {cuuint64_t(D) * 2};
+    const cuuint32_t qkbox[2] = {64, 128};
+    const cuuint64_t vdim[2] = {cuuint64_t(Sp), cuuint64_t(H * D)};
+    const cuuint64_t vstride[1] = {cuuint64_t(Sp) * 2};
+    const cuuint32_t vbox[2] = {64, cuuint32_t(D)};
+    if (enc(&qmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, qh, qkdim, qkstride, qkbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, kh, qkdim, qkstride, qkbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS ||
+        enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, vt, vdim, vstride, vbox, estride,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES);
+    if (e != cudaSuccess) return e;
+    attn_fwd_kernel<D><<<dim3(unsigned(Sp / AQ), unsigned(H)), ATHREADS, Lay::BYTES, ctx.stream>>>(
+        qmap, kmap, vmap, out, int(H), int(S), int(Sp), ctx.status, ctx.wait_ns);
+    return cudaPeekAtLastError();
+}
+
+}  // namespace
+
+size_t attention_ws_bytes(int64_t H, int64_t S, int64_t D) {
+    const int64_t Sp = (S + 127) / 128 * 128;
+    return size_t(3) * size_t(H) * size_t(Sp) * size_t(D) * 2;
+}
+
+cudaError_t launch_attention(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
+                             int64_t D, void *ws, const LaunchCtx &ctx) {
+    if (H > 65535 || S > (int64_t(1) << 24) || H * ((S + 127) / 128 * 128) > INT32_MAX) return cudaErrorInvalidValue;
+    if (D == 128) return launch_attention_d<128>(q, k, v, out, H, S, ws, ctx);
+    if (D == 64) return launch_attention_d<64>(q, k, v, out, H, S, ws, ctx);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace tq2

@@ -216,6 +216,30 @@ int tq2_act16_to_f32(const void *x16, float *x, int64_t m, int64_t k, void *stre
 int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, void *out16,
                    int64_t m, int64_t n, int64_t k, void *stream);
 
+/* DiT joint multi-head attention (the pages' `joint_attention_gpu`,
+ * "oxibonsai-image 0.2.2 src/gpu.rs", and its kernel
+ * `joint_attention_flash_f32`, "oxibonsai-kernels 0.1.5
+ * src/gpu_backend/metal_graph/pipelines.rs"):
+ *   out[t, h*dim + d] = sum_j softmax_j(q[h,t] . k[h,j] / sqrt(dim)) v[h,j,d]
+ * over all seq keys (non-causal).
+ *   q, k, v : device f32 [heads, seq, dim], head-major (RoPE already applied)
+ *   out     : device f32 [seq, heads*dim], token-major (may not overlap q, k, v)
+ *   dim     : 64 or 128
+ * Arithmetic: q (times log2(e)/sqrt(dim)), k and v are rounded to binary16
+ * (nearest even; their magnitudes must stay below 65504) and multiplied on the
+ * tensor cores with f32 accumulation; the softmax runs in f32 with the
+ * hardware 2^x, its weights rounded to binary16 for the second product; the
+ * normalisation by the weight sum is the last step (flash attention: one pass
+ * over the keys, no [seq, seq] matrix in memory).
+ * Memory: a temporary of 3*heads*ceil(seq/128)*128*dim*2 bytes from the
+ * device's default memory pool, ordered on `stream`.
+ * Errors: TQ2_ERR_INVALID_ARG (dim not 64 or 128, negative or too large sizes
+ * (heads <= 65535, seq <= 2^24), NULL, overlap), TQ2_ERR_MISALIGNED (pointers
+ * not 16-byte aligned), TQ2_ERR_TIMEOUT via tq2_device_status, TQ2_ERR_CUDA.
+ * heads = 0 or seq = 0: no-op. */
+int tq2_attention_f32(const float *q, const float *k, const float *v, float *out, int64_t heads,
+                      int64_t seq, int64_t dim, void *stream);
+
 /* Same operation as tq2_gemm, computed by the exact-f32 CUDA-core tiled
  * kernel (the role of the pages' non-matrix-unit `gemm_tq2_g128_v8_tiled`,
  * kept for tolerance checks). */

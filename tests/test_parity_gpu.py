@@ -657,3 +657,77 @@ def test_act16_errors(tq2):
     assert L.tq2_act16_from_f32(f.data_ptr(), h.data_ptr(), 4, 24, None) == tq2.TQ2_ERR_INVALID_ARG
     assert L.tq2_act16_to_f32(h.data_ptr(), f.data_ptr(), 4, 24, None) == tq2.TQ2_ERR_INVALID_ARG
     torch.cuda.synchronize()
+
+
+# ---------------------------------------------------------------------------
+# DiT joint attention
+
+def run_attention(tq2, q, k, v, h, s, d):
+    qd, kd, vd = (torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda() for a in (q, k, v))
+    out = torch.full((s, h * d), float("nan"), dtype=torch.float32, device="cuda")
+    tq2.tq2_attention_f32(qd, kd, vd, out, h, s, d)
+    torch.cuda.synchronize()
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    return out.cpu().numpy()
+
+
+def check_attention(got, q, k, v, h, s, d, *, rows=None, what=""):
+    """Per element: |out - ref| <= (2.1 ds + 4 * 2^-11) * sum_j p_j |v_j|, with
+    ds = 2^-10 max_j sum_e |q_e k_je| / sqrt(d) the score error from rounding q
+    and k to binary16 (carried through the softmax), and the 2^-11 terms for
+    rounding P and v and the normalisation; plus cosine >= 0.9999 per row."""
+    ref, absv = oracle.attention(q, k, v, heads=h, seq=s, dim=d, rows=rows)
+    t = np.arange(s) if rows is None else np.asarray(rows)
+    qa = np.abs(q.reshape(h, s, d).astype(np.float64))[:, t]
+    ka = np.abs(k.reshape(h, s, d).astype(np.float64))
+    ds = np.stack([(qa[hh] @ ka[hh].T).max(axis=1) for hh in range(h)], axis=1) * 2.0 ** -10 / np.sqrt(d)
+    bound = (2.1 * np.repeat(ds, d, axis=1) + 4 * 2.0 ** -11) * absv + 1e-30
+    got = got if rows is None else got[t]
+    err = np.abs(got - ref)
+    assert np.all(np.isfinite(got)), what
+    assert np.all(err <= bound), f"{what}: max err/bound {float(np.max(err / bound)):.3g}"
+    num = np.sum(got * ref, axis=1)
+    den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+    c = np.where(den > 0, num / np.where(den > 0, den, 1), 1.0)
+    assert np.all(c >= COS_MIN), f"{what}: min row cosine {c.min()}"
+
+
+@pytest.mark.parametrize("h,s,d", [(1, 128, 128), (2, 300, 128), (3, 77, 64), (1, 1, 128), (4, 1024, 128),
+                                   (2, 513, 64)])
+def test_attention_parity(tq2, h, s, d):
+    rng = np.random.default_rng(h * 1000 + s + d)
+    q, k, v = (rng.standard_normal((h, s, d)).astype(np.float32) for _ in range(3))
+    check_attention(run_attention(tq2, q, k, v, h, s, d), q, k, v, h, s, d, what=f"attn h={h} s={s} d={d}")
+
+
+def test_attention_growing_scores_rescale(tq2):
+    # scores that grow block after block (keys scaled up with their index) and a
+    # wide range (q times 4): the running maximum moves by more than 2^8 several
+    # times, so O and the sum are rescaled
+    h, s, d = 2, 640, 128
+    rng = np.random.default_rng(9)
+    q = (rng.standard_normal((h, s, d)) * 4).astype(np.float32)
+    k = (rng.standard_normal((h, s, d)) * np.linspace(0.2, 3.0, s)[None, :, None]).astype(np.float32)
+    v = rng.standard_normal((h, s, d)).astype(np.float32)
+    check_attention(run_attention(tq2, q, k, v, h, s, d), q, k, v, h, s, d, what="attn rescale")
+
+
+def test_attention_dit_shape_sampled(tq2):
+    # FLUX.2-sized: 24 heads of 128 (3072 features), 4096 tokens; sampled rows
+    h, s, d = 24, 4096, 128
+    rng = np.random.default_rng(24)
+    q, k, v = (rng.standard_normal((h, s, d)).astype(np.float32) for _ in range(3))
+    got = run_attention(tq2, q, k, v, h, s, d)
+    check_attention(got, q, k, v, h, s, d, rows=sample_rows(s), what="attn dit")
+
+
+def test_attention_errors(tq2):
+    a = torch.zeros(2, 128, 128, device="cuda")
+    o = torch.zeros(128, 256, device="cuda")
+    L = tq2.lib
+    assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 128, 96, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 0, 128, 128, None) == tq2.TQ2_OK
+    assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 0, 128, None) == tq2.TQ2_OK
+    assert L.tq2_attention_f32(a.data_ptr() + 4, a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 128, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), a.data_ptr(), 2, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    torch.cuda.synchronize()
