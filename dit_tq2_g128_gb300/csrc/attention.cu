@@ -52,19 +52,22 @@ struct AttnLayout {
     static constexpr int VB = D * AKB * 2;           // one V^T tile (D rows x 128 keys)
     static constexpr int PB = AQ * AKB * 2;          // P tile
     static constexpr int OFF_K = QB, OFF_V = OFF_K + 2 * KB, OFF_P = OFF_V + 2 * VB;
-    static constexpr int OFF_CTL = OFF_P + PB;
+    static constexpr int OFF_CTL = OFF_P + 2 * PB;   // two P buffers
     static constexpr int BYTES = OFF_CTL + 256 + 1024;  // barriers + alignment slack
     // f32 accumulator D, binary16 A and B, both K-major; N >> 3 at bit 17, M >> 4 at bit 24
     static constexpr uint32_t IDESC_S = (1u << 4) | (uint32_t(AKB >> 3) << 17) | (uint32_t(AQ >> 4) << 24);
     static constexpr uint32_t IDESC_O = (1u << 4) | (uint32_t(D >> 3) << 17) | (uint32_t(AQ >> 4) << 24);
 };
 
+static_assert(AttnLayout<128>::BYTES <= 232448, "shared memory budget");
+
 struct AttnCtl {
     uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2];
-    uint64_t p_full, pv_done, drain;
+    uint64_t p_full[2], pv_done[2], drain;  // per P buffer (block j uses buffer j % 2)
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(AttnCtl) <= 256, "control block");
 
 // Shared-memory matrix descriptor of a K-major operand with the 128-byte
 // swizzle: rows 128 B apart, 8-row groups 1024 B apart.
@@ -152,8 +155,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             mbar_init(&ctl->s_full[b], 1);
             mbar_init(&ctl->s_empty[b], 128);
         }
-        mbar_init(&ctl->p_full, 128);
-        mbar_init(&ctl->pv_done, 1);
+        mbar_init(&ctl->p_full[0], 128);
+        mbar_init(&ctl->p_full[1], 128);
+        mbar_init(&ctl->pv_done[0], 1);
+        mbar_init(&ctl->pv_done[1], 1);
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         fence_proxy_async_smem();
@@ -231,7 +236,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 }
                 if (j > 0) {
                     const int jj = j - 1, bb = jj & 1, uu = jj >> 1;
-                    if (!mbar_wait_bounded(&ctl->p_full, jj & 1, wait_ns, status) ||
+                    if (!mbar_wait_bounded(&ctl->p_full[bb], uu & 1, wait_ns, status) ||
                         !mbar_wait_bounded(&ctl->v_full[bb], uu & 1, wait_ns, status)) {
                         *abort_flag = 1;
                         break;
@@ -240,10 +245,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                     tc_fence_after();
 #pragma unroll
                     for (int kk = 0; kk < AKB / 16; ++kk)
-                        tc_mma_f16(tmem + 2u * AKB, att_desc(sP + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
+                        tc_mma_f16(tmem + 2u * AKB, att_desc(sP + bb * Lay::PB + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
                                    att_desc(sV + bb * Lay::VB + (kk >> 2) * (D * 128)) + 2 * (kk & 3),
                                    Lay::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&ctl->pv_done);
+                    tc_commit(&ctl->pv_done[bb]);
                     tc_commit(&ctl->v_empty[bb]);
                 }
             }
@@ -257,80 +262,111 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
             const int b = j & 1, u = j >> 1;
-            if (!mbar_wait_bounded(&ctl->s_full[b], u & 1, wait_ns, status)) *abort_flag = 1;
+            // S_j is ready, and P buffer b is free once P V of block j - 2 is done
+            if (!mbar_wait_bounded(&ctl->s_full[b], u & 1, wait_ns, status) ||
+                (j >= 2 && !mbar_wait_bounded(&ctl->pv_done[b], ((j - 2) >> 1) & 1, wait_ns, status)))
+                *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
             tc_fence_after();
             const uint32_t ts = tmem + tl + uint32_t(b * AKB);
+            const uint32_t pbuf = sP + uint32_t(b * Lay::PB);
             const int kvalid = S - j * AKB;  // keys of this block below S
-            // pass 1: row maximum over the valid keys
-            float mx = -INFINITY;
+            // P = 2^(s - mu) in binary16, stored to P buffer b as it is made,
+            // and its f32 row sum, optionally tracking the block maximum.  The
+            // next pair of score chunks is read while the current one is
+            // processed.  For blocks after the first the pass is speculative
+            // with the running maximum mu = m, redone (once, same code) only if
+            // a row's block maximum exceeds m by more than 8.
+            float lsum = 0.f, mx = -INFINITY;
+            float mu = m;
+            bool track = j > 0, grow = true;
+            if (j == 0) {
 #pragma unroll
-            for (int c = 0; c < AKB / 32; ++c) {
-                uint32_t v[32];
-                att_ld32(ts + uint32_t(c * 32), v);
-                tc_wait_ld();
+                for (int cp = 0; cp < AKB / 64; ++cp) {
+                    uint32_t va[32], vb[32];
+                    att_ld32(ts + uint32_t(cp * 64), va);
+                    att_ld32(ts + uint32_t(cp * 64 + 32), vb);
+                    tc_wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    if (c * 32 + i < kvalid) mx = fmaxf(mx, __uint_as_float(v[i]));
-            }
-            const bool grow = j == 0 || mx > m + kLazyLog2;
-            const float mu = grow ? mx : m;
-            const float alpha = grow ? att_ex2(m - mu) : 1.f;
-            // pass 2: P = 2^(s - mu) in binary16, and the sum of the rounded values
-            uint32_t pk[AKB / 2];
-            float lsum = 0.f;
-#pragma unroll
-            for (int c = 0; c < AKB / 32; ++c) {
-                uint32_t v[32];
-                att_ld32(ts + uint32_t(c * 32), v);
-                tc_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const float p0 = c * 32 + i < kvalid ? att_ex2(__uint_as_float(v[i]) - mu) : 0.f;
-                    const float p1 = c * 32 + i + 1 < kvalid ? att_ex2(__uint_as_float(v[i + 1]) - mu) : 0.f;
-                    const __half2 hp = __floats2half2_rn(p0, p1);
-                    lsum += __low2float(hp) + __high2float(hp);
-                    pk[c * 16 + i / 2] = *reinterpret_cast<const uint32_t *>(&hp);
+                    for (int i = 0; i < 64; ++i)
+                        if (cp * 64 + i < kvalid) mx = fmaxf(mx, __uint_as_float(i < 32 ? va[i] : vb[i - 32]));
                 }
+                mu = mx;
             }
+            // keys kb0 .. kb0 + 63 from the chunk pair (x0: first 32, x1: next 32)
+            auto half_pass = [&](const uint32_t (&x0)[32], const uint32_t (&x1)[32], int kb0) {
+#pragma unroll
+                for (int c8 = 0; c8 < 8; ++c8) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int i = c8 * 8 + 2 * e;  // 0..62
+                        const uint32_t u0 = i < 32 ? x0[i] : x1[i - 32], u1 = i < 32 ? x0[i + 1] : x1[i - 31];
+                        const int key = kb0 + i;
+                        const float s0 = key < kvalid ? __uint_as_float(u0) : -INFINITY;
+                        const float s1 = key + 1 < kvalid ? __uint_as_float(u1) : -INFINITY;
+                        if (track) mx = fmaxf(mx, fmaxf(s0, s1));
+                        const float p0 = att_ex2(s0 - mu), p1 = att_ex2(s1 - mu);
+                        lsum += p0 + p1;
+                        const __half2 hp = __floats2half2_rn(p0, p1);
+                        w[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                    }
+                    // keys kb0 + 8 c8 .. +7: 16-byte chunk c8 of sub-tile kb0 / 64, row r
+                    const uint32_t addr = pbuf + uint32_t((kb0 >> 6) * Lay::SUB) + att_sw_off(r, c8);
+                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
+                                 "r"(w[2]), "r"(w[3])
+                                 : "memory");
+                }
+            };
+#pragma unroll 1
+            for (int pass = 0; pass < 2; ++pass) {
+                lsum = 0.f;
+                uint32_t a0[32], a1[32], b0[32], b1[32];
+                att_ld32(ts, a0);
+                att_ld32(ts + 32u, a1);
+                tc_wait_ld();
+                att_ld32(ts + 64u, b0);
+                att_ld32(ts + 96u, b1);
+                half_pass(a0, a1, 0);
+                tc_wait_ld();
+                half_pass(b0, b1, 64);
+                if (!track) break;
+                grow = mx > m + kLazyLog2;
+                if (!__any_sync(0xffffffffu, grow)) break;
+                mu = grow ? mx : m;
+                track = false;
+            }
+            const float alpha = grow ? att_ex2(m - mu) : 1.f;
             // this S buffer is read: the next-but-one block may overwrite it
             tc_fence_before();
             mbar_arrive(&ctl->s_empty[b]);
-            // P of the previous block has been consumed and O is stable
-            if (j > 0) {
-                if (!mbar_wait_bounded(&ctl->pv_done, (j - 1) & 1, wait_ns, status)) *abort_flag = 1;
+            if (j > 0 && __any_sync(0xffffffffu, grow)) {
+                // rescale this row of O (rows that keep m scale by 1) once
+                // P V of block j - 1 has accumulated into it
+                if (!mbar_wait_bounded(&ctl->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, wait_ns, status))
+                    *abort_flag = 1;
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, grow)) {
-                    // rescale this row of O (rows that keep m scale by 1)
 #pragma unroll 1
-                    for (int c = 0; c < D / 32; ++c) {
-                        uint32_t o[32];
-                        att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
-                        tc_wait_ld();
+                for (int c = 0; c < D / 32; ++c) {
+                    uint32_t o[32];
+                    att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    tc_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        att_st32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
-                    }
-                    att_wait_st();
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    att_st32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
                 }
+                att_wait_st();
             }
             l = l * alpha + lsum;
             m = mu;
-            // P row r: keys 64s + 8c .. +7 in 16-byte chunk c of sub-tile s
-#pragma unroll
-            for (int q = 0; q < AKB / 8; ++q) {
-                const uint32_t addr = sP + uint32_t((q >> 3) * Lay::SUB) + att_sw_off(r, q & 7);
-                asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(pk[4 * q]),
-                             "r"(pk[4 * q + 1]), "r"(pk[4 * q + 2]), "r"(pk[4 * q + 3])
-                             : "memory");
-            }
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&ctl->p_full);
+            mbar_arrive(&ctl->p_full[b]);
         }
         if (ok) {
-            if (!mbar_wait_bounded(&ctl->pv_done, (nb - 1) & 1, wait_ns, status)) *abort_flag = 1;
+            if (!mbar_wait_bounded(&ctl->pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, wait_ns, status))
+                *abort_flag = 1;
             if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
                 tc_fence_after();
                 const float inv = 1.0f / l;
