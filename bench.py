@@ -606,6 +606,30 @@ def run_suite(args, local):
                      "entry": "tq2_gemm_act16", "us_total": round(tot_t * 1e6, 1),
                      "TFLOPs": round(tot_f / tot_t / 1e12, 2), "max_err_over_sum_abs_xw": worst,
                      "min_row_cos": cmin, "parity_rows": "2 sampled rows per layer"})
+    # DiT joint attention at the FLUX.2 shape: 24 heads x 128, 4096 tokens (4 H S^2 D flops)
+    ha, sa, da = 24, 4096, 128
+    rng = np.random.default_rng(24)
+    qa, ka, va = (rng.standard_normal((ha, sa, da)).astype(np.float32) for _ in range(3))
+    qd, kd, vd = (torch.from_numpy(a).to(device) for a in (qa, ka, va))
+    oa = torch.empty((sa, ha * da), dtype=torch.float32, device=device)
+    t = timed(lambda i: tq2.tq2_attention_f32(qd, kd, vd, oa, ha, sa, da), 5)
+    tq2.tq2_attention_f32(qd, kd, vd, oa, ha, sa, da)
+    torch.cuda.synchronize()
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    rows = sample(sa, 16)
+    t0 = time.perf_counter()
+    ref, absv = oracle.attention(qa, ka, va, heads=ha, seq=sa, dim=da, rows=rows)
+    t_or = time.perf_counter() - t0
+    got = oa.cpu().numpy().astype(np.float64)[rows]
+    num = np.sum(got * ref, axis=1)
+    den = np.linalg.norm(got, axis=1) * np.linalg.norm(ref, axis=1)
+    rows_out.append({"config": "DiT joint attention 24 x 4096 x 128", "entry": "tq2_attention_f32",
+                     "us_per_call": round(t * 1e6, 2), "TFLOPs": round(4.0 * ha * sa * sa * da / t / 1e12, 2),
+                     "max_err_over_sum_p_abs_v": float(np.max(np.abs(got - ref) / np.maximum(absv, 1e-30))),
+                     "min_row_cos": float(np.min(num / den)), "parity_rows": int(rows.size),
+                     "oracle_s_full_extrapolated": round(t_or * sa / rows.size, 3)})
+    del qd, kd, vd, oa
+    torch.cuda.empty_cache()
     # the encoder (f32 -> blocks) on the largest DiT weight: f32 bytes read per second
     n, k = 12288, 3072
     wf = torch.randn((n, k), device=device) * 0.02
