@@ -108,7 +108,8 @@ int make_ctx(cudaStream_t stream, tq2::LaunchCtx *ctx) {
 int finish(cudaError_t e) { return e == cudaSuccess ? TQ2_OK : TQ2_ERR_CUDA; }
 
 // M at and above which the tcgen05 kernel beats the f32 CUDA-core small-M kernel.
-constexpr int64_t kTcMinM = 4;
+// (measured at K = N = 4096: M=2 15.4 vs 17.6 us, M=3 20.8 vs 17.6 us)
+constexpr int64_t kTcMinM = 3;
 
 }  // namespace
 

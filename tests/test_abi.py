@@ -54,8 +54,9 @@ def test_kernel_selection(tq2):
     assert tq2.tq2_select_kernel(1, 4096, 12288) == tq2.TQ2_KERNEL_GEMV
     assert tq2.tq2_select_kernel(1536, 3072, 3072) == tq2.TQ2_KERNEL_TC
     assert tq2.tq2_select_kernel(4096, 3072, 12288) == tq2.TQ2_KERNEL_TC
-    for m in (2, 3, 7, 8, 9, 16, 64, 100):
-        assert tq2.tq2_select_kernel(m, 4096, 4096) in (tq2.TQ2_KERNEL_SKINNY, tq2.TQ2_KERNEL_TC)
+    assert tq2.tq2_select_kernel(2, 4096, 4096) == tq2.TQ2_KERNEL_SKINNY
+    for m in (3, 7, 8, 9, 16, 64, 100):
+        assert tq2.tq2_select_kernel(m, 4096, 4096) == tq2.TQ2_KERNEL_TC
 
 
 def rc_gemm(tq2, w, x, r, o, m, n, k, kernel=0):
