@@ -404,10 +404,14 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     }
 }
 
-// q, k -> binary16 [H][Sp][D] (q times `scale`), zero rows past S; 8 elements per item.
+// q, k -> binary16 [H][Sp][D] (blockIdx.y = 0: q times `qscale`; 1: k), zero
+// rows past S; 8 elements per item.
 __global__ void __launch_bounds__(256)
-attn_prep_qk_kernel(const float *__restrict__ src, __half *__restrict__ dst, int H, int S, int Sp, int D,
-                    float scale) {
+attn_prep_qk_kernel(const float *__restrict__ q, const float *__restrict__ k, __half *__restrict__ qh,
+                    __half *__restrict__ kh, int H, int S, int Sp, int D, float qscale) {
+    const float *src = blockIdx.y ? k : q;
+    __half *dst = blockIdx.y ? kh : qh;
+    const float scale = blockIdx.y ? 1.0f : qscale;
     const int64_t items = int64_t(H) * Sp * (D / 8), stride = int64_t(gridDim.x) * blockDim.x;
     for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
         const int64_t row = it / (D / 8);  // h * Sp + s
@@ -430,18 +434,32 @@ attn_prep_qk_kernel(const float *__restrict__ src, __half *__restrict__ dst, int
     }
 }
 
-// v [H][S][D] -> binary16 v^T [H][D][Sp], zero keys past S: 32 x 32 tiles through shared memory.
+// v [H][S][D] -> binary16 v^T [H][D][Sp], zero keys past S: 64 keys x 64 features
+// per block through shared memory, 16-byte reads and writes.
 __global__ void __launch_bounds__(256)
 attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S, int Sp, int D) {
-    __shared__ float tile[32][33];
-    const int s0 = blockIdx.x * 32, d0 = blockIdx.y * 32, h = blockIdx.z;
-    for (int i = threadIdx.y; i < 32; i += 8) {
-        const int s = s0 + i;
-        tile[i][threadIdx.x] = s < S ? v[(int64_t(h) * S + s) * D + d0 + threadIdx.x] : 0.f;
+    __shared__ __align__(16) __half tile[64][72];  // [feature][key], 8 halves of padding
+    const int s0 = blockIdx.x * 64, d0 = blockIdx.y * 64, h = blockIdx.z;
+    const int t = threadIdx.x;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int idx = t + 256 * i;           // 0..1023: key idx / 16, features 4 (idx % 16) .. +3
+        const int key = idx >> 4, f4 = idx & 15;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (s0 + key < S) x = __ldcs(reinterpret_cast<const float4 *>(v + (int64_t(h) * S + s0 + key) * D + d0) + f4);
+        tile[4 * f4 + 0][key] = __float2half_rn(x.x);
+        tile[4 * f4 + 1][key] = __float2half_rn(x.y);
+        tile[4 * f4 + 2][key] = __float2half_rn(x.z);
+        tile[4 * f4 + 3][key] = __float2half_rn(x.w);
     }
     __syncthreads();
-    for (int i = threadIdx.y; i < 32; i += 8)
-        vt[(int64_t(h) * D + d0 + i) * Sp + s0 + threadIdx.x] = __float2half_rn(tile[threadIdx.x][i]);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int idx = t + 256 * i;           // 0..511: feature idx / 8, keys 8 (idx % 8) .. +7
+        const int f = idx >> 3, c = idx & 7;
+        *reinterpret_cast<uint4 *>(vt + (int64_t(h) * D + d0 + f) * Sp + s0 + 8 * c) =
+            *reinterpret_cast<const uint4 *>(&tile[f][8 * c]);
+    }
 }
 
 template <int D>
@@ -455,9 +473,9 @@ cudaError_t launch_attention_d(const float *q, const float *k, const float *v, f
     const float qscale = 1.4426950408889634f / sqrtf(float(D));  // log2(e) / sqrt(D)
     const int64_t items = H * Sp * (D / 8);
     const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
-    attn_prep_qk_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(q, qh, int(H), int(S), int(Sp), D, qscale);
-    attn_prep_qk_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(k, kh, int(H), int(S), int(Sp), D, 1.0f);
-    attn_prep_vt_kernel<<<dim3(unsigned(Sp / 32), unsigned(D / 32), unsigned(H)), dim3(32, 8), 0, ctx.stream>>>(
+    attn_prep_qk_kernel<<<dim3(unsigned(pgrid), 2), 256, 0, ctx.stream>>>(q, k, qh, kh, int(H), int(S), int(Sp), D,
+                                                                          qscale);
+    attn_prep_vt_kernel<<<dim3(unsigned(Sp / 64), unsigned(D / 64), unsigned(H)), 256, 0, ctx.stream>>>(
         v, vt, int(S), int(Sp), D);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
