@@ -134,3 +134,55 @@ def test_python_wrapper_raises(tq2):
 def test_wait_timeout_setter_round_trips(tq2):
     old = tq2.tq2_set_wait_timeout_ns(12345)
     assert tq2.tq2_set_wait_timeout_ns(old) == 12345
+
+
+def test_argument_errors_of_the_next_row_entry_points(tq2):
+    # every check below returns before any device work (no GPU needed)
+    A = 1 << 20  # fake, 16-byte aligned, non-overlapping "device" addresses
+    W, X, O, R = A, 64 * A, 128 * A, 192 * A
+    L = tq2.lib
+    # encoder f32 -> blocks
+    assert L.tq2_quantize_f32(X, O, 4, 100, None) == tq2.TQ2_ERR_BAD_K
+    assert L.tq2_quantize_f32(X, O, -1, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert L.tq2_quantize_f32(None, None, 0, 128, None) == tq2.TQ2_OK
+    assert L.tq2_quantize_f32(None, O, 4, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert L.tq2_quantize_f32(X + 4, O, 4, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert L.tq2_quantize_f32(X, X + 16, 4, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    # fused gate/up + SwiGLU
+    f = L.tq2_gate_up_swiglu
+    assert f(W, X, O, 4, 8, 100, None) == tq2.TQ2_ERR_BAD_K
+    assert f(W, X, O, -1, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, O, 4, -8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(None, None, None, 0, 8, 128, None) == tq2.TQ2_OK
+    assert f(None, None, None, 4, 0, 128, None) == tq2.TQ2_OK
+    assert f(None, X, O, 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, O + 4, 4, 8, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert f(W, X, X + 16, 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert f(W, X, W, 4, 8, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    # binary16 activation GEMM and converters
+    g = L.tq2_gemm_act16
+    assert g(W, X, None, O, 4, 32, 100, None) == tq2.TQ2_ERR_BAD_K
+    assert g(W, X, None, O, 4, 40, 128, None) == tq2.TQ2_ERR_INVALID_ARG   # n % 16
+    assert g(None, None, None, None, 0, 32, 128, None) == tq2.TQ2_OK
+    assert g(W, None, None, O, 4, 32, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert g(W, X + 2, None, O, 4, 32, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert g(W, X, R + 2, O, 4, 32, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert g(W, X, None, X + 16, 4, 32, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert g(W, X, O + 16, O, 4, 32, 128, None) == tq2.TQ2_ERR_INVALID_ARG  # partial residual overlap
+    for conv in (L.tq2_act16_from_f32, L.tq2_act16_to_f32):
+        assert conv(X, O, 4, 24, None) == tq2.TQ2_ERR_INVALID_ARG            # k % 16
+        assert conv(X, O, -1, 32, None) == tq2.TQ2_ERR_INVALID_ARG
+        assert conv(None, None, 0, 32, None) == tq2.TQ2_OK
+        assert conv(None, O, 4, 32, None) == tq2.TQ2_ERR_INVALID_ARG
+        assert conv(X + 8, O, 4, 32, None) == tq2.TQ2_ERR_MISALIGNED
+        assert conv(X, X + 16, 4, 32, None) == tq2.TQ2_ERR_INVALID_ARG
+    # DiT joint attention
+    a = L.tq2_attention_f32
+    assert a(X, R, W, O, 2, 128, 96, None) == tq2.TQ2_ERR_INVALID_ARG        # dim not 64 or 128
+    assert a(X, R, W, O, -1, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert a(X, R, W, O, 70000, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG   # heads > 65535
+    assert a(None, None, None, None, 0, 128, 128, None) == tq2.TQ2_OK
+    assert a(None, None, None, None, 2, 0, 128, None) == tq2.TQ2_OK
+    assert a(None, R, W, O, 2, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG
+    assert a(X, R + 4, W, O, 2, 128, 128, None) == tq2.TQ2_ERR_MISALIGNED
+    assert a(X, R, W, X, 2, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG       # out over q
