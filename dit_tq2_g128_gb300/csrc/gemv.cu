@@ -242,11 +242,14 @@ constexpr int kGvWideConsumers = 16;
 // M = 1 decode GEMV (K <= 12288): bulk-copy streaming + integer dot products.
 //
 // Memory side.  One CTA per SM owns a contiguous row range, i.e. a contiguous
-// range of the qs plane.  The producer warp streams it into a shared-memory
-// ring with cp.async.bulk (four rows per stage, with their block scales;
+// range of the qs plane (with swiglu: a feature range, whose gate rows and up
+// rows are two ranges).  The producer warp streams it into a shared-memory
+// ring with cp.async.bulk (RS rows per stage with their block scales, RS in
+// 2..8 chosen per shape so that the stages balance across the consumer groups;
 // completion counted on an mbarrier), so the bytes in flight do not depend on
 // per-thread load slots.  Before waiting for the preceding kernel of the
-// stream it prefetches all of it into L2.
+// stream it prefetches all of it into L2.  x arrives once per CTA by a 2-D
+// tensor copy with the 128-byte swizzle.
 //
 // Arithmetic.  A row is cut into 1024-weight chunks; consumer warp w owns chunk
 // w % C of every row of the stages it takes, and lane l of it the 32 weights
