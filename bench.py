@@ -53,6 +53,10 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="instead of the bench line: every workload configuration (time per call, "
                          "rate, parity on sampled rows against the oracle, oracle time on the sample)")
+    ap.add_argument("--attention", action="store_true",
+                    help="instead of the bench line: the DiT joint attention alone (24 heads x 4096 "
+                         "tokens x 128, seeded N(0,1) inputs), `--steps` calls after `--warmup`, "
+                         "one JSON line with the time per call (for profiling that kernel)")
     return ap.parse_args()
 
 
@@ -405,6 +409,31 @@ def run_ours(args, world, rank, local, pg):
 # --suite: all workload configurations
 
 
+def run_attention_only(args):
+    """The DiT joint attention at the FLUX.2 shape, nothing else (the workload of
+    the attention kernel's ncu summary)."""
+    import torch
+    import dit_tq2_g128_gb300 as tq2
+
+    h, s, d = 24, 4096, 128
+    rng = np.random.default_rng(24)
+    q, k, v = (torch.from_numpy(rng.standard_normal((h, s, d)).astype(np.float32)).cuda() for _ in range(3))
+    out = torch.empty((s, h * d), dtype=torch.float32, device="cuda")
+    for _ in range(args.warmup):
+        tq2.tq2_attention_f32(q, k, v, out, h, s, d)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        tq2.tq2_attention_f32(q, k, v, out, h, s, d)
+    e1.record()
+    torch.cuda.synchronize()
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    t = e0.elapsed_time(e1) / 1e3 / max(args.steps, 1)
+    return {"workload": "dit_joint_attention_h24_s4096_d128", "steps": args.steps, "warmup": args.warmup,
+            "us_per_call": round(t * 1e6, 2), "TFLOPs": round(4.0 * h * s * s * d / t / 1e12, 2)}
+
+
 def run_suite(args, local):
     import torch
     import oracle
@@ -692,6 +721,9 @@ def main():
     args = parse()
     if args.suite:
         print(json.dumps(run_suite(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)
+        return
+    if args.attention:
+        print(json.dumps(run_attention_only(args)), flush=True)
         return
     world, rank, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
