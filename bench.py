@@ -18,6 +18,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import platform
 import os
 import statistics
 import subprocess
@@ -53,6 +54,9 @@ def parse():
     ap.add_argument("--suite", action="store_true",
                     help="instead of the bench line: every workload configuration (time per call, "
                          "rate, parity on sampled rows against the oracle, oracle time on the sample)")
+    ap.add_argument("--cpu-configs", action="store_true",
+                    help="instead of the bench line (no GPU): the CPU oracle on configs 1, 2a, 2b and 3, "
+                         "one whole call each, at one thread and at all threads")
     ap.add_argument("--attention", action="store_true",
                     help="instead of the bench line: the DiT joint attention alone (24 heads x 4096 "
                          "tokens x 128, seeded N(0,1) inputs), `--steps` calls after `--warmup`, "
@@ -690,6 +694,29 @@ def oracle_gemv_rate(p, seconds):
     return calls * wbytes / el / 1e9, calls, el, oracle.threads()
 
 
+def run_cpu_configs():
+    """The CPU oracle (f64 naive loop, OpenMP over output rows) on the small and
+    skinny configurations, one whole call each, at one thread and at all of the
+    host's threads: the reported CPU baseline of those rows."""
+    import oracle
+    probs = [("1 small", tq2_synth.small()), ("2a decode gate/up", tq2_synth.decode_gate_up()),
+             ("2b decode down + residual", tq2_synth.decode_down())]
+    probs += [(f"3 skinny m={m}", tq2_synth.skinny(m)) for m in tq2_synth.SKINNY_MS]
+    full = oracle.threads()
+    oracle.matmul(probs[0][1].w_aos, probs[0][1].x, n=probs[0][1].n, k=probs[0][1].k)  # build + warm
+    rows = []
+    for name, p in probs:
+        rec = {"config": name, "m": p.m, "n": p.n, "k": p.k}
+        for t in (1, full):
+            oracle.set_threads(t)
+            t0 = time.perf_counter()
+            oracle.matmul(p.w_aos, p.x, p.residual, n=p.n, k=p.k)
+            rec[f"seconds_{t}_threads"] = round(time.perf_counter() - t0, 4)
+        rows.append(rec)
+    oracle.set_threads(full)
+    return {"cpu_oracle": rows, "host_threads": full, "cpu": platform.machine()}
+
+
 def run_reference(args, world, rank):
     if rank != 0:
         return None
@@ -724,6 +751,9 @@ def main():
         return
     if args.attention:
         print(json.dumps(run_attention_only(args)), flush=True)
+        return
+    if args.cpu_configs:
+        print(json.dumps(run_cpu_configs()), flush=True)
         return
     world, rank, local, pg = dist_setup(args.gpus)
     if args.impl == "reference":
