@@ -1,13 +1,16 @@
-"""Benchmark of the TQ2_0_g128 ternary matmul library on GB300.
+"""Benchmark of the TQ2_0_g128 ternary matmul library on one GB300.
 
-Default workload (one JSON line on rank 0): the M=1 decode GEMV, K=4096,
-N=12288 (the fused gate/up shape), on seeded synthetic inputs.  One step is
-one tq2_gemv call through the C ABI; K steps are captured in a CUDA graph and
-replayed once inside the timed region, each step reading a different copy of
-the weight so that the copies together exceed twice the L2 size.  `value` is
-the weight bytes streamed per second (all ranks).  The same JSON line also
-carries the large-M GEMM numbers (M=1536, K=3072, N in {3072, 9216, 12288},
-TFLOP/s) measured the same way.
+Default workload (one JSON line): the M=1 decode GEMV, K=4096, N=12288 (the
+fused gate/up shape), on seeded synthetic inputs.  One step is one tq2_gemv
+call through the C ABI; K steps are captured in a CUDA graph, each step
+reading a different copy of the weight so that the copies together exceed
+twice the L2 size, and the graph is replayed several times inside the timed
+region (median and best reported).  `value` is the weight bytes streamed per
+second.  The same JSON line also carries the large-M GEMM numbers (M=1536,
+K=3072, N in {3072, 9216, 12288}, TFLOP/s) measured the same way.
+
+The library runs on one GPU only: a request for more GPUs (--gpus N > 1, or a
+multi-process launch) is refused before anything touches a GPU.
 
 `--impl reference` times the CPU oracle (test infrastructure, double
 precision) on the same workload and metric instead.
@@ -48,6 +51,7 @@ def parse():
     ap.add_argument("--no-gemm", action="store_true", help="skip the large-M GEMM section")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--gemm-steps", type=int, default=20)
+    ap.add_argument("--replays", type=int, default=7, help="timed replays of the GEMV graph (at least 5)")
     ap.add_argument("--gemm-n", type=int, default=0, help="only this N of the large-M set")
     ap.add_argument("--no-clock-window", action="store_true",
                     help="skip the 1 s sustained window that feeds the clock record")
@@ -77,40 +81,14 @@ def peaks():
         return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
 
 
-def dist_setup(gpus):
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-        import torch
-        backend = "nccl" if torch.cuda.is_available() else "gloo"
-        if backend == "nccl":
-            torch.cuda.set_device(local)
-        dist.init_process_group(backend=backend)
-        pg = dist
-    return world, rank, local, pg
+def world_from_env():
+    """(world size, rank) of a torchrun launch, (1, 0) otherwise."""
+    return int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0"))
 
 
-def max_over_ranks(value, pg, device):
-    if pg is None:
-        return value
-    import torch
-    t = torch.tensor([value], dtype=torch.float64, device=device)
-    pg.all_reduce(t, op=pg.ReduceOp.MAX)
-    return float(t.item())
-
-
-def barrier(pg):
-    if pg is not None:
-        pg.barrier()
-
-
-def whole_job_rate(world, units_per_rank, seconds):
-    """Units per second of the whole job: every rank processes `units_per_rank`
-    independent units (weak scaling) and `seconds` is the max over ranks."""
-    return world * units_per_rank / seconds
+SINGLE_GPU_ONLY = ("bench.py runs on one GPU only: the tensor-core kernels copy shared x tiles "
+                   "between the two CTAs of a cluster (cluster multicast), which is offered for "
+                   "single-GPU calls only, so no multi-GPU run of this library is provided")
 
 
 class ClockSampler:
@@ -211,11 +189,10 @@ def graph_of(fn, steps, torch):
     return g
 
 
-def time_graph(g, torch, pg, device, reps=1):
-    """Device time (s) of one replay, CUDA events on the replay stream, max over ranks."""
-    best = []
+def time_graph(g, torch, reps=1):
+    """Device times (s) of `reps` replays, CUDA events on the replay stream."""
+    ts = []
     for _ in range(reps):
-        barrier(pg)
         torch.cuda.synchronize()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
@@ -223,25 +200,29 @@ def time_graph(g, torch, pg, device, reps=1):
         g.replay()
         e1.record()
         torch.cuda.synchronize()
-        barrier(pg)
-        best.append(e0.elapsed_time(e1) / 1e3)
-    t = statistics.median(best)
-    return max_over_ranks(t, pg, device)
+        ts.append(e0.elapsed_time(e1) / 1e3)
+    return ts
 
 
-def run_ours(args, world, rank, local, pg):
+GEMV_CONFIG = {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288,
+               "weight_bytes": 13369344,
+               "l2": "inputs larger than L2: rotating weight copies, together more than twice the L2 size"}
+
+
+def run_ours(args):
     import torch
     import dit_tq2_g128_gb300 as tq2
 
-    device = torch.device("cuda", local)
+    device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     hbm, bf16, bf16s, peak_src = peaks()
     props = torch.cuda.get_device_properties(device)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2 ** 20))
 
-    # ---- decode GEMV workload (per rank an independent problem: weak scaling)
-    p = tq2_synth.decode_gate_up(seed=rank)
+    # ---- decode GEMV workload
+    p = tq2_synth.decode_gate_up(seed=0)
     wbytes = tq2.tq2_soa_bytes(p.n, p.k)
+    assert wbytes == GEMV_CONFIG["weight_bytes"]
     copies = max(2, -(-2 * l2 // wbytes) + 1)
     w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
     ws = [w0] + [w0.clone() for _ in range(copies - 1)]
@@ -259,21 +240,23 @@ def run_ours(args, world, rank, local, pg):
     gt = graph_of(step, args.steps, torch)
     gw.replay()
     torch.cuda.synchronize()
-    smi_id = str(local)
+    smi_id = "0"
     try:  # nvidia-smi numbers GPUs physically; the CUDA ordinal may differ
         smi_id = "GPU-" + str(props.uuid)
     except Exception:
         pass
+    reps = max(5, args.replays)
     with ClockSampler(smi_id) as clk:
         # sustained window for the clock record (same graph, >= 1 s of load)
         t_end = time.time() + (0.0 if args.no_clock_window else 1.0)
         while time.time() < t_end:
             gt.replay()
             torch.cuda.synchronize()
-        t_step = time_graph(gt, torch, pg, device, reps=1)
+        t_reps = time_graph(gt, torch, reps=reps)
     clocks = clk.summary()
+    t_step = statistics.median(t_reps)
     per_launch = t_step / args.steps
-    value = whole_job_rate(world, wbytes * args.steps, t_step) / 1e9
+    value = wbytes * args.steps / t_step / 1e9
     achieved = wbytes / per_launch / 1e9
 
     # ---- end to end through the C ABI with host buffers
@@ -290,7 +273,6 @@ def run_ours(args, world, rank, local, pg):
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
-    barrier(pg)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
@@ -298,9 +280,8 @@ def run_ours(args, world, rank, local, pg):
         e2e_step(i)
     e1.record(stream)
     torch.cuda.synchronize()
-    barrier(pg)
-    t_e2e = max_over_ranks(e0.elapsed_time(e1) / 1e3, pg, device)
-    e2e = {"value": whole_job_rate(world, wbytes * args.steps, t_e2e) / 1e9, "unit": "GB/s",
+    t_e2e = e0.elapsed_time(e1) / 1e3
+    e2e = {"value": wbytes * args.steps / t_e2e / 1e9, "unit": "GB/s",
            "h2d_bytes_per_step": int(x_host.numel() * 4), "d2h_bytes_per_step": int(out_host.numel() * 4),
            "note": "weights resident (uploaded once); x up and out down every step, pinned host buffers"}
 
@@ -309,7 +290,7 @@ def run_ours(args, world, rank, local, pg):
         "metric": METRIC,
         "value": round(value, 2),
         "unit": "GB/s (TQ2 weight bytes, M=1 GEMV)",
-        "n_gpus": world,
+        "n_gpus": 1,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(t_step / args.steps * 1e3, 6),
@@ -318,12 +299,17 @@ def run_ours(args, world, rank, local, pg):
         "vs_baseline": None,
         "dtype": "f32 in/out; x as 23-bit fixed point per 32-weight slice, int32 (dp4a) ternary dot products, f32 scale and sum",
         "data": "synthetic (seeded numpy: x~N(0,1), codes P(0)=0.4 P(+-1)=0.3, d=f16(|N(0,0.02)|+1e-4))",
-        "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288,
-                   "weight_bytes": wbytes, "kernel": "tq2_gemv",
-                   "l2": f"inputs larger than L2: {copies} rotating weight copies "
-                         f"({copies * wbytes / 2**20:.0f} MiB > 2x L2 {l2 / 2**20:.0f} MiB)",
-                   "timing": "K steps captured in one CUDA graph, one replay timed with CUDA events",
-                   "parallelism": f"replicas x{world} (independent problems per GPU)"},
+        "config": dict(GEMV_CONFIG),
+        "timing": {"entry": "tq2_gemv",
+                   "method": f"{args.steps} calls captured in one CUDA graph on {copies} rotating weight "
+                             f"copies ({copies * wbytes / 2**20:.0f} MiB, L2 {l2 / 2**20:.0f} MiB); "
+                             f"{reps} replays timed with CUDA events on the replay stream; value from the median",
+                   "us_per_call_median": round(t_step / args.steps * 1e6, 4),
+                   "us_per_call_best": round(min(t_reps) / args.steps * 1e6, 4),
+                   "us_per_call_replays": [round(t / args.steps * 1e6, 4) for t in t_reps],
+                   "sm_mhz_median": clocks.get("sm_mhz"),
+                   "note": "consecutive calls overlap through programmatic dependent launch: each call's "
+                           "launch and L2 prefetch of its weights run during the previous call"},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": hbm, "unit": "GB/s",
                      "frac": round(achieved / hbm, 4), "peak_source": f"{peak_src} (copy bandwidth)",
                      "traffic": ncu_traffic("gemv_m1_k4096_n12288", gemv_src),
@@ -331,7 +317,7 @@ def run_ours(args, world, rank, local, pg):
                      "note": "achieved = weight bytes / (graph time / launches); includes inter-kernel gaps"},
         "clocks": clocks,
         "e2e": e2e,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * reps,
         "impl": "ours",
     }
 
@@ -342,7 +328,7 @@ def run_ours(args, world, rank, local, pg):
         for n in tq2_synth.DIT_NS:
             if args.gemm_n and n != args.gemm_n:
                 continue
-            q = tq2_synth.dit(n, seed=rank)
+            q = tq2_synth.dit(n, seed=0)
             per = q.m * q.k * 4 + tq2.tq2_soa_bytes(q.n, q.k) + q.m * q.n * 4
             c = max(2, -(-2 * l2 // per) + 1)
             wq = tq2.upload_weight(q.w_aos, q.n, q.k)
@@ -374,8 +360,8 @@ def run_ours(args, world, rank, local, pg):
                 gg = graph_of(fn, args.gemm_steps, torch)
                 gg.replay()
                 torch.cuda.synchronize()
-                tg = time_graph(gg, torch, pg, device, reps=3) / args.gemm_steps
-                launches += args.gemm_steps * kernels_per_call[name]
+                tg = statistics.median(time_graph(gg, torch, reps=3)) / args.gemm_steps
+                launches += 3 * args.gemm_steps * kernels_per_call[name]
                 res[name] = (tg, flops / tg / 1e12)
             tg, tfl = res["tq2_gemm"]
             gemm[f"n{n}"] = {"m": q.m, "k": q.k, "n": q.n, "entry": "tq2_gemm",
@@ -438,12 +424,12 @@ def run_attention_only(args):
             "us_per_call": round(t * 1e6, 2), "TFLOPs": round(4.0 * h * s * s * d / t / 1e12, 2)}
 
 
-def run_suite(args, local):
+def run_suite(args):
     import torch
     import oracle
     import dit_tq2_g128_gb300 as tq2
 
-    device = torch.device("cuda", local)
+    device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 126 * 2 ** 20))
     rows_out = []
@@ -717,9 +703,8 @@ def run_cpu_configs():
     return {"cpu_oracle": rows, "host_threads": full, "cpu": platform.machine()}
 
 
-def run_reference(args, world, rank):
-    if rank != 0:
-        return None
+def run_reference(args):
+    """The reference arm: the CPU oracle on the decode GEMV workload, whole calls."""
     import oracle
     p = tq2_synth.decode_gate_up()
     wbytes = p.w_aos.size
@@ -733,10 +718,10 @@ def run_reference(args, world, rank):
     cores = oracle.threads()
     return {
         "metric": METRIC, "value": round(v, 4), "unit": "GB/s (TQ2 weight bytes, M=1 GEMV)",
-        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(el / args.steps * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic (same seeded workload)",
-        "config": {"workload": "decode_gemv_m1_k4096_n12288", "m": 1, "k": 4096, "n": 12288},
+        "config": dict(GEMV_CONFIG),
         "impl": "reference",
         "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.steps} full GEMV calls (12288x4096), double precision"},
@@ -746,8 +731,19 @@ def run_reference(args, world, rank):
 
 def main():
     args = parse()
+    world, rank = world_from_env()
+    if args.impl == "reference":
+        # the oracle runs on the host: under a multi-process launch rank 0
+        # alone runs and prints it, the other ranks leave without work
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1 or args.gpus != 1:
+        # refused before anything touches a GPU
+        sys.stderr.write(SINGLE_GPU_ONLY + f" (asked for --gpus {args.gpus}, WORLD_SIZE {world})\n")
+        sys.exit(2)
     if args.suite:
-        print(json.dumps(run_suite(args, int(os.environ.get("LOCAL_RANK", "0")))), flush=True)
+        print(json.dumps(run_suite(args)), flush=True)
         return
     if args.attention:
         print(json.dumps(run_attention_only(args)), flush=True)
@@ -755,24 +751,15 @@ def main():
     if args.cpu_configs:
         print(json.dumps(run_cpu_configs()), flush=True)
         return
-    world, rank, local, pg = dist_setup(args.gpus)
-    if args.impl == "reference":
-        line = run_reference(args, world, rank)
-        if line is not None:
-            print(json.dumps(line), flush=True)
-        return
-    line = run_ours(args, world, rank, local, pg)
-    if rank == 0:
-        if not args.no_cpu and world == 1:
-            p = tq2_synth.decode_gate_up()
-            v, calls, el, cores = oracle_gemv_rate(p, 10.0)
-            line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
-                                    "kind": "oracle",
-                                    "sample": f"{calls} full decode GEMV calls in {el:.1f} s "
-                                              "(double precision, OpenMP over output rows)"}
-        print(json.dumps(line), flush=True)
-    if pg is not None:
-        pg.destroy_process_group()
+    line = run_ours(args)
+    if not args.no_cpu:
+        p = tq2_synth.decode_gate_up()
+        v, calls, el, cores = oracle_gemv_rate(p, 10.0)
+        line["cpu_baseline"] = {"value": round(v, 4), "unit": "GB/s", "cores": cores,
+                                "kind": "oracle",
+                                "sample": f"{calls} full decode GEMV calls in {el:.1f} s "
+                                          "(double precision, OpenMP over output rows)"}
+    print(json.dumps(line), flush=True)
 
 
 if __name__ == "__main__":

@@ -6,6 +6,7 @@
 // K a multiple of 128.  Unlike the page, every failure is a returned status
 // and there is no CPU fallback.
 #include <atomic>
+#include <initializer_list>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -60,6 +61,29 @@ int current_device(DeviceInfo *out) {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Every operand a kernel reads or writes (through plain accesses, tensor maps,
+// bulk copies or the tensor kernels' cluster-multicast copies) must be device
+// memory of the current device: host memory, managed memory and another
+// GPU's memory (peer or imported mappings) are refused before any launch.
+// NULL pointers pass (the callers check them where they are required).
+bool on_current_device(const void *p, int dev) {
+    if (!p) return true;
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();  // not a pointer the runtime knows: not device memory
+        return false;
+    }
+    return a.type == cudaMemoryTypeDevice && a.device == dev;
+}
+
+int check_local(std::initializer_list<const void *> ptrs) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TQ2_ERR_CUDA;
+    for (const void *p : ptrs)
+        if (!on_current_device(p, dev)) return TQ2_ERR_INVALID_ARG;
+    return TQ2_OK;
+}
+
 bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
     uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
     return na && nb && x < y + nb && y < x + na;
@@ -103,6 +127,14 @@ int make_ctx(cudaStream_t stream, tq2::LaunchCtx *ctx) {
     ctx->wait_ns = g_wait_ns.load(std::memory_order_relaxed);
     ctx->num_sms = d.num_sms;
     return TQ2_OK;
+}
+
+// Launch context for the current device, then the residency check of every
+// operand the call's kernels touch (see on_current_device).
+int prepare(void *stream, tq2::LaunchCtx *ctx, std::initializer_list<const void *> ptrs) {
+    int st = make_ctx(static_cast<cudaStream_t>(stream), ctx);
+    if (st != TQ2_OK) return st;
+    return check_local(ptrs);
 }
 
 int finish(cudaError_t e) { return e == cudaSuccess ? TQ2_OK : TQ2_ERR_CUDA; }
@@ -165,7 +197,7 @@ int tq2_reformat_aos_to_soa(const void *w_aos, void *w_soa, int64_t n, int64_t k
     if (!aligned16(w_soa)) return TQ2_ERR_MISALIGNED;
     if (overlaps(w_aos, tq2_soa_bytes(n, k), w_soa, tq2_soa_bytes(n, k))) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    int st = prepare(stream, &ctx, {w_aos, w_soa});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_reformat(w_aos, w_soa, n, k, ctx));
 }
@@ -178,7 +210,7 @@ int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *st
     if (!aligned16(w) || !aligned16(w_aos)) return TQ2_ERR_MISALIGNED;
     if (overlaps(w, size_t(n) * size_t(k) * 4, w_aos, tq2_soa_bytes(n, k))) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    int st = prepare(stream, &ctx, {w, w_aos});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_quantize(w, w_aos, n, k, ctx));
 }
@@ -193,7 +225,7 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
     if (kernel == TQ2_KERNEL_SKINNY && m > tq2::kSkinnyMaxM) return TQ2_ERR_INVALID_ARG;
     if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_TC_DIRECT) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    st = prepare(stream, &ctx, {w_soa, x, residual, out});
     if (st != TQ2_OK) return st;
     switch (kernel) {
         case TQ2_KERNEL_GEMV: return finish(tq2::launch_gemv(w_soa, x, residual, out, n, k, ctx));
@@ -201,15 +233,14 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
             return finish(tq2::launch_skinny(w_soa, x, residual, out, m, n, k, ctx));
         case TQ2_KERNEL_TC: {
             // x -> f16 tiles in a stream-ordered temporary, then the clustered
-            // kernel; without the temporary, the kernel that converts x itself
+            // kernel.  A failed allocation is reported (TQ2_ERR_CUDA, the
+            // CUDA error left for the caller), never replaced by another kernel.
             void *ws = nullptr;
-            if (cudaMallocAsync(&ws, tq2::tc_ws_bytes(m, n, k), ctx.stream) == cudaSuccess) {
-                const cudaError_t e = tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, ws, ctx);
-                const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
-                return finish(e != cudaSuccess ? e : f);
-            }
-            (void)cudaGetLastError();  // the failed allocation is not an error of the call
-            return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
+            if (cudaMallocAsync(&ws, tq2::tc_ws_bytes(m, n, k), ctx.stream) != cudaSuccess)
+                return TQ2_ERR_CUDA;
+            const cudaError_t e = tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, ws, ctx);
+            const cudaError_t f = cudaFreeAsync(ws, ctx.stream);
+            return finish(e != cudaSuccess ? e : f);
         }
         case TQ2_KERNEL_TC_DIRECT:
             return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
@@ -240,7 +271,7 @@ int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float 
         overlaps(workspace, need, out, ob) || (residual && overlaps(workspace, need, residual, ob)))
         return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    st = prepare(stream, &ctx, {w_soa, x, residual, out, workspace});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_tc_ws(w_soa, x, residual, out, m, n, k, workspace, ctx));
 }
@@ -252,9 +283,12 @@ int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, f
     if (st != TQ2_OK || noop) return st;
     if (tq2_select_kernel(m, n, k) != TQ2_KERNEL_TC)  // these kernels use no scratch
         return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
+    // the one place that checks the shape against the fixed scratch; it comes
+    // before the device is looked up (a host-only decision, like the other
+    // argument checks)
     if (tq2::tc_ws_bytes(m, n, k) > tq2::kNoAllocScratchBytes) return TQ2_ERR_TOO_LARGE;
     tq2::LaunchCtx ctx;
-    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    st = prepare(stream, &ctx, {w_soa, x, residual, out});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_tc_noalloc(w_soa, x, residual, out, m, n, k, ctx));
 }
@@ -277,7 +311,7 @@ int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m,
     const size_t xb = size_t(m) * size_t(k) * 4, ob = size_t(m) * size_t(f) * 4;
     if (overlaps(out, ob, x, xb) || overlaps(out, ob, w_soa, wb)) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    st = prepare(stream, &ctx, {w_soa, x, out});
     if (st != TQ2_OK) return st;
     cudaError_t e = cudaErrorNotSupported;
     if (m == 1) {
@@ -314,7 +348,7 @@ int tq2_act16_from_f32(const float *x, void *x16, int64_t m, int64_t k, void *st
     if (!aligned16(x) || !aligned16(x16)) return TQ2_ERR_MISALIGNED;
     if (overlaps(x, size_t(m) * size_t(k) * 4, x16, size_t(m) * size_t(k) * 2)) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    int st = prepare(stream, &ctx, {x, x16});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_act16_from_f32(x, static_cast<__half *>(x16), m, k, ctx));
 }
@@ -326,7 +360,7 @@ int tq2_act16_to_f32(const void *x16, float *x, int64_t m, int64_t k, void *stre
     if (!aligned16(x) || !aligned16(x16)) return TQ2_ERR_MISALIGNED;
     if (overlaps(x, size_t(m) * size_t(k) * 4, x16, size_t(m) * size_t(k) * 2)) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    int st = prepare(stream, &ctx, {x16, x});
     if (st != TQ2_OK) return st;
     return finish(tq2::launch_act16_to_f32(static_cast<const __half *>(x16), x, m, k, ctx));
 }
@@ -345,7 +379,7 @@ int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, v
     if (overlaps(out16, ob, x16, xb) || overlaps(out16, ob, w_soa, wb)) return TQ2_ERR_INVALID_ARG;
     if (residual16 && residual16 != out16 && overlaps(out16, ob, residual16, ob)) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    st = prepare(stream, &ctx, {w_soa, x16, residual16, out16});
     if (st != TQ2_OK) return st;
     const size_t need = tq2::tc_act16_ws_bytes(m, n, k);
     void *ws = nullptr;
@@ -375,7 +409,7 @@ int tq2_attention_f32(const float *q, const float *k, const float *v, float *out
     if (overlaps(out, nb, q, nb) || overlaps(out, nb, k, nb) || overlaps(out, nb, v, nb))
         return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
-    int st = make_ctx(static_cast<cudaStream_t>(stream), &ctx);
+    int st = prepare(stream, &ctx, {q, k, v, out});
     if (st != TQ2_OK) return st;
     void *ws = nullptr;
     if (cudaMallocAsync(&ws, tq2::attention_ws_bytes(heads, seq, dim), ctx.stream) != cudaSuccess) {

@@ -808,7 +808,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes]
 
 cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *residual, float *out,
                               int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx) {
-    if (tc_ws_bytes(m, n, k) > kNoAllocScratchBytes) return cudaErrorInvalidValue;
+    // (the API layer has checked the shape against the scratch size)
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -829,16 +829,23 @@ cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *re
     return launch_tc_ws(w_soa, x, residual, out, m, n, k, scratch, ctx);
 }
 
-// K slices per output tile pair: enough work items for the 76 CTA pairs of a
-// 152-SM GB300 when the shape has fewer tile pairs, at least 4 stages each.
-// A function of the shape only (the workspace size must not depend on the device).
-int tc_ksplit(int64_t m, int64_t n, int64_t k) {
-    const int64_t pairs = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2);
-    int64_t s = pairs < 76 ? 76 / pairs : 1;
+// K slices per output tile pair when `pairs` CTA pairs are available: enough
+// work items for all of them when the shape has fewer tile pairs, at least 4
+// stages per slice, at most 16 slices.
+static int ksplit_for(int64_t m, int64_t n, int64_t k, int64_t pairs) {
+    const int64_t tiles = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2);
+    int64_t s = tiles < pairs ? pairs / tiles : 1;
     s = std::min<int64_t>(s, (k / BK) / 4);
     s = std::min<int64_t>(s, 16);
     return int(std::max<int64_t>(s, 1));
 }
+
+// The split the workspace is sized for: a function of the shape only (callers
+// size workspaces without a device), computed for the 76 CTA pairs of a
+// 152-SM GB300.  A launch uses the split of the device it runs on, capped by
+// this one (what the workspace holds).
+constexpr int64_t kWsPairs = 76;
+int tc_ksplit(int64_t m, int64_t n, int64_t k) { return ksplit_for(m, n, k, kWsPairs); }
 
 static size_t x_tile_bytes(int64_t m, int64_t k) {
     const int64_t mt = (m + BM - 1) / BM;
@@ -954,7 +961,8 @@ cudaError_t launch_tc_ws_mode(const void *w_soa, const TcIo &io, int64_t m, int6
     if (e != cudaSuccess) return e;
     // clusters of two CTAs, each cluster a pair of neighbouring weight tiles
     // (times the K slices of a split problem)
-    const int ksplit = swiglu ? 1 : tc_ksplit(m, n, k);
+    const int ksplit =
+        swiglu ? 1 : std::min(tc_ksplit(m, n, k), ksplit_for(m, n, k, std::max(1, ctx.num_sms / 2)));
     float *partial = nullptr;
     if (ksplit > 1)
         partial = act16 ? static_cast<float *>(ws)

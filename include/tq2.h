@@ -32,9 +32,20 @@
  * The total size equals the AoS size, tq2_soa_bytes(n, k) = N*(K/128)*34.
  *
  * Conventions shared by every entry point below:
- *  - Pointers are DEVICE pointers owned by the caller; the library allocates
- *    nothing, frees nothing and keeps no cache of weights (the pages' pointer-
- *    keyed upload cache is the caller's job here).
+ *  - Pointers are DEVICE pointers of the current device, owned by the caller.
+ *    Before any launch every operand is checked (cudaPointerGetAttributes):
+ *    memory that is not device memory of the current device (pageable or
+ *    pinned host memory, managed memory, another GPU's memory reached through
+ *    a peer or imported mapping) gives TQ2_ERR_INVALID_ARG.  Every call runs
+ *    on one GPU.
+ *  - Memory: the library keeps no cache of weights (the pages' pointer-keyed
+ *    upload cache is the caller's job here) and frees only what it took.  The
+ *    entry points whose doc has a "Memory:" paragraph take a temporary from
+ *    the device's default stream-ordered pool (cudaMallocAsync, released by
+ *    cudaFreeAsync on the same stream; both are legal inside stream capture)
+ *    and return TQ2_ERR_CUDA if it cannot be had; all others allocate nothing
+ *    (tq2_gemm_ws and tq2_gemm_noalloc are the allocation-free forms of the
+ *    tensor-core path).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
  *    is asynchronous on it and never synchronises the host.
  *  - Errors are returned as a tq2_status; nothing aborts and there is no CPU
@@ -150,10 +161,11 @@ int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *ou
  * exact f32 products and f32 accumulation.
  * Memory: on the tensor-core path the call takes a temporary of
  * tq2_gemm_workspace_bytes(m,n,k) bytes from the device's default memory pool,
- * ordered on `stream` (cudaMallocAsync, released by cudaFreeAsync on the same
- * stream; both are legal inside stream capture).  If that allocation fails it
- * runs TQ2_KERNEL_TC_DIRECT instead, which needs no temporary.  Callers that
- * manage memory themselves use tq2_gemm_ws or tq2_gemm_noalloc. */
+ * ordered on `stream`; if it cannot be had the call returns TQ2_ERR_CUDA
+ * without launching anything (no silent change of kernel).  Callers that
+ * manage memory themselves use tq2_gemm_ws or tq2_gemm_noalloc, or
+ * tq2_gemm_with(TQ2_KERNEL_TC_DIRECT), which converts x inside the kernel and
+ * needs no temporary (about half the speed). */
 int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t m, int64_t n, int64_t k, void *stream);
 
@@ -284,7 +296,9 @@ int tq2_gemm_ws(const void *w_soa, const float *x, const float *residual, float 
  * the same results.  Other shapes use no scratch and behave like tq2_gemm.
  *   - Limit: shapes with tq2_gemm_workspace_bytes(m,n,k) >
  *     TQ2_NOALLOC_SCRATCH_BYTES return TQ2_ERR_TOO_LARGE before any work
- *     (e.g. m = 4096 with k up to 4096 fits; k = 12288 does not).
+ *     (e.g. m = 4096 with k up to 4096 fits; k = 12288 does not).  Like the
+ *     other argument checks this is decided on the host before the device is
+ *     looked up, so it precedes TQ2_ERR_UNSUPPORTED_DEVICE.
  *   - It calls no cudaMalloc, cudaFree or other allocating routine.
  *   - The first call on a device looks up the scratch array's device address
  *     (one-time set-up, with that device current); make that first call before

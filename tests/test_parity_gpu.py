@@ -251,15 +251,6 @@ def test_skinny_sweep_tc(tq2, m):
     check(run(tq2, tq2.TQ2_KERNEL_TC, w, p), p, TOL_TC, cos=True, what=f"tc m={m}")
 
 
-@pytest.mark.parametrize("n", tq2_synth.DIT_NS)
-def test_dit_large_m_tc(tq2, n):
-    p = tq2_synth.dit(n)
-    w = upload(tq2, p)
-    out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
-    assert tq2.tq2_select_kernel(p.m, p.n, p.k) == tq2.TQ2_KERNEL_TC
-    check(out, p, TOL_TC, rows=sample_rows(p.m), cos=True, what=f"dit n={n}")
-
-
 def test_dit_large_m_tc_direct(tq2):
     p = tq2_synth.dit(3072)
     w = upload(tq2, p)
@@ -272,15 +263,6 @@ def test_dit_large_m_f32ref(tq2):
     w = upload(tq2, p)
     check(run(tq2, tq2.TQ2_KERNEL_F32REF, w, p), p, TOL_F32, rows=sample_rows(p.m, extra=6),
           what="f32ref dit")
-
-
-@pytest.mark.parametrize("layer", [0, 1, 40, 41, 60, 61, 80, 81])
-def test_dit_forward_layers(tq2, layer):
-    p = tq2_synth.dit_forward_layer(layer)
-    w = upload(tq2, p)
-    out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
-    check(out, p, TOL_TC, rows=sample_rows(p.m, extra=4, seed=layer), cos=True,
-          what=f"dit forward layer {layer}")
 
 
 # ---------------------------------------------------------------------------

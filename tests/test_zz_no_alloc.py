@@ -1,6 +1,8 @@
 """tq2_gemm_noalloc: the entry point for callers that cannot allocate device
 memory.  It must give the same results as tq2_gemm_ws (which takes a
-caller-provided workspace) without allocating anything, call after call.
+caller-provided workspace) without allocating anything, call after call: the
+test also watches torch's allocator and the device's stream-ordered memory
+pool around each call.
 
 This file is collected last on purpose: if it fails, a run that stops at the
 first failure has already run every other test.  It passes on its own in a
@@ -36,6 +38,37 @@ def test_noalloc_rejects_oversize_before_any_work(tq2):
     assert tq2.lib.tq2_gemm_noalloc(A, 2 * A, None, 3 * A, 8, 8, 100, None) == tq2.TQ2_ERR_BAD_K
 
 
+def _default_pool_usage():
+    """(reserved bytes, used high-water mark) of the device's default
+    stream-ordered memory pool, the one cudaMallocAsync draws from, with the
+    high-water mark reset to zero first; None where the CUDA runtime library
+    cannot be loaded by path."""
+    import os
+    for path in ("/usr/local/cuda/lib64/libcudart.so", "libcudart.so.13", "libcudart.so"):
+        try:
+            rt = ctypes.CDLL(path)
+            break
+        except OSError:
+            rt = None
+    if rt is None:
+        return None
+    pool = ctypes.c_void_p()
+    if rt.cudaDeviceGetDefaultMemPool(ctypes.byref(pool), 0) != 0:
+        return None
+    reserved_current, used_high = 5, 8  # cudaMemPoolAttr enumerators
+    val = ctypes.c_uint64(0)
+    rt.cudaMemPoolGetAttribute(pool, reserved_current, ctypes.byref(val))
+    reserved = val.value
+    rt.cudaMemPoolGetAttribute(pool, used_high, ctypes.byref(val))
+    return rt, pool, reserved, val.value
+
+
+def _reset_pool_high(state):
+    rt, pool = state[0], state[1]
+    zero = ctypes.c_uint64(0)
+    rt.cudaMemPoolSetAttribute(pool, 8, ctypes.byref(zero))
+
+
 @pytest.mark.gpu
 def test_noalloc_matches_workspace_entry_point_twice(tq2):
     torch = pytest.importorskip("torch")
@@ -57,11 +90,24 @@ def test_noalloc_matches_workspace_entry_point_twice(tq2):
         ws = tq2.workspace(p.m, p.n, p.k)
         tq2.tq2_gemm_ws(w, x, r, want, p.m, p.n, p.k, ws, ws.numel())
         got = torch.full((p.m, p.n), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        # nothing may be allocated by the call: neither through torch's
+        # allocator nor from the stream-ordered pool (used high-water mark
+        # reset to zero just before)
+        pool = _default_pool_usage()
+        if pool is not None:
+            _reset_pool_high(pool)
+        torch_before = (torch.cuda.memory_allocated(), torch.cuda.memory_reserved())
         rc = tq2.lib.tq2_gemm_noalloc(w.data_ptr(), x.data_ptr(),
                                       None if r is None else r.data_ptr(), got.data_ptr(),
                                       p.m, p.n, p.k, ctypes.c_void_p(stream))
         assert rc == tq2.TQ2_OK, tq2.status_string(rc)
         torch.cuda.synchronize()
+        assert (torch.cuda.memory_allocated(), torch.cuda.memory_reserved()) == torch_before
+        if pool is not None:
+            after = _default_pool_usage()
+            assert after[3] == 0, "the call drew memory from the stream-ordered pool"
+            assert after[2] == pool[2]
         assert tq2.tq2_device_status() == tq2.TQ2_OK
         g = got.cpu().numpy().astype(np.float64)
         e = want.cpu().numpy().astype(np.float64)
