@@ -61,6 +61,9 @@ def parse():
     ap.add_argument("--cpu-configs", action="store_true",
                     help="instead of the bench line (no GPU): the CPU oracle on configs 1, 2a, 2b and 3, "
                          "one whole call each, at one thread and at all threads")
+    ap.add_argument("--cpu-full", action="store_true",
+                    help="instead of the bench line (no GPU): the CPU oracle on the DiT configurations in "
+                         "full (M=1536 at each N, then the 100-layer forward set at M=4096), all host threads")
     ap.add_argument("--attention", action="store_true",
                     help="instead of the bench line: the DiT joint attention alone (24 heads x 4096 "
                          "tokens x 128, seeded N(0,1) inputs), `--steps` calls after `--warmup`, "
@@ -297,7 +300,7 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f32 in/out; x as 23-bit fixed point per 32-weight slice, int32 (dp4a) ternary dot products, f32 scale and sum",
+        "dtype": "f32 in/out; x as 23-bit fixed point per 128-weight block, int32 (dp4a) ternary dot products, f32 scale and sum",
         "data": "synthetic (seeded numpy: x~N(0,1), codes P(0)=0.4 P(+-1)=0.3, d=f16(|N(0,0.02)|+1e-4))",
         "config": dict(GEMV_CONFIG),
         "timing": {"entry": "tq2_gemv",
@@ -703,6 +706,38 @@ def run_cpu_configs():
     return {"cpu_oracle": rows, "host_threads": full, "cpu": platform.machine()}
 
 
+def run_cpu_full():
+    """The CPU oracle (f64 naive loop, OpenMP over output rows) on the DiT
+    configurations in full, every output element: M=1536 at each N, then the
+    100 layers of the forward set at M=4096 one after another.  Input
+    generation is outside the timed calls."""
+    import oracle
+    full = oracle.threads()
+    p0 = tq2_synth.small()
+    oracle.matmul(p0.w_aos, p0.x, n=p0.n, k=p0.k)  # build + warm
+    rows = []
+    for n in tq2_synth.DIT_NS:
+        p = tq2_synth.dit(n)
+        t0 = time.perf_counter()
+        oracle.matmul(p.w_aos, p.x, p.residual, n=p.n, k=p.k)
+        el = time.perf_counter() - t0
+        rows.append({"config": f"4 dit m=1536 n={n}", "seconds": round(el, 3),
+                     "GFLOP": round(2.0 * p.m * p.n * p.k / 1e9, 1), "GFLOPs": round(2.0 * p.m * p.n * p.k / el / 1e9, 2)})
+        print(json.dumps(rows[-1]), flush=True)
+    tot, flops, per = 0.0, 0.0, []
+    for li in range(len(tq2_synth.DIT_FORWARD_SHAPES)):
+        p = tq2_synth.dit_forward_layer(li)
+        t0 = time.perf_counter()
+        oracle.matmul(p.w_aos, p.x, p.residual, n=p.n, k=p.k)
+        el = time.perf_counter() - t0
+        tot += el
+        flops += 2.0 * p.m * p.n * p.k
+        per.append(round(el, 2))
+    rows.append({"config": "5 dit forward, 100 layers at M=4096 (every element)", "seconds": round(tot, 1),
+                 "TFLOP": round(flops / 1e12, 2), "GFLOPs": round(flops / tot / 1e9, 2), "per_layer_s": per})
+    return {"cpu_oracle_full": rows, "host_threads": full, "cpu": platform.machine()}
+
+
 def run_reference(args):
     """The reference arm: the CPU oracle on the decode GEMV workload, whole calls."""
     import oracle
@@ -750,6 +785,9 @@ def main():
         return
     if args.cpu_configs:
         print(json.dumps(run_cpu_configs()), flush=True)
+        return
+    if args.cpu_full:
+        print(json.dumps(run_cpu_full()), flush=True)
         return
     line = run_ours(args)
     if not args.no_cpu:

@@ -37,7 +37,8 @@ TQ2_KERNEL_SKINNY = 2
 TQ2_KERNEL_TC = 3
 TQ2_KERNEL_F32REF = 4
 TQ2_KERNEL_TC_DIRECT = 5
-KERNEL_NAMES = {0: "auto", 1: "gemv", 2: "skinny", 3: "tc", 4: "f32ref", 5: "tc_direct"}
+TQ2_KERNEL_SKINNY_MMA = 6
+KERNEL_NAMES = {0: "auto", 1: "gemv", 2: "skinny", 3: "tc", 4: "f32ref", 5: "tc_direct", 6: "skinny_mma"}
 
 # Every symbol include/tq2.h declares.
 EXPORTS = (

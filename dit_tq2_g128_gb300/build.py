@@ -18,7 +18,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtq2_gb300.so")
-SOURCES = ["api.cu", "reformat.cu", "quantize.cu", "act16.cu", "attention.cu", "gemv.cu", "f32ref.cu", "gemm_tc.cu", "gemm_tc_ws.cu"]
+SOURCES = ["api.cu", "reformat.cu", "quantize.cu", "act16.cu", "attention.cu", "gemv.cu", "f32ref.cu", "gemm_tc.cu", "gemm_tc_ws.cu", "skinny_mma.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC]
 

@@ -142,6 +142,8 @@ int finish(cudaError_t e) { return e == cudaSuccess ? TQ2_OK : TQ2_ERR_CUDA; }
 // M at and above which the tcgen05 kernel beats the f32 CUDA-core small-M kernel.
 // (measured at K = N = 4096: M=2 15.4 vs 17.6 us, M=3 20.8 vs 17.6 us)
 constexpr int64_t kTcMinM = 3;
+// Largest M that tq2_gemm sends to the one-launch skinny tensor-core kernel.
+constexpr int64_t kSkinnyMmaMaxM = 32;
 
 }  // namespace
 
@@ -182,9 +184,8 @@ int tq2_device_status(void *stream) {
 }
 
 int tq2_select_kernel(int64_t m, int64_t n, int64_t k) {
-    (void)n;
-    (void)k;
     if (m == 1) return TQ2_KERNEL_GEMV;
+    if (m <= kSkinnyMmaMaxM && tq2::skinny_mma_fits(m, n, k)) return TQ2_KERNEL_SKINNY_MMA;
     if (m < kTcMinM && m <= tq2::kSkinnyMaxM) return TQ2_KERNEL_SKINNY;
     return TQ2_KERNEL_TC;
 }
@@ -223,7 +224,8 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
     if (kernel == TQ2_KERNEL_AUTO) kernel = tq2_select_kernel(m, n, k);
     if (kernel == TQ2_KERNEL_GEMV && m != 1) return TQ2_ERR_INVALID_ARG;
     if (kernel == TQ2_KERNEL_SKINNY && m > tq2::kSkinnyMaxM) return TQ2_ERR_INVALID_ARG;
-    if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_TC_DIRECT) return TQ2_ERR_INVALID_ARG;
+    if (kernel == TQ2_KERNEL_SKINNY_MMA && !tq2::skinny_mma_fits(m, n, k)) return TQ2_ERR_INVALID_ARG;
+    if (kernel < TQ2_KERNEL_GEMV || kernel > TQ2_KERNEL_SKINNY_MMA) return TQ2_ERR_INVALID_ARG;
     tq2::LaunchCtx ctx;
     st = prepare(stream, &ctx, {w_soa, x, residual, out});
     if (st != TQ2_OK) return st;
@@ -244,6 +246,8 @@ int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *re
         }
         case TQ2_KERNEL_TC_DIRECT:
             return finish(tq2::launch_tc(w_soa, x, residual, out, m, n, k, ctx));
+        case TQ2_KERNEL_SKINNY_MMA:
+            return finish(tq2::launch_skinny_mma(w_soa, x, residual, out, m, n, k, ctx));
         default: return finish(tq2::launch_f32ref(w_soa, x, residual, out, m, n, k, ctx));
     }
 }
@@ -399,7 +403,7 @@ int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, v
 
 int tq2_attention_f32(const float *q, const float *k, const float *v, float *out, int64_t heads,
                       int64_t seq, int64_t dim, void *stream) {
-    if (heads < 0 || seq < 0 || (dim != 64 && dim != 128)) return TQ2_ERR_INVALID_ARG;
+    if (heads < 0 || seq < 0 || dim < 8 || dim > 128 || dim % 8) return TQ2_ERR_INVALID_ARG;
     if (heads > 65535 || seq > (int64_t(1) << 24) || heads * ((seq + 127) / 128 * 128) > INT32_MAX)
         return TQ2_ERR_INVALID_ARG;
     if (heads == 0 || seq == 0) return TQ2_OK;

@@ -132,7 +132,7 @@ __device__ __forceinline__ float att_ex2(float x) {
 template <int D>
 __global__ void __launch_bounds__(ATHREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
-                const __grid_constant__ CUtensorMap vmap, float *__restrict__ out, int H, int S, int Sp,
+                const __grid_constant__ CUtensorMap vmap, float *__restrict__ out, int H, int S, int Sp, int Dout,
                 unsigned int *status, uint64_t wait_ns) {
     using Lay = AttnLayout<D>;
     extern __shared__ uint8_t att_raw[];
@@ -371,18 +371,22 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 tc_fence_after();
                 const float inv = 1.0f / l;
                 const int t = qb * AQ + r;
-                float *orow = out + int64_t(t) * H * D + int64_t(h) * D;
+                // the head's Dout real features (the staged operands pad D to
+                // the kernel's width with zeros; those columns are not written)
+                float *orow = out + int64_t(t) * H * Dout + int64_t(h) * Dout;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
+                    if (c * 32 >= Dout) break;
                     uint32_t o[32];
                     att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
                     tc_wait_ld();
                     if (t < S) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
-                            *reinterpret_cast<float4 *>(orow + c * 32 + i) =
-                                make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
-                                            __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
+                            if (c * 32 + i < Dout)
+                                *reinterpret_cast<float4 *>(orow + c * 32 + i) =
+                                    make_float4(__uint_as_float(o[i]) * inv, __uint_as_float(o[i + 1]) * inv,
+                                                __uint_as_float(o[i + 2]) * inv, __uint_as_float(o[i + 3]) * inv);
                     }
                 }
             }
@@ -404,11 +408,11 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     }
 }
 
-// q, k -> binary16 [H][Sp][D] (blockIdx.y = 0: q times `qscale`; 1: k), zero
-// rows past S; 8 elements per item.
+// q, k [H][S][Din] -> binary16 [H][Sp][D] (blockIdx.y = 0: q times `qscale`;
+// 1: k), zero rows past S and zero features past Din; 8 elements per item.
 __global__ void __launch_bounds__(256)
 attn_prep_qk_kernel(const float *__restrict__ q, const float *__restrict__ k, __half *__restrict__ qh,
-                    __half *__restrict__ kh, int H, int S, int Sp, int D, float qscale) {
+                    __half *__restrict__ kh, int H, int S, int Sp, int D, int Din, float qscale) {
     const float *src = blockIdx.y ? k : q;
     __half *dst = blockIdx.y ? kh : qh;
     const float scale = blockIdx.y ? 1.0f : qscale;
@@ -418,8 +422,8 @@ attn_prep_qk_kernel(const float *__restrict__ q, const float *__restrict__ k, __
         const int g = int(it % (D / 8));
         const int h = int(row / Sp), s = int(row % Sp);
         float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (s < S) {
-            const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t(h) * S + s) * D + g * 8);
+        if (s < S && g * 8 < Din) {
+            const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t(h) * S + s) * Din + g * 8);
             const float4 a = __ldcs(p), c = __ldcs(p + 1);
             f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
         }
@@ -434,10 +438,11 @@ attn_prep_qk_kernel(const float *__restrict__ q, const float *__restrict__ k, __
     }
 }
 
-// v [H][S][D] -> binary16 v^T [H][D][Sp], zero keys past S: 64 keys x 64 features
-// per block through shared memory, 16-byte reads and writes.
+// v [H][S][Din] -> binary16 v^T [H][D][Sp], zero keys past S and features past
+// Din: 64 keys x 64 features per block through shared memory, 16-byte reads
+// and writes.
 __global__ void __launch_bounds__(256)
-attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S, int Sp, int D) {
+attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S, int Sp, int D, int Din) {
     __shared__ __align__(16) __half tile[64][72];  // [feature][key], 8 halves of padding
     const int s0 = blockIdx.x * 64, d0 = blockIdx.y * 64, h = blockIdx.z;
     const int t = threadIdx.x;
@@ -446,7 +451,8 @@ attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S,
         const int idx = t + 256 * i;           // 0..1023: key idx / 16, features 4 (idx % 16) .. +3
         const int key = idx >> 4, f4 = idx & 15;
         float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s0 + key < S) x = __ldcs(reinterpret_cast<const float4 *>(v + (int64_t(h) * S + s0 + key) * D + d0) + f4);
+        if (s0 + key < S && d0 + 4 * f4 < Din)
+            x = __ldcs(reinterpret_cast<const float4 *>(v + (int64_t(h) * S + s0 + key) * Din + d0) + f4);
         tile[4 * f4 + 0][key] = __float2half_rn(x.x);
         tile[4 * f4 + 1][key] = __float2half_rn(x.y);
         tile[4 * f4 + 2][key] = __float2half_rn(x.z);
@@ -462,21 +468,22 @@ attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S,
     }
 }
 
+// D: the kernel's head width (64 or 128); Din <= D the caller's (a multiple of 8)
 template <int D>
 cudaError_t launch_attention_d(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
-                               void *ws, const LaunchCtx &ctx) {
+                               int Din, void *ws, const LaunchCtx &ctx) {
     using Lay = AttnLayout<D>;
     const int64_t Sp = (S + 127) / 128 * 128;
     __half *qh = static_cast<__half *>(ws);
     __half *kh = qh + H * Sp * D;
     __half *vt = kh + H * Sp * D;
-    const float qscale = 1.4426950408889634f / sqrtf(float(D));  // log2(e) / sqrt(D)
+    const float qscale = 1.4426950408889634f / sqrtf(float(Din));  // log2(e) / sqrt(head dim)
     const int64_t items = H * Sp * (D / 8);
     const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
     attn_prep_qk_kernel<<<dim3(unsigned(pgrid), 2), 256, 0, ctx.stream>>>(q, k, qh, kh, int(H), int(S), int(Sp), D,
-                                                                          qscale);
+                                                                          Din, qscale);
     attn_prep_vt_kernel<<<dim3(unsigned(Sp / 64), unsigned(D / 64), unsigned(H)), 256, 0, ctx.stream>>>(
-        v, vt, int(S), int(Sp), D);
+        v, vt, int(S), int(Sp), D, Din);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -502,23 +509,26 @@ cudaError_t launch_attention_d(const float *q, const float *k, const float *v, f
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES);
     if (e != cudaSuccess) return e;
     attn_fwd_kernel<D><<<dim3(unsigned(Sp / AQ), unsigned(H)), ATHREADS, Lay::BYTES, ctx.stream>>>(
-        qmap, kmap, vmap, out, int(H), int(S), int(Sp), ctx.status, ctx.wait_ns);
+        qmap, kmap, vmap, out, int(H), int(S), int(Sp), Din, ctx.status, ctx.wait_ns);
     return cudaPeekAtLastError();
 }
 
 }  // namespace
 
+// Head width of the kernel that serves head dim D (a multiple of 8, <= 128).
+static int64_t attn_width(int64_t D) { return D <= 64 ? 64 : 128; }
+
 size_t attention_ws_bytes(int64_t H, int64_t S, int64_t D) {
     const int64_t Sp = (S + 127) / 128 * 128;
-    return size_t(3) * size_t(H) * size_t(Sp) * size_t(D) * 2;
+    return size_t(3) * size_t(H) * size_t(Sp) * size_t(attn_width(D)) * 2;
 }
 
 cudaError_t launch_attention(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
                              int64_t D, void *ws, const LaunchCtx &ctx) {
     if (H > 65535 || S > (int64_t(1) << 24) || H * ((S + 127) / 128 * 128) > INT32_MAX) return cudaErrorInvalidValue;
-    if (D == 128) return launch_attention_d<128>(q, k, v, out, H, S, ws, ctx);
-    if (D == 64) return launch_attention_d<64>(q, k, v, out, H, S, ws, ctx);
-    return cudaErrorInvalidValue;
+    if (D < 8 || D > 128 || D % 8) return cudaErrorInvalidValue;
+    if (attn_width(D) == 64) return launch_attention_d<64>(q, k, v, out, H, S, int(D), ws, ctx);
+    return launch_attention_d<128>(q, k, v, out, H, S, int(D), ws, ctx);
 }
 
 }  // namespace tq2

@@ -263,6 +263,9 @@ __device__ __forceinline__ void decode_word(uint32_t w, __half2 d2, uint32_t (&o
 
 __global__ void __launch_bounds__(256)
 x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, int K, int MT) {
+    // the tensor-core kernel behind this one may launch now: it waits for this
+    // kernel's completion before it reads a tile
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int groups = K / 16;                 // 16-float groups per row
     const int KT = K / BK;
     const int64_t items = int64_t(MT) * BM * groups;
@@ -302,7 +305,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
              const __grid_constant__ CUtensorMap xmap, const __half *__restrict__ dpl,
              const uint8_t *__restrict__ xtiles, const float *residual, float *out, const __half *res16,
-             __half *out16, int M, int N, int K, int epi_mode, int ksplit, float *partial,
+             __half *out16, int M, int N, int K, int epi_mode, int ksplit, float *partial, int after_prepass,
              unsigned int *status, uint64_t wait_ns) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = smem_u32(smem_raw);
@@ -385,6 +388,11 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         if (lane == 0) {
             if (codes)
                 asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+            // Launched right behind the x pre-pass (programmatic dependent
+            // launch): the pre-pass writes only the x tiles, so only their
+            // issuer waits for it; weight codes stream and decode meanwhile.
+            // (Everything before the pre-pass completed before it started.)
+            if (!codes && after_prepass) asm volatile("griddepcontrol.wait;" ::: "memory");
             int64_t g = 0;
             int last_round[STAGES > CSTAGES ? STAGES : CSTAGES];
             for (int s = 0; s < depth; ++s) last_round[s] = -1;
@@ -970,10 +978,24 @@ cudaError_t launch_tc_ws_mode(const void *w_soa, const TcIo &io, int64_t m, int6
                                                     ((x_tile_bytes(m, k) + 255) & ~size_t(255)));
     const int64_t nitems = ((m + BX - 1) / BX) * ((((n + BW - 1) / BW) + 1) / 2) * ksplit;
     const int64_t grid = 2 * std::min<int64_t>(nitems, ctx.num_sms / 2);
-    tc_ws_kernel<<<unsigned(grid), NUM_THREADS, SMEM_BYTES, ctx.stream>>>(
-        qmap, omap, xmap, v.d, static_cast<const uint8_t *>(ws), io.residual, io.out, io.res16, io.out16,
-        int(m), int(n), int(k), epi_mode, ksplit, partial, ctx.status, ctx.wait_ns);
-    e = cudaPeekAtLastError();
+    {
+        // behind the pre-pass: programmatic dependent launch (see the x issuer)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(unsigned(grid));
+        cfg.blockDim = dim3(NUM_THREADS);
+        cfg.dynamicSmemBytes = SMEM_BYTES;
+        cfg.stream = ctx.stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = act16 ? 0 : 1;
+        const int after_prepass = act16 ? 0 : 1;
+        e = cudaLaunchKernelEx(&cfg, tc_ws_kernel, qmap, omap, xmap, v.d, static_cast<const uint8_t *>(ws),
+                               io.residual, io.out, io.res16, io.out16, int(m), int(n), int(k), epi_mode, ksplit,
+                               partial, after_prepass, ctx.status, ctx.wait_ns);
+    }
+    if (e == cudaSuccess) e = cudaPeekAtLastError();
     if (e != cudaSuccess || ksplit == 1) return e;
     const int64_t mn = m * n;
     const int64_t rgrid = std::min<int64_t>((mn / 4 + 255) / 256 + 1, int64_t(ctx.num_sms) * 8);

@@ -253,23 +253,26 @@ constexpr int kGvWideConsumers = 16;
 //
 // Arithmetic.  A row is cut into 1024-weight chunks; consumer warp w owns chunk
 // w % C of every row of the stages it takes, and lane l of it the 32 weights
-// [1024 c + 32 l, +32), i.e. a fixed slice of x.  Each lane quantises its own
-// slice once, to a signed fixed-point integer X = rint(x * 2^22 / s) with s =
-// max |x| over the slice (|X| <= 2^22), held in registers as three 8-bit limbs
-// (top limb signed): no shared-memory table and no block-wide barrier between
-// the quantisation and the dot products.  For one 32-bit code word (16
-// weights, code i at bits 2i), (w >> 2t) & 0x03030303 gathers the codes of
-// weights t, t+4, t+8, t+12 into four bytes, and dp4a multiplies them with the
-// matching limb bytes and accumulates exactly in int32.  Per row and slice,
-// sum_i (c_i - 1) X_i = sum c*X - sum X is exact; one conversion to f32 and one
-// multiply by s * 2^-22 * d finish the slice.  Per weight this is 3/4 dp4a +
-// 7/16 shift/logic operations instead of the 2 operations of an exact-f32
-// decode.  The error is the quantisation of x (per element at most 2^-22 * s:
-// half a step plus the rounding of the reciprocal), the rounding of the
-// slice's integer sum to f32 (|sum| <= 2^27) and the f32 sums over slices.
-// The row's 32 lane partials of a chunk are reduced with shuffles;
-// per-(row, chunk) partials meet in shared memory and are summed per row at
-// the end (plus the residual).
+// [1024 c + 32 l, +32), i.e. a fixed slice of x, inside 128-weight block l / 4.
+// Each lane quantises its own slice once, to a signed fixed-point integer
+// X = rint(x * 2^22 / s) with s = max |x| over the slice's 128-weight block
+// (the four lanes 4j .. 4j+3 agree on it by two shuffles; |X| <= 2^22), held in
+// registers as three 8-bit limbs (top limb signed): no shared-memory table and
+// no block-wide barrier between the quantisation and the dot products.  For one
+// 32-bit code word (16 weights, code i at bits 2i), (w >> 2t) & 0x03030303
+// gathers the codes of weights t, t+4, t+8, t+12 into four bytes, and dp4a
+// multiplies them with the matching limb bytes and accumulates exactly in
+// int32.  Per row and lane, T = sum_i (c_i - 1) X_i = sum c*X - sum X is exact
+// (|T| <= 2^28).  The rows of a stage are then reduced over the warp by a
+// halving butterfly: its first two levels add the four lanes of one block,
+// which share s, as integers (exact, |sum| <= 2^30); each value left is
+// converted once to f32 and multiplied by s * 2^-22 * d of its block; float
+// levels finish the sum over the chunk.  Per weight this is 3/4 dp4a + 7/16
+// shift/logic operations instead of the 2 operations of an exact-f32 decode.
+// The error is the quantisation of x (per element at most 2^-22 * s: half a
+// step plus the rounding of the reciprocal), the rounding of each block's
+// integer sum to f32 and the f32 sums over blocks.  Per-(row, chunk) partials
+// meet in shared memory and are summed per row at the end (plus the residual).
 
 __device__ __forceinline__ void bulk_g2s_gv(uint32_t dst, const void *src, uint32_t bytes,
                                             uint64_t *bar) {
@@ -443,7 +446,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
-                if (!mbar_wait_bounded(&empty[slot], (u - 1) & 1, wait_ns, status)) {
+                if (!mbar_wait_spin(&empty[slot], (u - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -453,7 +456,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             // every copy issued must land before the CTA exits: the last round of each slot
             const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
             for (int st = max(0, nstages - P.ns); st < nstages; ++st)
-                mbar_wait_bounded(&full[st % P.ns], (st / P.ns) & 1, drain, status);
+                mbar_wait_spin(&full[st % P.ns], (st / P.ns) & 1, drain, status);
         }
     } else if (warp < consumers) {
         // Warp w takes chunk c = w % C of the stages st = g, g + groups, ...
@@ -470,7 +473,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         uint32_t L[2][4][3];
         int sx = 0;
         float sc;
-        if (!mbar_wait_bounded(xbar, 0, wait_ns, status)) *abort_flag = 1;
+        if (!mbar_wait_spin(xbar, 0, wait_ns, status)) *abort_flag = 1;
         {
             float xv[kGvLaneW];
             const int xrow = kw_rd / kGvLaneW;  // this lane's 128-byte row of the x tile
@@ -486,6 +489,11 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             float s = 0.f;
 #pragma unroll
             for (int j = 0; j < kGvLaneW; ++j) s = fmaxf(s, fabsf(xv[j]));
+            // one scale per 128-weight block: the largest |x| over the block's
+            // four lanes (lanes 4j .. 4j+3), so that the block's four integer
+            // sums share it and can be added exactly before any scaling
+            s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 1));
+            s = fmaxf(s, __shfl_xor_sync(0xffffffffu, s, 2));
             // 2^22 / s: the correctly rounded reciprocal times 2^22 (exact scaling)
             const float inv = s > 0.f ? __frcp_rn(s) * 4194304.0f : 0.f;
             // X = x * inv rounded to the nearest integer (ties to even) by one
@@ -499,6 +507,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
                 X[j] = __float_as_int(__fmaf_rn(xv[j], inv, 12582912.0f)) - 0x4B400000;
                 sx += X[j];
             }
+            sx = -sx;  // the first accumulator of every row starts at -sum X (the "- 1" of c - 1)
 #pragma unroll
             for (int q = 0; q < 2; ++q)
 #pragma unroll
@@ -524,7 +533,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         const int64_t dcol = kw_rd / kBlockW;
         int slot = g, ph = 0;  // ring slot and phase of stage st, advanced incrementally
         for (int st = g; st < nstages; st += P.groups) {
-            if (!mbar_wait_bounded(&full[slot], uint32_t(ph), wait_ns, status)) {
+            if (!mbar_wait_spin(&full[slot], uint32_t(ph), wait_ns, status)) {
                 *abort_flag = 1;
                 break;
             }
@@ -537,44 +546,92 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             // All RS rows of the slot are read: rows past nv (the CTA's last
             // stage) hold stale bytes of the slot and their results are dropped.
             uint2 cw[RS];
-            float d[RS];
+#pragma unroll
+            for (int uu = 0; uu < RS; ++uu)
+                cw[uu] = *reinterpret_cast<const uint2 *>(sb + code_off + uint32_t(uu) * kq32);
+            // Release this chunk's share of the slot once all its reads are
+            // done: right here when the block scales come from global memory,
+            // after the scale reads below when they travel in the slot.
+            if (!dbulk) mbar_arrive(&empty[slot]);
+            // Per row: T = sum_i (c_i - 1) X_i over the lane's 32 weights, exact
+            // in int32 (|T| <= 2^28).  Codes of weights t, t+4, t+8, t+12 of a
+            // word are the bytes of (w >> 2t) & 0x03030303; each dp4a multiplies
+            // them with one 8-bit limb of the matching X values.
+            constexpr int V = RS <= 2 ? 2 : RS <= 4 ? 4 : 8;  // reduction width (power of two)
+            int tv[V];
+#pragma unroll
+            for (int uu = 0; uu < V; ++uu) tv[uu] = 0;
 #pragma unroll
             for (int uu = 0; uu < RS; ++uu) {
-                cw[uu] = *reinterpret_cast<const uint2 *>(sb + code_off + uint32_t(uu) * kq32);
-                d[uu] = dbulk ? __half2float(*reinterpret_cast<const __half *>(sb + d_off + uint32_t(uu) * kb2))
-                              : (uu < nv ? __half2float(__ushort_as_half(ldg_u16(dpl + int64_t(real_row(r0 + uu)) * kb + dcol)))
-                                         : 0.f);
-            }
-            // every lane has read its codes: release this chunk's share of the slot
-            mbar_arrive(&empty[slot]);
-            // the rows' 3 * RS accumulator chains advance together
-            int a0[RS], a1[RS], a2[RS];
+                int a0 = sx, a1 = 0, a2 = 0;
 #pragma unroll
-            for (int uu = 0; uu < RS; ++uu) a0[uu] = a1[uu] = a2[uu] = 0;
+                for (int q = 0; q < 2; ++q)
 #pragma unroll
-            for (int q = 0; q < 2; ++q)
-#pragma unroll
-                for (int t = 0; t < 4; ++t)
-#pragma unroll
-                    for (int uu = 0; uu < RS; ++uu) {
+                    for (int t = 0; t < 4; ++t) {
                         const uint32_t wq = q == 0 ? cw[uu].x : cw[uu].y;
                         const uint32_t cv = (wq >> (2 * t)) & 0x03030303u;
-                        a0[uu] = dp4a_uu(cv, L[q][t][0], a0[uu]);
-                        a1[uu] = dp4a_uu(cv, L[q][t][1], a1[uu]);
-                        a2[uu] = dp4a_us(cv, L[q][t][2], a2[uu]);
+                        a0 = dp4a_uu(cv, L[q][t][0], a0);
+                        a1 = dp4a_uu(cv, L[q][t][1], a1);
+                        a2 = dp4a_us(cv, L[q][t][2], a2);
                     }
-            constexpr int V = RS <= 2 ? 2 : RS <= 4 ? 4 : 8;  // reduction width (power of two)
-            float v[V];
-#pragma unroll
-            for (int uu = 0; uu < V; ++uu) {
-                const int tot = uu < RS ? (a2[uu] << 16) + (a1[uu] << 8) + a0[uu] - sx : 0;
-                v[uu] = uu < RS ? float(tot) * (sc * d[uu]) : 0.f;
+                tv[uu] = a0 + (a1 << 8) + (a2 << 16);
             }
-            butterfly<V>(v, lane);
-            constexpr int G = 32 / V;
-            if (lane % G == 0) {
-                const int uu = lane / G;
-                if (uu < RS && uu < nv) partial[(r0 + uu) * C + c] = v[0];
+            // Reduction over the 32 lanes, one row per value (halving
+            // butterfly: at each level a lane keeps half of its rows and adds the
+            // partner's share of them).  The first two levels pair the four
+            // lanes of one 128-weight block, which share the x scale: exact
+            // integer adds (|sum| <= 2^30).  Then each remaining value (row) is
+            // scaled once by s_b * 2^-22 * d of its block and the float levels
+            // follow.
+            constexpr int NI = V >= 4 ? 2 : 1;  // integer halving levels
+#pragma unroll
+            for (int lv = 0; lv < NI; ++lv) {
+                const int o = 1 << lv, half = V >> (lv + 1);
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < V / 2; ++i)
+                    if (i < half) {
+                        const int give = upper ? tv[i] : tv[i + half];
+                        const int keep = upper ? tv[i + half] : tv[i];
+                        tv[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+                    }
+            }
+            if (V == 2) tv[0] += __shfl_xor_sync(0xffffffffu, tv[0], 2);  // the block's other lane pair
+            // rows held now: lane bits 0 (and 1) select which part of the stage
+            constexpr int VH = V >> NI;  // values per lane after the integer levels
+            const int sel = NI == 2 ? ((lane & 1) << 1) | ((lane >> 1) & 1) : (lane & 1);
+            float fv[VH];
+#pragma unroll
+            for (int i = 0; i < VH; ++i) {
+                const int uu = sel * VH + i;  // stage row of value i
+                float dd = 0.f;
+                if (uu < nv)
+                    dd = dbulk ? __half2float(*reinterpret_cast<const __half *>(sb + d_off + uint32_t(uu) * kb2))
+                               : __half2float(__ushort_as_half(ldg_u16(dpl + int64_t(real_row(r0 + uu)) * kb + dcol)));
+                fv[i] = active ? float(tv[i]) * (sc * dd) : 0.f;
+            }
+            if (dbulk) mbar_arrive(&empty[slot]);
+            // float halving levels at offsets 4, 8, ... until one value is left, then full levels
+#pragma unroll
+            for (int lv = 0; (VH >> lv) > 1; ++lv) {
+                const int o = 4 << lv, half = VH >> (lv + 1);
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < VH / 2; ++i)
+                    if (i < half) {
+                        const float give = upper ? fv[i] : fv[i + half];
+                        const float keep = upper ? fv[i + half] : fv[i];
+                        fv[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+                    }
+            }
+            constexpr int LV = V == 8 ? 3 : 2;  // levels done so far (offsets 1 .. 2^(LV-1))
+#pragma unroll
+            for (int o = 1 << LV; o < 32; o <<= 1) fv[0] += __shfl_xor_sync(0xffffffffu, fv[0], o);
+            // lane l (l < 2^LV) holds the row whose index bits are lane bits 0, 1(, 2), most significant first
+            if (lane < V) {
+                const int uu = V == 8 ? ((lane & 1) << 2) | (((lane >> 1) & 1) << 1) | ((lane >> 2) & 1)
+                                      : V == 4 ? ((lane & 1) << 1) | ((lane >> 1) & 1) : (lane & 1);
+                if (uu < RS && uu < nv) partial[(r0 + uu) * C + c] = fv[0];
             }
             slot += P.groups;
             if (slot >= P.ns) slot -= P.ns, ph ^= 1;

@@ -98,6 +98,12 @@ size_t attention_ws_bytes(int64_t H, int64_t S, int64_t D);
 cudaError_t launch_attention(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
                              int64_t D, void *ws, const LaunchCtx &ctx);
 
+// Skinny-M tensor-core kernel (2 <= m <= 32, k up to the shared-memory limit
+// of its K slices): one launch, no workspace.  cudaErrorNotSupported outside.
+bool skinny_mma_fits(int64_t m, int64_t n, int64_t k);
+cudaError_t launch_skinny_mma(const void *w_soa, const float *x, const float *residual, float *out,
+                              int64_t m, int64_t n, int64_t k, const LaunchCtx &ctx);
+
 // Largest M the small-M CUDA-core kernel handles.
 constexpr int64_t kSkinnyMaxM = 16;
 
@@ -157,6 +163,34 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (globaltimer_ns() - t0 >= limit_ns) {
             atomicOr(status, static_cast<unsigned int>(TQ2_ERR_TIMEOUT));
             return false;
+        }
+    }
+}
+
+// Bounded wait that spins without a suspend hint (no sleeping between polls:
+// the phase is seen as soon as it completes), reading the timer only every 64
+// polls.  For waits that are usually short (data that is about to land).
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, uint64_t limit_ns,
+                                               unsigned int *status) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        uint32_t ok;
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(ok)
+            : "r"(smem_u32(bar)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if ((it & 63u) == 0) {
+            const uint64_t t = globaltimer_ns();
+            if (it == 0) {
+                t0 = t;
+            } else if (t - t0 >= limit_ns) {
+                atomicOr(status, static_cast<unsigned int>(TQ2_ERR_TIMEOUT));
+                return false;
+            }
         }
     }
 }

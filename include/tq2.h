@@ -94,8 +94,10 @@ typedef enum {
                               stream-ordered temporary, then the clustered kernel; f16
                               operands, f32 accumulation in TMEM */
     TQ2_KERNEL_F32REF = 4, /* exact-f32 CUDA-core tiled kernel */
-    TQ2_KERNEL_TC_DIRECT = 5 /* tcgen05 kernel that converts x itself (no temporary memory);
-                                same arithmetic as TQ2_KERNEL_TC */
+    TQ2_KERNEL_TC_DIRECT = 5, /* tcgen05 kernel that converts x itself (no temporary memory);
+                                 same arithmetic as TQ2_KERNEL_TC */
+    TQ2_KERNEL_SKINNY_MMA = 6 /* 2 <= M <= 32: one-launch tensor-core kernel for few rows (x
+                                 rounded to binary16, f32 accumulation; no temporary memory) */
 } tq2_kernel;
 
 /* Bytes of a weight of n rows and k columns in either layout: n*(k/128)*34.
@@ -136,18 +138,19 @@ int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *st
  *   x        : device f32 [k], finite
  *   residual : device f32 [n], or NULL
  *   out      : device f32 [n]
- * Arithmetic (k <= 12288): x is quantised per 32-weight slice to a signed
- * fixed-point integer relative to the slice's largest |x| (23 bits:
- * |x - xq| <= 2^-22 * max|x_slice|); the ternary dot products are then exact
- * integer sums, scaled by max|x_slice| * 2^-22 * d and summed in f32.
- * Per element: |error| <= sum over slices of 2^-22 * max|x_slice| * sum_slice |w|
- * plus f32 rounding of the slice sums and of the final sum.  For k > 12288:
+ * Arithmetic (k <= 12288): x is quantised per 128-weight block to a signed
+ * fixed-point integer relative to the block's largest |x| (23 bits:
+ * |x - xq| <= 2^-22 * max|x_block|); the ternary dot products are then exact
+ * integer sums per block, scaled by max|x_block| * 2^-22 * d and summed in f32.
+ * Per element: |error| <= sum over blocks of 2^-22 * max|x_block| * sum_block |w|
+ * plus f32 rounding of the block sums and of the final sum.  For k > 12288:
  * exact f32 products and f32 accumulation. */
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t n, int64_t k, void *stream);
 
 /* Any-M matmul with optional residual epilogue, dispatching on M (and N, K)
- * between the GEMV, the small-M CUDA-core kernel and the tcgen05 tensor-core
+ * between the GEMV (m = 1), the one-launch skinny tensor-core kernel
+ * (2 <= m <= 32, TQ2_KERNEL_SKINNY_MMA below) and the tcgen05 tensor-core
  * kernel ("oxibonsai-image 0.2.2 src/gpu.rs", `ternary_matmul_gpu`;
  * the batched TQ2 GEMMs of the "oxibonsai-kernels 0.1.5 ... pipelines.rs"
  * page).
@@ -181,7 +184,7 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
  *   w_soa : device SoA weight of n = 2f rows (from tq2_reformat_aos_to_soa)
  *   x     : device f32 [m, k] row-major
  *   out   : device f32 [m, f] row-major (may not overlap x or w_soa)
- * Arithmetic: m = 1 runs the GEMV (x quantised per 32-weight slice, exact
+ * Arithmetic: m = 1 runs the GEMV (x quantised per 128-weight block, exact
  * integer dot products; see tq2_gemv) for k <= 12288; m >= 2 runs the
  * tensor-core kernel (x rounded to binary16; see tq2_gemm) with the activation
  * in its epilogue when f % 16 == 0.  Other shapes compute the plain product
@@ -236,16 +239,20 @@ int tq2_gemm_act16(const void *w_soa, const void *x16, const void *residual16, v
  * over all seq keys (non-causal).
  *   q, k, v : device f32 [heads, seq, dim], head-major (RoPE already applied)
  *   out     : device f32 [seq, heads*dim], token-major (may not overlap q, k, v)
- *   dim     : 64 or 128
+ *   dim     : head dimension, a multiple of 8 from 8 to 128 (the page's
+ *             range); the kernel runs 64 (dim <= 64) or 128 features wide
+ *             with the extra features zero in its staged copies, which
+ *             changes no result
  * Arithmetic: q (times log2(e)/sqrt(dim)), k and v are rounded to binary16
  * (nearest even; their magnitudes must stay below 65504) and multiplied on the
  * tensor cores with f32 accumulation; the softmax runs in f32 with the
  * hardware 2^x, its weights rounded to binary16 for the second product; the
  * normalisation by the weight sum is the last step (flash attention: one pass
  * over the keys, no [seq, seq] matrix in memory).
- * Memory: a temporary of 3*heads*ceil(seq/128)*128*dim*2 bytes from the
- * device's default memory pool, ordered on `stream`.
- * Errors: TQ2_ERR_INVALID_ARG (dim not 64 or 128, negative or too large sizes
+ * Memory: a temporary of 3*heads*ceil(seq/128)*128*w*2 bytes (w = 64 for
+ * dim <= 64, else 128) from the device's default memory pool, ordered on
+ * `stream`.
+ * Errors: TQ2_ERR_INVALID_ARG (dim not a multiple of 8 in [8, 128], negative or too large sizes
  * (heads <= 65535, seq <= 2^24), NULL, overlap), TQ2_ERR_MISALIGNED (pointers
  * not 16-byte aligned), TQ2_ERR_TIMEOUT via tq2_device_status, TQ2_ERR_CUDA.
  * heads = 0 or seq = 0: no-op. */
@@ -312,9 +319,20 @@ int tq2_gemm_noalloc(const void *w_soa, const float *x, const float *residual, f
                      int64_t m, int64_t n, int64_t k, void *stream);
 
 /* tq2_gemm with an explicit kernel choice (a tq2_kernel value), for
- * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1 and
- * TQ2_KERNEL_SKINNY m <= 16 (else TQ2_ERR_INVALID_ARG).  TQ2_KERNEL_TC
- * allocates as tq2_gemm does. */
+ * benchmarks and tests.  TQ2_KERNEL_GEMV requires m == 1, TQ2_KERNEL_SKINNY
+ * m <= 16 and TQ2_KERNEL_SKINNY_MMA 2 <= m <= 32 with k small enough for its
+ * K slices' shared memory (k <= 12288 at m = 32) (else TQ2_ERR_INVALID_ARG).
+ * TQ2_KERNEL_TC allocates as tq2_gemm does.
+ *
+ * TQ2_KERNEL_SKINNY_MMA ("the few-row batches" of the pages' TQ2 GEMMs, any
+ * batch size): one launch.  CTAs of 128 weight rows each take a K slice; the
+ * CTAs of one row tile form a thread-block cluster and sum their partial
+ * results through distributed shared memory in a fixed order (results are
+ * the same bits on every call).  Warp-level tensor-core MMAs take the weight
+ * codes decoded in registers as the A operand and x rounded to binary16
+ * (nearest even; |x| < 65504) as the B operand, with f32 accumulation per
+ * 128-weight block, then the block's d applied in f32: the tensor-core
+ * path's arithmetic. */
 int tq2_gemm_with(int kernel, const void *w_soa, const float *x, const float *residual,
                   float *out, int64_t m, int64_t n, int64_t k, void *stream);
 

@@ -54,9 +54,13 @@ def test_kernel_selection(tq2):
     assert tq2.tq2_select_kernel(1, 4096, 12288) == tq2.TQ2_KERNEL_GEMV
     assert tq2.tq2_select_kernel(1536, 3072, 3072) == tq2.TQ2_KERNEL_TC
     assert tq2.tq2_select_kernel(4096, 3072, 12288) == tq2.TQ2_KERNEL_TC
-    assert tq2.tq2_select_kernel(2, 4096, 4096) == tq2.TQ2_KERNEL_SKINNY
-    for m in (3, 7, 8, 9, 16, 64, 100):
+    for m in (2, 3, 7, 8, 9, 16, 32):
+        assert tq2.tq2_select_kernel(m, 4096, 4096) == tq2.TQ2_KERNEL_SKINNY_MMA
+        assert tq2.tq2_select_kernel(m, 1024, 1024) == tq2.TQ2_KERNEL_SKINNY_MMA
+    for m in (33, 64, 100):
         assert tq2.tq2_select_kernel(m, 4096, 4096) == tq2.TQ2_KERNEL_TC
+    # rows too long for the skinny kernel's K slices go to the tcgen05 kernel
+    assert tq2.tq2_select_kernel(32, 4096, 1 << 17) == tq2.TQ2_KERNEL_TC
 
 
 def rc_gemm(tq2, w, x, r, o, m, n, k, kernel=0):
@@ -101,7 +105,9 @@ def test_argument_errors_are_returned_before_any_launch(tq2):
     assert rc_gemm(tq2, W, X, None, O, 2, 4, 128, tq2.TQ2_KERNEL_GEMV) == tq2.TQ2_ERR_INVALID_ARG
     assert rc_gemm(tq2, W, X, None, O, 17, 4, 128, tq2.TQ2_KERNEL_SKINNY) == tq2.TQ2_ERR_INVALID_ARG
     assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 9) == tq2.TQ2_ERR_INVALID_ARG
-    assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 6) == tq2.TQ2_ERR_INVALID_ARG
+    assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, 7) == tq2.TQ2_ERR_INVALID_ARG
+    assert rc_gemm(tq2, W, X, None, O, 33, 4, 128, tq2.TQ2_KERNEL_SKINNY_MMA) == tq2.TQ2_ERR_INVALID_ARG
+    assert rc_gemm(tq2, W, X, None, O, 1, 4, 128, tq2.TQ2_KERNEL_SKINNY_MMA) == tq2.TQ2_ERR_INVALID_ARG
     assert rc_gemm(tq2, W, X, None, O, 4, 4, 128, -1) == tq2.TQ2_ERR_INVALID_ARG
 
 
@@ -178,7 +184,8 @@ def test_argument_errors_of_the_next_row_entry_points(tq2):
         assert conv(X, X + 16, 4, 32, None) == tq2.TQ2_ERR_INVALID_ARG
     # DiT joint attention
     a = L.tq2_attention_f32
-    assert a(X, R, W, O, 2, 128, 96, None) == tq2.TQ2_ERR_INVALID_ARG        # dim not 64 or 128
+    for bad in (100, 4, 136):                                                  # dim not 8 * j <= 128
+        assert a(X, R, W, O, 2, 128, bad, None) == tq2.TQ2_ERR_INVALID_ARG
     assert a(X, R, W, O, -1, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG
     assert a(X, R, W, O, 70000, 128, 128, None) == tq2.TQ2_ERR_INVALID_ARG   # heads > 65535
     assert a(None, None, None, None, 0, 128, 128, None) == tq2.TQ2_OK

@@ -72,6 +72,8 @@ def kernels_for(tq2, m):
         ks.append(("GEMV", tq2.TQ2_KERNEL_GEMV))
     if m <= 16:
         ks.append(("SKINNY", tq2.TQ2_KERNEL_SKINNY))
+    if 2 <= m <= 32:
+        ks.append(("SKINNY_MMA", tq2.TQ2_KERNEL_SKINNY_MMA))
     return ks
 
 
@@ -189,14 +191,17 @@ def test_operands_not_on_this_device_are_refused(tq2):
     # host memory: pageable (numpy) and page-locked (torch pinned)
     host = np.zeros(8 * m * max(n, k), dtype=np.float32)
     pinned = torch.zeros(8 * m * max(n, k), dtype=torch.float32).pin_memory()
-    for label, hp in (("pageable", host.ctypes.data), ("pinned", pinned.data_ptr())):
+    # 256-byte aligned host addresses, so that only residency can be the reason for a refusal
+    host_a = (host.ctypes.data + 255) & ~255
+    pinned_a = (pinned.data_ptr() + 255) & ~255
+    for label, hp in (("pageable", host_a), ("pinned", pinned_a)):
         bad = tq2.TQ2_ERR_INVALID_ARG
         # element-wise converter first (a plain-load kernel), then every other entry point
         assert L.tq2_act16_from_f32(hp, x16.data_ptr(), m, k, stream) == bad, label
         assert L.tq2_act16_to_f32(o16.data_ptr(), hp, m, n, stream) == bad, label
         assert L.tq2_gemv(w.data_ptr(), hp, None, out.data_ptr(), n, k, stream) == bad, label
         assert L.tq2_gemv(hp, x.data_ptr(), None, out.data_ptr(), n, k, stream) == bad, label
-        for kern in (0, 1, 2, 3, 4, 5):
+        for kern in (0, 1, 2, 3, 4, 5, 6):
             mm = 1 if kern == 1 else m
             for args in ((hp, x.data_ptr(), None, out.data_ptr()), (w.data_ptr(), hp, None, out.data_ptr()),
                          (w.data_ptr(), x.data_ptr(), hp, out.data_ptr()),

@@ -30,7 +30,8 @@ def tq2():
 
 
 def tol_for(tq2, kernel):
-    return TOL_TC if kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT) else TOL_F32
+    tc = (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT, tq2.TQ2_KERNEL_SKINNY_MMA)
+    return TOL_TC if kernel in tc else TOL_F32
 
 
 def upload(tq2, p):
@@ -137,8 +138,9 @@ def test_gemv_edge_shapes(tq2, n, k):
 
 def test_gemv_quantisation_bound_with_wide_dynamic_range(tq2):
     # one huge activation per 64 elements next to tiny ones: the GEMV's
-    # documented bound (2^-22 * max|x_slice| * sum_slice |w| per 32-weight
-    # slice) must hold, also on the slices that hold only tiny values
+    # documented bound (2^-22 * max|x_block| * sum_block |w| per 128-weight
+    # block, the granularity of its x scale) must hold, and so must the
+    # contract's 1e-5 * sum|x w|
     n, k = 512, 4096
     p = tq2_synth.make_problem(1, n, k, seed=17)
     rng = np.random.default_rng(5)
@@ -149,16 +151,18 @@ def test_gemv_quantisation_bound_with_wide_dynamic_range(tq2):
     out = run(tq2, tq2.TQ2_KERNEL_GEMV, w, p)[0].astype(np.float64)
     ref, scale = oracle.matmul(p.w_aos, p.x, n=n, k=k)
     W = np.abs(oracle.dequant(p.w_aos, n, k))
-    smax = np.abs(x.astype(np.float64)).reshape(-1, 32).max(axis=1)
-    bound = (W.reshape(n, -1, 32).sum(axis=2) * smax[None, :]).sum(axis=1) * 2.0 ** -22
+    smax = np.abs(x.astype(np.float64)).reshape(-1, 128).max(axis=1)
+    bound = (W.reshape(n, -1, 128).sum(axis=2) * smax[None, :]).sum(axis=1) * 2.0 ** -22
     bound += 1e-6 * scale[0]
     assert np.all(np.abs(out - ref[0]) <= bound)
+    assert np.all(np.abs(out - ref[0]) <= TOL_F32 * scale[0])
 
 
 # ---------------------------------------------------------------------------
 # all kernels on the small configuration and on ragged shapes
 
-KERNELS = ["TQ2_KERNEL_TC", "TQ2_KERNEL_TC_DIRECT", "TQ2_KERNEL_F32REF", "TQ2_KERNEL_SKINNY"]
+KERNELS = ["TQ2_KERNEL_TC", "TQ2_KERNEL_TC_DIRECT", "TQ2_KERNEL_F32REF", "TQ2_KERNEL_SKINNY",
+           "TQ2_KERNEL_SKINNY_MMA"]
 
 
 @pytest.mark.parametrize("kname", KERNELS)
@@ -179,6 +183,8 @@ def test_ragged_shapes(tq2, m, n, k, kname):
     kernel = getattr(tq2, kname)
     if kernel == tq2.TQ2_KERNEL_SKINNY and m > 16:
         pytest.skip("small-M kernel is limited to M <= 16")
+    if kernel == tq2.TQ2_KERNEL_SKINNY_MMA and not 2 <= m <= 32:
+        pytest.skip("skinny tensor-core kernel is limited to 2 <= M <= 32")
     p = tq2_synth.make_problem(m, n, k, seed=m * 1000 + n + k, residual=(m + n) % 2 == 0,
                                outlier_frac=0.01)
     w = upload(tq2, p)
@@ -203,7 +209,7 @@ def test_code3_decodes_to_plus_two_everywhere(tq2):
     p.w_aos[:, :, :32] = 0xFF
     w = upload(tq2, p)
     for kernel in (tq2.TQ2_KERNEL_TC, tq2.TQ2_KERNEL_TC_DIRECT, tq2.TQ2_KERNEL_F32REF,
-                   tq2.TQ2_KERNEL_SKINNY):
+                   tq2.TQ2_KERNEL_SKINNY, tq2.TQ2_KERNEL_SKINNY_MMA):
         check(run(tq2, kernel, w, p), p, tol_for(tq2, kernel), what=f"code3 {kernel}")
     p1 = tq2_synth.make_problem(1, n, k, seed=3)
     p1.w_aos[:] = p.w_aos
@@ -241,7 +247,20 @@ def test_skinny_sweep_auto(tq2, m):
     w = upload(tq2, p)
     kernel = tq2.tq2_select_kernel(m, p.n, p.k)
     out = run(tq2, tq2.TQ2_KERNEL_AUTO, w, p)
-    check(out, p, tol_for(tq2, kernel), cos=kernel == tq2.TQ2_KERNEL_TC, what=f"skinny m={m}")
+    check(out, p, tol_for(tq2, kernel), cos=tol_for(tq2, kernel) == TOL_TC, what=f"skinny m={m}")
+
+
+@pytest.mark.parametrize("m", [2, 3, 7, 8, 9, 15, 16, 17, 24, 31, 32])
+@pytest.mark.parametrize("n,k,res", [(4096, 4096, False), (1000, 1152, True), (12288, 4096, False),
+                                     (300, 12288, True)])
+def test_skinny_mma(tq2, m, n, k, res):
+    p = tq2_synth.make_problem(m, n, k, seed=31 * m + n, residual=res, outlier_frac=0.01)
+    w = upload(tq2, p)
+    assert tq2.tq2_select_kernel(m, n, k) == tq2.TQ2_KERNEL_SKINNY_MMA
+    a = run(tq2, tq2.TQ2_KERNEL_SKINNY_MMA, w, p)
+    check(a, p, TOL_TC, cos=True, what=f"skinny mma {m}x{n}x{k}")
+    b = run(tq2, tq2.TQ2_KERNEL_SKINNY_MMA, w, p)
+    assert np.array_equal(a, b)  # same bits on every call (fixed reduction order)
 
 
 @pytest.mark.parametrize("m", [7, 8, 9, 16])
@@ -290,7 +309,7 @@ def test_ws_ragged(tq2, m, n, k, residual):
     p = tq2_synth.make_problem(m, n, k, seed=m + n + k, residual=residual, outlier_frac=0.01)
     w = upload(tq2, p)
     eff = tq2.tq2_select_kernel(m, n, k)
-    check(run_ws(tq2, w, p), p, tol_for(tq2, eff), cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16),
+    check(run_ws(tq2, w, p), p, tol_for(tq2, eff), cos=(tol_for(tq2, eff) == TOL_TC and n >= 16),
           what=f"ws {m}x{n}x{k}")
 
 
@@ -311,7 +330,7 @@ def test_ws_inplace_ragged(tq2, m, n, k):
     w = upload(tq2, p)
     eff = tq2.tq2_select_kernel(m, n, k)
     check(run_ws(tq2, w, p, inplace=True), p, tol_for(tq2, eff),
-          cos=(eff == tq2.TQ2_KERNEL_TC and n >= 16), what=f"ws in-place {m}x{n}x{k}")
+          cos=(tol_for(tq2, eff) == TOL_TC and n >= 16), what=f"ws in-place {m}x{n}x{k}")
 
 
 @pytest.mark.parametrize("n", tq2_synth.DIT_NS)
@@ -675,7 +694,8 @@ def check_attention(got, q, k, v, h, s, d, *, rows=None, what=""):
 
 
 @pytest.mark.parametrize("h,s,d", [(1, 128, 128), (2, 300, 128), (3, 77, 64), (1, 1, 128), (4, 1024, 128),
-                                   (2, 513, 64)])
+                                   (2, 513, 64), (2, 200, 8), (3, 129, 24), (2, 300, 72), (1, 257, 120),
+                                   (2, 128, 56), (1, 64, 16), (2, 100, 96)])
 def test_attention_parity(tq2, h, s, d):
     rng = np.random.default_rng(h * 1000 + s + d)
     q, k, v = (rng.standard_normal((h, s, d)).astype(np.float32) for _ in range(3))
@@ -707,7 +727,10 @@ def test_attention_errors(tq2):
     a = torch.zeros(2, 128, 128, device="cuda")
     o = torch.zeros(128, 256, device="cuda")
     L = tq2.lib
-    assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 128, 96, None) == tq2.TQ2_ERR_INVALID_ARG
+    # the head dimension must be a multiple of 8 in [8, 128]
+    for bad in (0, 4, 12, 100, 136, 256, -8):
+        assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 128, bad,
+                                   None) == tq2.TQ2_ERR_INVALID_ARG
     assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 0, 128, 128, None) == tq2.TQ2_OK
     assert L.tq2_attention_f32(a.data_ptr(), a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 0, 128, None) == tq2.TQ2_OK
     assert L.tq2_attention_f32(a.data_ptr() + 4, a.data_ptr(), a.data_ptr(), o.data_ptr(), 2, 128, 128, None) == tq2.TQ2_ERR_MISALIGNED
