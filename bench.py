@@ -64,6 +64,10 @@ def parse():
     ap.add_argument("--cpu-full", action="store_true",
                     help="instead of the bench line (no GPU): the CPU oracle on the DiT configurations in "
                          "full (M=1536 at each N, then the 100-layer forward set at M=4096), all host threads")
+    ap.add_argument("--skinny", type=int, default=0,
+                    help="instead of the bench line: tq2_gemm at the skinny-sweep shape (M rows, K=N=4096) "
+                         "alone, `--steps` calls after `--warmup` on rotating weight copies, one JSON line "
+                         "with the time per call (for profiling that path)")
     ap.add_argument("--attention", action="store_true",
                     help="instead of the bench line: the DiT joint attention alone (24 heads x 4096 "
                          "tokens x 128, seeded N(0,1) inputs), `--steps` calls after `--warmup`, "
@@ -427,6 +431,37 @@ def run_attention_only(args):
             "us_per_call": round(t * 1e6, 2), "TFLOPs": round(4.0 * h * s * s * d / t / 1e12, 2)}
 
 
+def run_skinny_only(args):
+    """tq2_gemm at M = args.skinny rows, K = N = 4096 (the skinny sweep's shape),
+    nothing else: the workload of the skinny kernel's ncu summary."""
+    import torch
+    import dit_tq2_g128_gb300 as tq2
+
+    m = args.skinny
+    p = tq2_synth.skinny(m)
+    l2 = int(getattr(torch.cuda.get_device_properties(0), "L2_cache_size", 126 * 2 ** 20))
+    wb = tq2.tq2_soa_bytes(p.n, p.k)
+    c = max(2, -(-2 * l2 // wb) + 1)
+    w0 = tq2.upload_weight(p.w_aos, p.n, p.k)
+    ws = [w0] + [w0.clone() for _ in range(c - 1)]
+    x = torch.from_numpy(p.x).cuda()
+    out = torch.empty((p.m, p.n), dtype=torch.float32, device="cuda")
+    for i in range(args.warmup):
+        tq2.tq2_gemm(ws[i % c], x, None, out, p.m, p.n, p.k)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        tq2.tq2_gemm(ws[i % c], x, None, out, p.m, p.n, p.k)
+    e1.record()
+    torch.cuda.synchronize()
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    t = e0.elapsed_time(e1) / 1e3 / max(args.steps, 1)
+    return {"workload": f"skinny_m{m}_k4096_n4096", "kernel": tq2.KERNEL_NAMES[tq2.tq2_select_kernel(p.m, p.n, p.k)],
+            "steps": args.steps, "warmup": args.warmup, "us_per_call": round(t * 1e6, 2),
+            "weight_GBps": round(wb / t / 1e9, 1), "copies": c}
+
+
 def run_suite(args):
     import torch
     import oracle
@@ -782,6 +817,9 @@ def main():
         return
     if args.attention:
         print(json.dumps(run_attention_only(args)), flush=True)
+        return
+    if args.skinny:
+        print(json.dumps(run_skinny_only(args)), flush=True)
         return
     if args.cpu_configs:
         print(json.dumps(run_cpu_configs()), flush=True)
