@@ -83,12 +83,6 @@ __device__ __forceinline__ uint32_t sk_mapa(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ float sk_ld_dsmem(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
-
 // D += A * B, m16n8k16, f16 inputs, f32 accumulation.
 __device__ __forceinline__ void mma16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
@@ -122,7 +116,7 @@ skinny_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__rest
     __half *xs = reinterpret_cast<__half *>(base + P.off_x);     // [mpad][xstride] binary16, activation order
     float *dsm = reinterpret_cast<float *>(base + P.off_d);      // [SK_ROWS][nbs_max] block scales
     float *bsm = reinterpret_cast<float *>(base + P.off_bias);   // [nbs_max][mpad] bias sums
-    float *part = reinterpret_cast<float *>(base + P.off_part);  // [mpad][SK_ROWS + pad] partial sums
+    float *part = reinterpret_cast<float *>(base + P.off_part);  // receive buffer [S][mpad][SK_ROWS / S]
     uint64_t *bar = reinterpret_cast<uint64_t *>(base + P.off_bar);
 
     if (tid == 0) {
@@ -151,51 +145,80 @@ skinny_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__rest
             sk_tma_2d(smem_u32(base) + uint32_t(j) * SK_BOX_BYTES, &qmap, (b0 * kBlockW + j * SK_BOX_W) / 4, row0,
                       bar);
     }
-    // x slice -> binary16 in the activation order (rows past M are zero); one
-    // item = one 16-element group of one row: four 16-byte loads, two 16-byte stores
+    // x slice -> binary16 in the activation order (rows past M are zero), and
+    // the block scales of the tile's rows (rows past N: 0).  Every load of a
+    // round is issued before any of it is used: the loads' latency is paid once
+    // per round, not once per item.
     {
         const int groups = kslice / 16;
         const int k0 = b0 * kBlockW;
-        for (int it = tid; it < P.mpad * groups; it += SK_THREADS) {
-            const int nrow = it / groups, gi = it - nrow * groups;
-            float f[16];
-            if (nrow < P.M) {
-                const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(nrow) * P.K + k0 + 16 * gi);
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 v = __ldg(src + q);
-                    f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] = 0.f;
-            }
-            uint32_t h[8];
-            float bsum = 0.f;  // this group's share of sum (bias + 1) * x16 over its block
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const __half2 v = __floats2half2_rn(f[i], f[i + 8]);  // positions 2i, 2i+1
-                h[i] = *reinterpret_cast<const uint32_t *>(&v);
-                const float2 r = __half22float2(v);
-                bsum = fmaf(sk_pos_bias(2 * i) + 1.0f, r.x + r.y, bsum);
-            }
-            uint4 *dst = reinterpret_cast<uint4 *>(xs + int64_t(nrow) * P.xstride + 16 * gi);
-            dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
-            dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
-            // the 8 groups of a block sit in 8 consecutive lanes (groups per
-            // row and the thread stride are multiples of 8): a fixed-order sum
-            bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
-            bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
-            bsum += __shfl_xor_sync(0xffffffffu, bsum, 4);
-            if ((gi & 7) == 0) bsm[(gi >> 3) * P.mpad + nrow] = bsum;
-        }
-        // block scales of the tile's rows (rows past N: 0)
         const int kb = P.nb;
-        for (int it = tid; it < SK_ROWS * nbs; it += SK_THREADS) {
-            const int r = it / nbs, b = it - r * nbs;
-            const int grow = row0 + r;
-            dsm[r * P.nbs_max + b] =
-                grow < P.N ? __half2float(__ushort_as_half(ldg_u16(dpl + int64_t(grow) * kb + b0 + b))) : 0.f;
+        const int nx = P.mpad * groups, nd = SK_ROWS * nbs;
+        // x items (one 16-element group of one row) two per thread and round,
+        // block scales four per thread and round; the item count of x is a
+        // multiple of 64, so every round is warp-uniform for the shuffles below
+        for (int r0 = 0; r0 < nx || r0 < nd; r0 += 4 * SK_THREADS) {
+            unsigned short dv[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int it = r0 + j * SK_THREADS + tid;
+                const int r = it / nbs, b = it - r * nbs;
+                dv[j] = (it < nd && row0 + r < P.N) ? ldg_u16(dpl + int64_t(row0 + r) * kb + b0 + b) : 0;
+            }
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                const int xb = r0 + half * 2 * SK_THREADS;
+                if (xb >= nx) break;  // warp-uniform (nx % 64 == 0)
+                float f[2][16];
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int it = xb + j * SK_THREADS + tid;
+                    const int nrow = it / groups, gi = it - nrow * groups;
+                    if (it < nx && nrow < P.M) {
+                        const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(nrow) * P.K + k0 + 16 * gi);
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq) {
+                            const float4 v = __ldg(src + qq);
+                            f[j][4 * qq] = v.x; f[j][4 * qq + 1] = v.y; f[j][4 * qq + 2] = v.z; f[j][4 * qq + 3] = v.w;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) f[j][i] = 0.f;
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int it = xb + j * SK_THREADS + tid;
+                    if (it >= nx) break;  // warp-uniform
+                    const int nrow = it / groups, gi = it - nrow * groups;
+                    uint32_t h[8];
+                    float bsum = 0.f;  // this group's share of sum (bias + 1) * x16 over its block
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const __half2 v = __floats2half2_rn(f[j][i], f[j][i + 8]);  // positions 2i, 2i+1
+                        h[i] = *reinterpret_cast<const uint32_t *>(&v);
+                        const float2 rr = __half22float2(v);
+                        bsum = fmaf(sk_pos_bias(2 * i) + 1.0f, rr.x + rr.y, bsum);
+                    }
+                    uint4 *dst = reinterpret_cast<uint4 *>(xs + int64_t(nrow) * P.xstride + 16 * gi);
+                    dst[0] = make_uint4(h[0], h[1], h[2], h[3]);
+                    dst[1] = make_uint4(h[4], h[5], h[6], h[7]);
+                    // the 8 groups of a block sit in 8 consecutive lanes (groups per
+                    // row and the thread stride are multiples of 8): a fixed-order sum
+                    bsum += __shfl_xor_sync(0xffffffffu, bsum, 1);
+                    bsum += __shfl_xor_sync(0xffffffffu, bsum, 2);
+                    bsum += __shfl_xor_sync(0xffffffffu, bsum, 4);
+                    if ((gi & 7) == 0) bsm[(gi >> 3) * P.mpad + nrow] = bsum;
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int it = r0 + j * SK_THREADS + tid;
+                if (it < nd) {
+                    const int r = it / nbs, b = it - r * nbs;
+                    dsm[r * P.nbs_max + b] = __half2float(__ushort_as_half(dv[j]));
+                }
+            }
         }
     }
     __syncthreads();
@@ -217,13 +240,17 @@ skinny_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__rest
         const __half *xrow[NT];
 #pragma unroll
         for (int t = 0; t < NT; ++t) xrow[t] = xs + int64_t(t * 8 + g) * P.xstride + 2 * q;
+        // independent accumulator chains per n-tile (k16-step mod CH) hide the
+        // MMA latency: four when there are one or two n-tiles, else two
+        constexpr int CH = NT <= 2 ? 4 : 2;
         for (int b = 0; b < nbs; ++b) {
-            // two accumulator chains per n-tile (even and odd code words) for MMA latency
-            float ce[NT][4], co[NT][4];
+            float cc[CH][NT][4];
 #pragma unroll
-            for (int t = 0; t < NT; ++t)
+            for (int h = 0; h < CH; ++h)
 #pragma unroll
-                for (int j = 0; j < 4; ++j) ce[t][j] = co[t][j] = 0.f;
+                for (int t = 0; t < NT; ++t)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) cc[h][t][j] = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
                 // 16 bytes (four code words) of rows ra and rb: chunk c of box j
@@ -245,10 +272,7 @@ skinny_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__rest
                     for (int t = 0; t < NT; ++t) {
                         const uint32_t bb0 = *reinterpret_cast<const uint32_t *>(xrow[t] + kx);
                         const uint32_t bb1 = *reinterpret_cast<const uint32_t *>(xrow[t] + kx + 8);
-                        if (u & 1)
-                            mma16816(co[t], a, bb0, bb1);
-                        else
-                            mma16816(ce[t], a, bb0, bb1);
+                        mma16816(cc[(h * 4 + u) % CH][t], a, bb0, bb1);
                     }
                 }
             }
@@ -256,43 +280,55 @@ skinny_mma_kernel(const __grid_constant__ CUtensorMap qmap, const __half *__rest
             const float da = dsm[ra * P.nbs_max + b], db = dsm[rb * P.nbs_max + b];
 #pragma unroll
             for (int t = 0; t < NT; ++t) {
+                float sm[4];
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    float v = cc[0][t][jj];
+#pragma unroll
+                    for (int hh = 1; hh < CH; ++hh) v += cc[hh][t][jj];
+                    sm[jj] = v;
+                }
                 const float2 bs = *reinterpret_cast<const float2 *>(bsm + b * P.mpad + t * 8 + 2 * q);
-                acc[t][0] = fmaf(da, (ce[t][0] + co[t][0]) - bs.x, acc[t][0]);
-                acc[t][1] = fmaf(da, (ce[t][1] + co[t][1]) - bs.y, acc[t][1]);
-                acc[t][2] = fmaf(db, (ce[t][2] + co[t][2]) - bs.x, acc[t][2]);
-                acc[t][3] = fmaf(db, (ce[t][3] + co[t][3]) - bs.y, acc[t][3]);
+                acc[t][0] = fmaf(da, sm[0] - bs.x, acc[t][0]);
+                acc[t][1] = fmaf(da, sm[1] - bs.y, acc[t][1]);
+                acc[t][2] = fmaf(db, sm[2] - bs.x, acc[t][2]);
+                acc[t][3] = fmaf(db, sm[3] - bs.y, acc[t][3]);
             }
         }
     }
-    // partial sums of the tile: part[x row][tile row]
-    const int pstride = SK_ROWS + SK_PART_PAD;
+    // Reduction over the S CTAs of the tile.  CTA r finishes tile rows
+    // [r * rpr, (r + 1) * rpr): every CTA pushes its partial sums of those
+    // rows into CTA r's receive buffer (slot = the sender's rank) with
+    // distributed-shared-memory stores, one cluster barrier makes them
+    // visible, and each CTA sums its slots in rank order (+ residual).  Nothing
+    // is read from another CTA after the barrier, so no second one is needed.
+    const int rpr = SK_ROWS / S;
+    const uint32_t part_addr = smem_u32(part);
+    auto push = [&](int row, int n, float v) {
+        const int o = row / rpr, rl = row - o * rpr;
+        const uint32_t off = uint32_t(((rank * P.mpad + n) * rpr + rl) * 4);
+        asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(sk_mapa(part_addr + off, uint32_t(o))), "f"(v)
+                     : "memory");
+    };
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
         const int n0 = t * 8 + 2 * q;
-        part[n0 * pstride + ra] = acc[t][0];
-        part[(n0 + 1) * pstride + ra] = acc[t][1];
-        part[n0 * pstride + rb] = acc[t][2];
-        part[(n0 + 1) * pstride + rb] = acc[t][3];
+        push(ra, n0, acc[t][0]);
+        push(ra, n0 + 1, acc[t][1]);
+        push(rb, n0, acc[t][2]);
+        push(rb, n0 + 1, acc[t][3]);
     }
-    // every CTA of the cluster has its partials in place
     sk_cluster_sync();
-    // this CTA finishes rows [rank * rpr, (rank + 1) * rpr) of the tile: the sum
-    // over the S slices in rank order (+ residual)
-    const int rpr = SK_ROWS / S;
-    const uint32_t part_addr = smem_u32(part);
     for (int it = tid; it < P.M * rpr; it += SK_THREADS) {
-        const int nrow = it / rpr, r = rank * rpr + (it - nrow * rpr);
-        const int grow = row0 + r;
+        const int nrow = it / rpr, rl = it - nrow * rpr;
+        const int grow = row0 + rank * rpr + rl;
         if (grow >= P.N) continue;
-        const uint32_t off = uint32_t((nrow * pstride + r) * 4);
         float sum = 0.f;
-        for (int s = 0; s < S; ++s) sum += sk_ld_dsmem(sk_mapa(part_addr + off, uint32_t(s)));
+        for (int sr = 0; sr < S; ++sr) sum += part[(sr * P.mpad + nrow) * rpr + rl];
         const int64_t o = int64_t(nrow) * P.N + grow;
         if (residual) sum += residual[o];
         out[o] = sum;
     }
-    // no CTA leaves while another may still read its partials
-    sk_cluster_sync();
     if (!ok && tid == 0) {
         // the code copies never completed: give them a fixed 200 us to land
         // before the CTA's shared memory goes away
@@ -341,6 +377,7 @@ cudaError_t launch_skinny_mma(const void *w_soa, const float *x, const float *re
     while (S < 8 && 2 * S <= nb && tiles * 2 * S <= ctx.num_sms) S *= 2;
     while (S < 8 && 2 * S <= nb && smem_for(S) > SK_SMEM_BUDGET) S *= 2;
     if (smem_for(S) > SK_SMEM_BUDGET) return cudaErrorNotSupported;
+
     SkParams P;
     P.M = int(m);
     P.N = int(n);
