@@ -231,12 +231,11 @@ cudaError_t launch_tpl(const void *w_soa, const float *x, const float *residual,
 
 constexpr int kGvLaneW = 32;                 // weights per lane: a quarter of a 128-weight block
 constexpr int kGvChunk = 32 * kGvLaneW;      // weights per warp-chunk (1024)
-// Consumer warps per CTA: up to 12 (three per scheduler, 72 registers per
-// thread for two CTAs per SM) or, for shapes with at least four groups of
-// chunk warps (K <= 4096), 16 (four per scheduler, 56 registers): measured
-// 7.07 -> 6.86 us at K=4096, N=12288 and 3.80 -> 3.62 us at K=N=4096.
+// Consumer warps per CTA: up to 12 (three per scheduler, up to 72 registers
+// per thread with two CTAs per SM).  With 16 (56 registers) the per-row code
+// spends more instructions on register moves: 6.67 vs 6.51 us at K=4096,
+// N=12288.
 constexpr int kGvMaxConsumers = 12;
-constexpr int kGvWideConsumers = 16;
 
 // ---------------------------------------------------------------------------
 // M = 1 decode GEMV (K <= 12288): bulk-copy streaming + integer dot products.
@@ -670,8 +669,7 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.C = C;
     P.swiglu = swiglu ? 1 : 0;
     P.f = int(n / 2);
-    const bool wide = kGvWideConsumers / C >= 4;  // four or more groups: the 16-warp kernel
-    P.groups = std::max(1, (wide ? kGvWideConsumers : kGvMaxConsumers) / C);  // groups of C warps (one per chunk)
+    P.groups = std::max(1, kGvMaxConsumers / C);  // groups of C warps (one per chunk)
     // the CTAs split the rows (with swiglu: the features, two rows each)
     const int64_t units = swiglu ? n / 2 : n;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + 7) / 8));
@@ -737,8 +735,7 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     void (*kern)(const CUtensorMap, const uint8_t *, const __half *, const float *, float *, GvsParams,
                  unsigned int *, uint64_t) = nullptr;
 #define TQ2_GV_KERN(RSV)                                                                                    \
-    kern = wide ? (dbulk ? gemv_stream_kernel<RSV, true, kGvWideConsumers> : gemv_stream_kernel<RSV, false, kGvWideConsumers>) \
-                : (dbulk ? gemv_stream_kernel<RSV, true, kGvMaxConsumers> : gemv_stream_kernel<RSV, false, kGvMaxConsumers>)
+    kern = dbulk ? gemv_stream_kernel<RSV, true, kGvMaxConsumers> : gemv_stream_kernel<RSV, false, kGvMaxConsumers>
     switch (P.rs) {
         case 2: TQ2_GV_KERN(2); break;
         case 3: TQ2_GV_KERN(3); break;
