@@ -259,41 +259,66 @@ __device__ __forceinline__ void decode_word(uint32_t w, __half2 d2, uint32_t (&o
 }
 
 // --------------------------------------------------------------------------
-// Pre-pass: x f32 [M,K] -> f16 MMA tiles.  Item = (row, 16-float group).
+// Pre-pass: x f32 [M,K] -> f16 MMA tiles.  Item = (row, 16-float group).  A
+// thread converts kPrepassItems items, all loaded before any is stored; the
+// grid is sized so that its blocks are resident together.  Block b also asks
+// L2 for slice b of the weight planes, which the tensor kernel behind this one
+// reads from its first stage on.
+constexpr int kPrepassItems = 2;
+constexpr int kPrepassThreads = 256;
 
-__global__ void __launch_bounds__(256)
-x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, int K, int MT) {
+__global__ void __launch_bounds__(kPrepassThreads)
+x_to_tiles_kernel(const float *__restrict__ x, uint8_t *__restrict__ ws, int M, int K, int MT,
+                  const uint8_t *__restrict__ w, int64_t wbytes) {
     // the tensor-core kernel behind this one may launch now: it waits for this
     // kernel's completion before it reads a tile
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (threadIdx.x == 0) {
+        // L2 is the point of coherence: a prefetch cannot leave stale data behind
+        const int64_t chunk = ((wbytes + gridDim.x - 1) / gridDim.x + 15) & ~int64_t(15);
+        const int64_t b0 = int64_t(blockIdx.x) * chunk;
+        const int64_t len = (b0 < wbytes ? (wbytes - b0 < chunk ? wbytes - b0 : chunk) : 0) & ~int64_t(15);
+        if (len > 0)
+            asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w + b0), "r"(uint32_t(len)) : "memory");
+    }
     const int groups = K / 16;                 // 16-float groups per row
     const int KT = K / BK;
     const int64_t items = int64_t(MT) * BM * groups;
-    for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < items;
-         it += int64_t(gridDim.x) * blockDim.x) {
-        const int row = int(it / groups), g = int(it % groups);
-        float f[16];
-        if (row < M) {
-            const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(row) * K + 16 * g);
+    const int64_t nth = int64_t(gridDim.x) * blockDim.x;
+    for (int64_t it0 = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it0 < items; it0 += kPrepassItems * nth) {
+        float f[kPrepassItems][16];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const float4 v = __ldg(src + q);
-                f[4 * q] = v.x; f[4 * q + 1] = v.y; f[4 * q + 2] = v.z; f[4 * q + 3] = v.w;
+        for (int u = 0; u < kPrepassItems; ++u) {
+            const int64_t it = it0 + u * nth;
+            const int row = int(it / groups), g = int(it % groups);
+            if (it < items && row < M) {
+                const float4 *src = reinterpret_cast<const float4 *>(x + int64_t(row) * K + 16 * g);
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const float4 v = __ldg(src + q);
+                    f[u][4 * q] = v.x; f[u][4 * q + 1] = v.y; f[u][4 * q + 2] = v.z; f[u][4 * q + 3] = v.w;
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[u][i] = 0.f;
             }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) f[i] = 0.f;
         }
-        const int mt = row / BM, r = row % BM, kt = g / 4, q = g % 4;
-        uint8_t *tile = ws + (int64_t(mt) * KT + kt) * A_BYTES;
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint4 v;
-            v.x = h2u(__floats2half2_rn(f[4 * h + 0], f[8 + 4 * h + 0]));
-            v.y = h2u(__floats2half2_rn(f[4 * h + 1], f[8 + 4 * h + 1]));
-            v.z = h2u(__floats2half2_rn(f[4 * h + 2], f[8 + 4 * h + 2]));
-            v.w = h2u(__floats2half2_rn(f[4 * h + 3], f[8 + 4 * h + 3]));
-            *reinterpret_cast<uint4 *>(tile + sw128_off(r, 2 * q + h)) = v;
+        for (int u = 0; u < kPrepassItems; ++u) {
+            const int64_t it = it0 + u * nth;
+            if (it >= items) break;
+            const int row = int(it / groups), g = int(it % groups);
+            const int mt = row / BM, r = row % BM, kt = g / 4, q = g % 4;
+            uint8_t *tile = ws + (int64_t(mt) * KT + kt) * A_BYTES;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 v;
+                v.x = h2u(__floats2half2_rn(f[u][4 * h + 0], f[u][8 + 4 * h + 0]));
+                v.y = h2u(__floats2half2_rn(f[u][4 * h + 1], f[u][8 + 4 * h + 1]));
+                v.z = h2u(__floats2half2_rn(f[u][4 * h + 2], f[u][8 + 4 * h + 2]));
+                v.w = h2u(__floats2half2_rn(f[u][4 * h + 3], f[u][8 + 4 * h + 3]));
+                *reinterpret_cast<uint4 *>(tile + sw128_off(r, 2 * q + h)) = v;
+            }
         }
     }
 }
@@ -406,7 +431,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                     const int s = int(g % depth);
                     const int u = int(g / depth);
                     uint64_t *freed = codes ? &ctl->codes_empty[s] : &ctl->empty[s];
-                    if (u > 0 && !mbar_wait_bounded(freed, (u - 1) & 1, wait_ns, status)) {
+                    if (u > 0 && !mbar_wait_spin(freed, (u - 1) & 1, wait_ns, status)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -462,6 +487,9 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
         }
         __syncwarp();
     } else if (warp == MMA_WARP) {
+        // The single-thread roles (this issuer and the two copy issuers) wait
+        // by spinning: the suspend-hinted wait wakes them measurably late
+        // (0.5 us per call at M=1536, N=3072; 1.4 us at N=12288).
         if (lane == 0) {
             int64_t g = 0;
             int i = 0;
@@ -470,7 +498,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 const int nk = item(t).nk;
                 const int a = i & 1;
                 // accumulator a was last used by tile i - 2: wait for its epilogue
-                if (i >= 2 && !mbar_wait_bounded(&ctl->tmem_empty[a], ((i >> 1) - 1) & 1, wait_ns, status)) {
+                if (i >= 2 && !mbar_wait_spin(&ctl->tmem_empty[a], ((i >> 1) - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -479,7 +507,7 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
                 for (int j = 0; j < nk; ++j, ++g) {
                     const int s = int(g % STAGES);
                     const uint32_t par = uint32_t(g / STAGES) & 1;
-                    if (!mbar_wait_bounded(&ctl->full[s], par, wait_ns, status)) {
+                    if (!mbar_wait_spin(&ctl->full[s], par, wait_ns, status)) {
                         *abort_flag = 1;
                         ok = false;
                         break;
@@ -958,9 +986,11 @@ cudaError_t launch_tc_ws_mode(const void *w_soa, const TcIo &io, int64_t m, int6
         // pre-pass: f32 x -> binary16 MMA tiles in the workspace
         const int MT = int((m + BM - 1) / BM);
         const int64_t items = int64_t(MT) * BM * (k / 16);
-        const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
-        x_to_tiles_kernel<<<unsigned(pgrid), 256, 0, ctx.stream>>>(io.x, static_cast<uint8_t *>(ws), int(m),
-                                                                   int(k), MT);
+        const int64_t per_block = int64_t(kPrepassThreads) * kPrepassItems;
+        const int64_t pgrid = std::min<int64_t>((items + per_block - 1) / per_block, int64_t(ctx.num_sms) * 4);
+        const int64_t wbytes = n * (k / kBlockW) * (kQsBytes + 2);  // code and scale planes
+        x_to_tiles_kernel<<<unsigned(pgrid), kPrepassThreads, 0, ctx.stream>>>(
+            io.x, static_cast<uint8_t *>(ws), int(m), int(k), MT, static_cast<const uint8_t *>(w_soa), wbytes);
         e = cudaPeekAtLastError();
         if (e != cudaSuccess) return e;
     }

@@ -185,9 +185,9 @@ __device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, u
         if (ok) return true;
         if ((it & 63u) == 0) {
             const uint64_t t = globaltimer_ns();
-            if (it == 0) {
-                t0 = t;
-            } else if (t - t0 >= limit_ns) {
+            if (it == 0) t0 = t;
+            // (a zero limit gives up at the first poll that finds the phase open)
+            if (t - t0 >= limit_ns) {
                 atomicOr(status, static_cast<unsigned int>(TQ2_ERR_TIMEOUT));
                 return false;
             }
