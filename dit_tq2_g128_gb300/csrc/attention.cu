@@ -14,17 +14,31 @@
 //    ([H, D, Sp]); Sp = S rounded up to 128, padding zero.  All three are
 //    then K-major MMA operands loaded by tensor copies with the 128-byte
 //    swizzle.
-//  * One CTA per (head, 128 queries); keys in blocks of 128.  Warp 0 copies
-//    Q once and K, V^T tiles through two-stage rings; warp 1 issues the MMAs:
-//    S_j = Q K_j^T (M=128, N=128, K=D) into one of two TMEM score buffers,
-//    then O += P_{j-1} V_{j-1} (M=128, N=D, K=128) into the TMEM output, so
-//    the next scores are computed while the softmax works.  Warps 4-7 (one
-//    thread per query row = TMEM lane) read a score row, take the row maximum
-//    over the valid keys, write P = 2^(s - m) as binary16 into shared memory
-//    (the A operand of P V) and keep the running sum l.
-//  * Lazy rescale: the running maximum m changes (and O and l are rescaled by
-//    2^(m_old - m_new)) only when a block's maximum exceeds m by more than 8,
-//    so P <= 2^8 always fits binary16 and the rescale is rare.
+//  * One CTA per (head, 256 queries) = two query tiles of 128 that share every
+//    K and V^T tile they copy (each copied tile feeds twice the MMA work of a
+//    one-tile CTA: the SM's L2 -> shared-memory bandwidth, not the tensor
+//    core, paced the one-tile form).  Warp 0 copies Q once and K, V^T through
+//    two-stage rings; warp 1 issues the MMAs (the whole warp waits and
+//    computes the descriptors, lane 0 issues); warps 4-7 run the softmax of
+//    tile 0 and warps 8-11 that of tile 1 (one thread per query row = TMEM
+//    lane).
+//  * Tensor memory: the scores S_t of tile t at columns 128 t, its output O_t
+//    at 256 + 128 t.  The softmax reads S_t and writes P_t = 2^(S_t - m) as
+//    binary16 over the first 64 columns of S_t; P_t V is then an MMA whose A
+//    operand is read from tensor memory (lane = query, column c = keys 2c,
+//    2c + 1), so P never passes through shared memory.
+//  * MMA order per key block j: P_0 V_j, S_0 of block j + 1, P_1 V_j, S_1 of
+//    block j + 1.  Tile 0's softmax of block j + 1 overlaps P_1 V_j and S_1;
+//    tile 1's overlaps the next P_0 V and S_0.  MMAs of one thread execute in
+//    issue order, so S_t of block j + 1 overwrites P_t only after P_t V_j has
+//    read it.
+//  * Softmax per block: the row maximum over the valid keys first, then
+//    P = 2^(s - mu).  Lazy rescale: the running maximum mu changes (and O and
+//    l are rescaled by 2^(m_old - m_new)) only when a block's maximum exceeds
+//    it by more than 8, so P <= 2^8 always fits binary16 and the rescale is
+//    rare.  (Measured alternatives: two threads per row, one pass with P held
+//    in registers, part of the exponentials by a polynomial on the FMA pipe:
+//    all slower at the DiT shape.)
 //  * Epilogue: out = O / l, f32.
 // Every wait is bounded; a timeout sets the device status word and the CTA
 // drains and exits.
@@ -37,22 +51,24 @@
 namespace tq2 {
 namespace {
 
-constexpr int AQ = 128;        // queries per CTA (MMA M)
+constexpr int AQ = 128;        // queries per tile (MMA M)
+constexpr int AQT = 2;         // query tiles per CTA
 constexpr int AKB = 128;       // keys per block
-constexpr int ATHREADS = 256;  // warp 0 copies, warp 1 MMA + TMEM, warps 4-7 softmax
+constexpr int ATHREADS = 384;  // warp 0 copies, warp 1 MMA + TMEM, warps 4-7 / 8-11 softmax of tile 0 / 1
+constexpr int A_SMT = AQ;      // softmax threads per tile (one per query row)
 constexpr int A_TMA = 0, A_MMA = 1, A_SM0 = 4;
 constexpr float kLazyLog2 = 8.0f;
-constexpr uint32_t ATMEM_COLS = 512;  // S buffers at 0 and 128, O at 256
+constexpr uint32_t ATMEM_COLS = 512;  // S/P of tile t at 128 t, O of tile t at 256 + 128 t
+constexpr uint32_t A_OCOL = 256;
 
 template <int D>
 struct AttnLayout {
     static constexpr int SUB = 128 * 128;            // one swizzled 128-row x 64-element sub-tile
-    static constexpr int QB = AQ * D * 2;            // Q tile
+    static constexpr int QB = AQ * D * 2;            // one Q tile
     static constexpr int KB = AKB * D * 2;           // one K tile
     static constexpr int VB = D * AKB * 2;           // one V^T tile (D rows x 128 keys)
-    static constexpr int PB = AQ * AKB * 2;          // P tile
-    static constexpr int OFF_K = QB, OFF_V = OFF_K + 2 * KB, OFF_P = OFF_V + 2 * VB;
-    static constexpr int OFF_CTL = OFF_P + 2 * PB;   // two P buffers
+    static constexpr int OFF_K = AQT * QB, OFF_V = OFF_K + 2 * KB;
+    static constexpr int OFF_CTL = OFF_V + 2 * VB;
     static constexpr int BYTES = OFF_CTL + 256 + 1024;  // barriers + alignment slack
     // f32 accumulator D, binary16 A and B, both K-major; N >> 3 at bit 17, M >> 4 at bit 24
     static constexpr uint32_t IDESC_S = (1u << 4) | (uint32_t(AKB >> 3) << 17) | (uint32_t(AQ >> 4) << 24);
@@ -62,8 +78,8 @@ struct AttnLayout {
 static_assert(AttnLayout<128>::BYTES <= 232448, "shared memory budget");
 
 struct AttnCtl {
-    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], s_empty[2];
-    uint64_t p_full[2], pv_done[2], drain;  // per P buffer (block j uses buffer j % 2)
+    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2];
+    uint64_t s_full[AQT], p_full[AQT], o_done[AQT], drain;  // per query tile
     uint32_t tmem_base;
     int abort;
 };
@@ -76,11 +92,6 @@ __device__ __forceinline__ uint64_t att_desc(uint32_t saddr) {
            (uint64_t(1) << 46) | (uint64_t(2) << 61);
 }
 
-// Byte offset of 16-byte chunk j of row r in a swizzled sub-tile.
-__device__ __forceinline__ uint32_t att_sw_off(int r, int j) {
-    return uint32_t((r >> 3) * 1024 + (r & 7) * 128 + ((j ^ (r & 7)) << 4));
-}
-
 __device__ __forceinline__ void att_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
                  : "memory");
@@ -91,6 +102,18 @@ __device__ __forceinline__ void att_tma_2d(uint32_t dst, const CUtensorMap *map,
         "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
         "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T, kind::f16: A is read from tensor memory
+// (128 lanes = rows, 32-bit column c = elements 2c, 2c + 1 of the row).
+__device__ __forceinline__ void att_mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
 
@@ -129,6 +152,7 @@ __device__ __forceinline__ float att_ex2(float x) {
     return y;
 }
 
+
 template <int D>
 __global__ void __launch_bounds__(ATHREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -141,9 +165,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     const uint32_t sbase = raw_addr + pad;
     AttnCtl *ctl = reinterpret_cast<AttnCtl *>(att_raw + pad + Lay::OFF_CTL);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int qb = blockIdx.x, h = blockIdx.y;
-    const int nb = (S + AKB - 1) / AKB;  // key blocks
-    const uint32_t sQ = sbase, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V, sP = sbase + Lay::OFF_P;
+    const int qp = blockIdx.x, h = blockIdx.y;  // queries AQT * AQ * qp .. + AQT * AQ - 1 of head h
+    const int nb = (S + AKB - 1) / AKB;         // key blocks
+    const uint32_t sQ = sbase, sK = sbase + Lay::OFF_K, sV = sbase + Lay::OFF_V;
 
     if (threadIdx.x == 0) {
         mbar_init(&ctl->q_full, 1);
@@ -152,13 +176,12 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             mbar_init(&ctl->k_empty[b], 1);
             mbar_init(&ctl->v_full[b], 1);
             mbar_init(&ctl->v_empty[b], 1);
-            mbar_init(&ctl->s_full[b], 1);
-            mbar_init(&ctl->s_empty[b], 128);
         }
-        mbar_init(&ctl->p_full[0], 128);
-        mbar_init(&ctl->p_full[1], 128);
-        mbar_init(&ctl->pv_done[0], 1);
-        mbar_init(&ctl->pv_done[1], 1);
+        for (int t = 0; t < AQT; ++t) {
+            mbar_init(&ctl->s_full[t], 1);
+            mbar_init(&ctl->p_full[t], A_SMT);
+            mbar_init(&ctl->o_done[t], 1);
+        }
         mbar_init(&ctl->drain, 1);
         ctl->abort = 0;
         fence_proxy_async_smem();
@@ -178,13 +201,17 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
-            att_expect_tx(&ctl->q_full, Lay::QB);
-            for (int sub = 0; sub < D / 64; ++sub)
-                att_tma_2d(sQ + sub * Lay::SUB, &qmap, sub * 64, h * Sp + qb * AQ, &ctl->q_full);
+            // both query tiles (a tile past the end of the head reads other
+            // rows or the fill value: its rows are computed, never written)
+            att_expect_tx(&ctl->q_full, AQT * Lay::QB);
+            for (int t = 0; t < AQT; ++t)
+                for (int sub = 0; sub < D / 64; ++sub)
+                    att_tma_2d(sQ + t * Lay::QB + sub * Lay::SUB, &qmap, sub * 64, h * Sp + (AQT * qp + t) * AQ,
+                               &ctl->q_full);
             int issued = 0;
             for (int j = 0; j < nb; ++j, ++issued) {
                 const int b = j & 1, u = j >> 1;
-                if (u > 0 && !mbar_wait_bounded(&ctl->k_empty[b], (u - 1) & 1, wait_ns, status)) {
+                if (u > 0 && !mbar_wait_spin(&ctl->k_empty[b], (u - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -192,7 +219,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 att_expect_tx(&ctl->k_full[b], Lay::KB);
                 for (int sub = 0; sub < D / 64; ++sub)
                     att_tma_2d(sK + b * Lay::KB + sub * Lay::SUB, &kmap, sub * 64, h * Sp + j * AKB, &ctl->k_full[b]);
-                if (u > 0 && !mbar_wait_bounded(&ctl->v_empty[b], (u - 1) & 1, wait_ns, status)) {
+                if (u > 0 && !mbar_wait_spin(&ctl->v_empty[b], (u - 1) & 1, wait_ns, status)) {
                     *abort_flag = 1;
                     break;
                 }
@@ -211,176 +238,177 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         }
         __syncwarp();
     } else if (warp == A_MMA) {
-        if (lane == 0) {
-            bool ok = mbar_wait_bounded(&ctl->q_full, 0, wait_ns, status);
-            if (!ok) *abort_flag = 1;
-            tc_fence_after();
-            for (int j = 0; j <= nb && ok; ++j) {
-                if (j < nb) {
-                    const int b = j & 1, u = j >> 1;
-                    if (!mbar_wait_bounded(&ctl->k_full[b], u & 1, wait_ns, status) ||
-                        (u > 0 && !mbar_wait_bounded(&ctl->s_empty[b], (u - 1) & 1, wait_ns, status))) {
-                        *abort_flag = 1;
-                        break;
-                    }
-                    if (*abort_flag) break;
-                    tc_fence_after();
+        // The whole warp runs the loop (waits, descriptors); lane 0 issues.
+        // Descriptor of a shared-memory operand + byte offset d: the 16-byte
+        // address field is the low 14 bits and never carries out here.
+        const uint64_t dq0 = att_desc(sQ), dq1 = att_desc(sQ + Lay::QB);
+        const uint64_t dk0 = att_desc(sK), dk1 = att_desc(sK + Lay::KB);
+        const uint64_t dv0 = att_desc(sV), dv1 = att_desc(sV + Lay::VB);
+        const bool leader = lane == 0;
+        // waits by the whole warp, with one verdict for all lanes
+        auto wait_all = [&](uint64_t *bar, uint32_t parity) {
+            const bool got = mbar_wait_spin(bar, parity, wait_ns, status);
+            return __all_sync(0xffffffffu, got && *abort_flag == 0);
+        };
+        // S_t of block j into columns 128 t (A = Q_t, B = K_j from shared memory)
+        auto issue_s = [&](int t, int j) {
+            const uint64_t a0 = t ? dq1 : dq0, b0 = (j & 1) ? dk1 : dk0;
+            if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        tc_mma_f16(tmem + uint32_t(b * AKB),
-                                   att_desc(sQ + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
-                                   att_desc(sK + b * Lay::KB + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
-                                   Lay::IDESC_S, kk > 0);
-                    tc_commit(&ctl->s_full[b]);
-                    tc_commit(&ctl->k_empty[b]);
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t off = uint64_t((((kk >> 2) * Lay::SUB) >> 4) + 2 * (kk & 3));
+                    tc_mma_f16(tmem + uint32_t(t * AKB), a0 + off, b0 + off, Lay::IDESC_S, kk > 0);
                 }
-                if (j > 0) {
-                    const int jj = j - 1, bb = jj & 1, uu = jj >> 1;
-                    if (!mbar_wait_bounded(&ctl->p_full[bb], uu & 1, wait_ns, status) ||
-                        !mbar_wait_bounded(&ctl->v_full[bb], uu & 1, wait_ns, status)) {
-                        *abort_flag = 1;
+                tc_commit(&ctl->s_full[t]);
+            }
+            __syncwarp();
+        };
+        // O_t += P_t V_j (A = P_t from tensor memory, B = V_j^T from shared memory)
+        auto issue_pv = [&](int t, int j) {
+            const uint64_t b0 = (j & 1) ? dv1 : dv0;
+            if (leader) {
+#pragma unroll
+                for (int kk = 0; kk < AKB / 16; ++kk)
+                    att_mma_ts(tmem + A_OCOL + uint32_t(t * AKB), tmem + uint32_t(t * AKB + 8 * kk),
+                               b0 + uint64_t((((kk >> 2) * (D * 128)) >> 4) + 2 * (kk & 3)), Lay::IDESC_O,
+                               (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(&ctl->o_done[t]);
+            }
+            __syncwarp();
+        };
+        auto commit = [&](uint64_t *bar) {
+            if (leader) tc_commit(bar);
+            __syncwarp();
+        };
+        bool ok = wait_all(&ctl->q_full, 0) && wait_all(&ctl->k_full[0], 0);
+        if (ok) {
+            tc_fence_after();
+            issue_s(0, 0);
+            issue_s(1, 0);
+            commit(&ctl->k_empty[0]);
+        }
+        for (int j = 0; j < nb && ok; ++j) {
+            const bool next = j + 1 < nb;
+            if (!wait_all(&ctl->v_full[j & 1], (j >> 1) & 1)) { ok = false; break; }
+            for (int t = 0; t < AQT && ok; ++t) {
+                // P_t of block j written by the softmax (which has also read S_t)
+                if (!wait_all(&ctl->p_full[t], j & 1)) { ok = false; break; }
+                tc_fence_after();
+                issue_pv(t, j);
+                if (t == AQT - 1) commit(&ctl->v_empty[j & 1]);
+                if (next) {
+                    if (t == 0 && !wait_all(&ctl->k_full[(j + 1) & 1], ((j + 1) >> 1) & 1)) {
+                        ok = false;
                         break;
                     }
-                    if (*abort_flag) break;
                     tc_fence_after();
-#pragma unroll
-                    for (int kk = 0; kk < AKB / 16; ++kk)
-                        tc_mma_f16(tmem + 2u * AKB, att_desc(sP + bb * Lay::PB + (kk >> 2) * Lay::SUB) + 2 * (kk & 3),
-                                   att_desc(sV + bb * Lay::VB + (kk >> 2) * (D * 128)) + 2 * (kk & 3),
-                                   Lay::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(&ctl->pv_done[bb]);
-                    tc_commit(&ctl->v_empty[bb]);
+                    issue_s(t, j + 1);
+                    if (t == AQT - 1) commit(&ctl->k_empty[(j + 1) & 1]);
                 }
             }
         }
+        if (!ok && leader) *abort_flag = 1;
         __syncwarp();
     } else if (warp >= A_SM0) {
-        const int quarter = warp - A_SM0;
+        const int t = (warp - A_SM0) >> 2;             // query tile
+        const int quarter = warp & 3;                  // TMEM lanes 32 quarter .. + 31
         const int r = quarter * 32 + lane;             // query row in the tile = TMEM lane
         const uint32_t tl = uint32_t(quarter * 32) << 16;
+        const uint32_t ts = tmem + tl + uint32_t(t * AKB);          // this row's S / P
+        const uint32_t to = tmem + tl + A_OCOL + uint32_t(t * AKB); // this row's O
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < nb; ++j) {
-            const int b = j & 1, u = j >> 1;
-            // S_j is ready, and P buffer b is free once P V of block j - 2 is done
-            if (!mbar_wait_bounded(&ctl->s_full[b], u & 1, wait_ns, status) ||
-                (j >= 2 && !mbar_wait_bounded(&ctl->pv_done[b], ((j - 2) >> 1) & 1, wait_ns, status)))
-                *abort_flag = 1;
+            if (!mbar_wait_spin(&ctl->s_full[t], j & 1, wait_ns, status)) *abort_flag = 1;
             if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t ts = tmem + tl + uint32_t(b * AKB);
-            const uint32_t pbuf = sP + uint32_t(b * Lay::PB);
             const int kvalid = S - j * AKB;  // keys of this block below S
-            // P = 2^(s - mu) in binary16, stored to P buffer b as it is made,
-            // and its f32 row sum, optionally tracking the block maximum.  The
-            // next pair of score chunks is read while the current one is
-            // processed.  For blocks after the first the pass is speculative
-            // with the running maximum mu = m, redone (once, same code) only if
-            // a row's block maximum exceeds m by more than 8.
-            float lsum = 0.f, mx = -INFINITY;
-            float mu = m;
-            bool track = j > 0, grow = true;
-            if (j == 0) {
+            // the row maximum over the valid keys
+            float mx = -INFINITY;
 #pragma unroll
-                for (int cp = 0; cp < AKB / 64; ++cp) {
-                    uint32_t va[32], vb[32];
-                    att_ld32(ts + uint32_t(cp * 64), va);
-                    att_ld32(ts + uint32_t(cp * 64 + 32), vb);
-                    tc_wait_ld();
+            for (int cp = 0; cp < AKB / 64; ++cp) {
+                uint32_t va[32], vb[32];
+                att_ld32(ts + uint32_t(cp * 64), va);
+                att_ld32(ts + uint32_t(cp * 64 + 32), vb);
+                tc_wait_ld();
+                if (kvalid >= AKB) {
 #pragma unroll
-                    for (int i = 0; i < 64; ++i)
-                        if (cp * 64 + i < kvalid) mx = fmaxf(mx, __uint_as_float(i < 32 ? va[i] : vb[i - 32]));
-                }
-                mu = mx;
-            }
-            // keys kb0 .. kb0 + 63 from the chunk pair (x0: first 32, x1: next 32)
-            auto half_pass = [&](const uint32_t (&x0)[32], const uint32_t (&x1)[32], int kb0) {
+                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(__uint_as_float(va[i]), __uint_as_float(vb[i])));
+                } else {
 #pragma unroll
-                for (int c8 = 0; c8 < 8; ++c8) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int i = c8 * 8 + 2 * e;  // 0..62
-                        const uint32_t u0 = i < 32 ? x0[i] : x1[i - 32], u1 = i < 32 ? x0[i + 1] : x1[i - 31];
-                        const int key = kb0 + i;
-                        const float s0 = key < kvalid ? __uint_as_float(u0) : -INFINITY;
-                        const float s1 = key + 1 < kvalid ? __uint_as_float(u1) : -INFINITY;
-                        if (track) mx = fmaxf(mx, fmaxf(s0, s1));
-                        const float p0 = att_ex2(s0 - mu), p1 = att_ex2(s1 - mu);
-                        lsum += p0 + p1;
-                        const __half2 hp = __floats2half2_rn(p0, p1);
-                        w[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                    for (int i = 0; i < 32; ++i) {
+                        if (cp * 64 + i < kvalid) mx = fmaxf(mx, __uint_as_float(va[i]));
+                        if (cp * 64 + 32 + i < kvalid) mx = fmaxf(mx, __uint_as_float(vb[i]));
                     }
-                    // keys kb0 + 8 c8 .. +7: 16-byte chunk c8 of sub-tile kb0 / 64, row r
-                    const uint32_t addr = pbuf + uint32_t((kb0 >> 6) * Lay::SUB) + att_sw_off(r, c8);
-                    asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(w[0]), "r"(w[1]),
-                                 "r"(w[2]), "r"(w[3])
-                                 : "memory");
                 }
-            };
-#pragma unroll 1
-            for (int pass = 0; pass < 2; ++pass) {
-                lsum = 0.f;
-                uint32_t a0[32], a1[32], b0[32], b1[32];
-                att_ld32(ts, a0);
-                att_ld32(ts + 32u, a1);
-                tc_wait_ld();
-                att_ld32(ts + 64u, b0);
-                att_ld32(ts + 96u, b1);
-                half_pass(a0, a1, 0);
-                tc_wait_ld();
-                half_pass(b0, b1, 64);
-                if (!track) break;
-                grow = mx > m + kLazyLog2;
-                if (!__any_sync(0xffffffffu, grow)) break;
-                mu = grow ? mx : m;
-                track = false;
             }
-            const float alpha = grow ? att_ex2(m - mu) : 1.f;
-            // this S buffer is read: the next-but-one block may overwrite it
-            tc_fence_before();
-            mbar_arrive(&ctl->s_empty[b]);
+            // lazy rescale: keep the running maximum unless this block's exceeds it by more than 8
+            const bool grow = j == 0 || mx > m + kLazyLog2;
+            const float mu = grow ? mx : m;
+            const float alpha = (j > 0 && grow) ? att_ex2(m - mu) : 1.f;
+            // P = 2^(s - mu) as binary16 over the first 64 columns of S (keys
+            // 64 cp .. 64 cp + 63 -> columns 32 cp .. 32 cp + 31, read before written)
+            float lsum = 0.f;
+#pragma unroll
+            for (int cp = 0; cp < AKB / 64; ++cp) {
+                uint32_t va[32], vb[32], w[32];
+                att_ld32(ts + uint32_t(cp * 64), va);
+                att_ld32(ts + uint32_t(cp * 64 + 32), vb);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int i = 2 * e;  // keys 64 cp + i, + i + 1
+                    float s0 = __uint_as_float(i < 32 ? va[i] : vb[i - 32]);
+                    float s1 = __uint_as_float(i < 32 ? va[i + 1] : vb[i - 31]);
+                    if (kvalid < AKB) {
+                        if (cp * 64 + i >= kvalid) s0 = -INFINITY;
+                        if (cp * 64 + i + 1 >= kvalid) s1 = -INFINITY;
+                    }
+                    const float p0 = att_ex2(s0 - mu), p1 = att_ex2(s1 - mu);
+                    lsum += p0 + p1;
+                    const __half2 hp = __floats2half2_rn(p0, p1);
+                    w[e] = *reinterpret_cast<const uint32_t *>(&hp);
+                }
+                att_st32(ts + uint32_t(cp * 32), w);
+            }
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // rescale this row of O (rows that keep m scale by 1) once
                 // P V of block j - 1 has accumulated into it
-                if (!mbar_wait_bounded(&ctl->pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, wait_ns, status))
-                    *abort_flag = 1;
+                if (!mbar_wait_spin(&ctl->o_done[t], (j - 1) & 1, wait_ns, status)) *abort_flag = 1;
                 if (__any_sync(0xffffffffu, *abort_flag != 0)) { ok = false; break; }
                 tc_fence_after();
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     uint32_t o[32];
-                    att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    att_ld32(to + uint32_t(c * 32), o);
                     tc_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    att_st32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    for (int q = 0; q < 32; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * alpha);
+                    att_st32(to + uint32_t(c * 32), o);
                 }
-                att_wait_st();
             }
             l = l * alpha + lsum;
             m = mu;
-            fence_proxy_async_smem();
+            att_wait_st();
             tc_fence_before();
-            mbar_arrive(&ctl->p_full[b]);
+            mbar_arrive(&ctl->p_full[t]);
         }
         if (ok) {
-            if (!mbar_wait_bounded(&ctl->pv_done[(nb - 1) & 1], ((nb - 1) >> 1) & 1, wait_ns, status))
-                *abort_flag = 1;
+            if (!mbar_wait_spin(&ctl->o_done[t], (nb - 1) & 1, wait_ns, status)) *abort_flag = 1;
             if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
                 tc_fence_after();
                 const float inv = 1.0f / l;
-                const int t = qb * AQ + r;
+                const int tok = (AQT * qp + t) * AQ + r;
                 // the head's Dout real features (the staged operands pad D to
                 // the kernel's width with zeros; those columns are not written)
-                float *orow = out + int64_t(t) * H * Dout + int64_t(h) * Dout;
+                float *orow = out + int64_t(tok) * H * Dout + int64_t(h) * Dout;
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
                     if (c * 32 >= Dout) break;
                     uint32_t o[32];
-                    att_ld32(tmem + tl + 2u * AKB + uint32_t(c * 32), o);
+                    att_ld32(to + uint32_t(c * 32), o);
                     tc_wait_ld();
-                    if (t < S) {
+                    if (tok < S) {
 #pragma unroll
                         for (int i = 0; i < 32; i += 4)
                             if (c * 32 + i < Dout)
@@ -508,7 +536,8 @@ cudaError_t launch_attention_d(const float *q, const float *k, const float *v, f
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<D><<<dim3(unsigned(Sp / AQ), unsigned(H)), ATHREADS, Lay::BYTES, ctx.stream>>>(
+    attn_fwd_kernel<D><<<dim3(unsigned((Sp / AQ + AQT - 1) / AQT), unsigned(H)), ATHREADS, Lay::BYTES,
+                         ctx.stream>>>(
         qmap, kmap, vmap, out, int(H), int(S), int(Sp), Din, ctx.status, ctx.wait_ns);
     return cudaPeekAtLastError();
 }

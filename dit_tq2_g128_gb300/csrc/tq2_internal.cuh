@@ -93,7 +93,7 @@ cudaError_t launch_tc_noalloc(const void *w_soa, const float *x, const float *re
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 
 // DiT joint attention: q, k, v head-major f32 [H, S, D] -> out token-major
-// f32 [S, H*D]; D in {64, 128}; ws: attention_ws_bytes (binary16 copies).
+// f32 [S, H*D]; D a multiple of 8 up to 128; ws: attention_ws_bytes (binary16 copies).
 size_t attention_ws_bytes(int64_t H, int64_t S, int64_t D);
 cudaError_t launch_attention(const float *q, const float *k, const float *v, float *out, int64_t H, int64_t S,
                              int64_t D, void *ws, const LaunchCtx &ctx);

@@ -723,6 +723,28 @@ def test_attention_dit_shape_sampled(tq2):
     check_attention(got, q, k, v, h, s, d, rows=sample_rows(s), what="attn dit")
 
 
+@pytest.mark.parametrize("d", [128, 64])
+def test_attention_wait_timeout_is_reported_and_context_survives(tq2, d):
+    # a zero wait limit makes the kernel's first open wait give up: every role
+    # (copies, MMA issue, the paired softmax warps) must leave without hanging,
+    # the timeout must reach the status word, and the next call must be exact
+    h, s = 2, 300
+    rng = np.random.default_rng(31 + d)
+    q, k, v = (rng.standard_normal((h, s, d)).astype(np.float32) for _ in range(3))
+    qd, kd, vd = (torch.from_numpy(a).cuda() for a in (q, k, v))
+    out = torch.zeros((s, h * d), dtype=torch.float32, device="cuda")
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    old = tq2.tq2_set_wait_timeout_ns(0)
+    try:
+        tq2.tq2_attention_f32(qd, kd, vd, out, h, s, d)
+        torch.cuda.synchronize()
+        st = tq2.tq2_device_status()
+    finally:
+        tq2.tq2_set_wait_timeout_ns(old)
+    assert st == tq2.TQ2_ERR_TIMEOUT
+    check_attention(run_attention(tq2, q, k, v, h, s, d), q, k, v, h, s, d, what="attn after timeout")
+
+
 def test_attention_errors(tq2):
     a = torch.zeros(2, 128, 128, device="cuda")
     o = torch.zeros(128, 256, device="cuda")
