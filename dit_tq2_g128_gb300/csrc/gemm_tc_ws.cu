@@ -598,6 +598,42 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             gbase += it.nk;
             if (__any_sync(0xffffffffu, stop || *abort_flag)) break;
         }
+        // The decoders then join the epilogue of the CTA's last tile (plain f32
+        // output): 20 warps instead of 4 drain its accumulator, five per TMEM
+        // lane quarter, chunk c of 32 columns to worker c % 5 (worker 0 is the
+        // epilogue warp).  With one tile per CTA (M=1536, N=3072) the epilogue
+        // is otherwise exposed: 4.0 -> 2.5 us.
+        {
+            const int cnt = cl < nitems ? (nitems - 1 - cl) / ncl + 1 : 0;
+            const bool wide = cnt > 0 && ksplit == 1 && (epi_mode == EPI_DIRECT || epi_mode == EPI_TMA_STORE);
+            if (wide && !__any_sync(0xffffffffu, *abort_flag != 0)) {
+                const int il = cnt - 1;
+                const Item it = item(cl + il * ncl);
+                const int a = il & 1;
+                const int quarter = warp & 3, worker = 1 + ((warp - DEC_WARP0) >> 2);
+                if (!mbar_wait_bounded(&ctl->tmem_full[a], (il >> 1) & 1, wait_ns, status)) *abort_flag = 1;
+                if (!__any_sync(0xffffffffu, *abort_flag != 0)) {
+                    tc_fence_after();
+                    const int col = it.nw * BW + quarter * 32 + lane;
+                    for (int c = worker; c < BX / 32; c += 5) {
+                        uint32_t r[32];
+                        tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + ACC_COL + uint32_t(a) * BX +
+                                      uint32_t(c * 32),
+                                  r);
+                        tc_wait_ld();
+                        const int row0 = it.mx * BX + c * 32;
+                        if (row0 < M && col < N) {
+                            const int nr = min(32, M - row0);  // rows of this block inside the output
+                            float *op = out + int64_t(row0) * N + col;
+                            const float *rp = residual ? residual + int64_t(row0) * N + col : nullptr;
+#pragma unroll
+                            for (int j = 0; j < 32; ++j)
+                                if (j < nr) op[int64_t(j) * N] = __uint_as_float(r[j]) + (rp ? rp[int64_t(j) * N] : 0.f);
+                        }
+                    }
+                }
+            }
+        }
     } else if (warp >= EPI_WARP0) {
         const int quarter = warp - EPI_WARP0;  // TMEM lanes 32*quarter .. +31 = output columns
         const uint32_t ebuf = ebase + uint32_t(quarter) * EPI_NB * EPI_BYTES;
@@ -636,7 +672,10 @@ tc_ws_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ C
             tc_fence_after();
             const int col0 = nw * BW + quarter * 32;
             const int col = col0 + lane;
-            for (int c = 0; c < BX / 32; ++c) {
+            // the last tile's chunks are shared with the decoder warps (above)
+            const int cnt = cl < nitems ? (nitems - 1 - cl) / ncl + 1 : 0;
+            const bool wide = i == cnt - 1 && ksplit == 1 && (epi_mode == EPI_DIRECT || epi_mode == EPI_TMA_STORE);
+            for (int c = 0; c < BX / 32; c += wide ? 5 : 1) {
                 uint32_t r[32];
                 tmem_ld32(tmem + (uint32_t(quarter * 32) << 16) + ACC_COL + uint32_t(a) * BX +
                               uint32_t(c * 32),
