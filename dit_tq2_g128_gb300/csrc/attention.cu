@@ -153,6 +153,29 @@ __device__ __forceinline__ float att_ex2(float x) {
 }
 
 
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf)
+__device__ __forceinline__ float att_max3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
+// Two f32 lanes in one 64-bit register, and their lane-wise sum (each lane
+// rounded as a scalar add).
+__device__ __forceinline__ uint64_t att_pack2(float a, float b) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void att_unpack2(uint64_t r, float &a, float &b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ uint64_t att_add2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 template <int D>
 __global__ void __launch_bounds__(ATHREADS, 1)
 attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
@@ -201,6 +224,10 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
             asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+            // Launched right behind the binary16 pre-pass (programmatic
+            // dependent launch): the set-up above overlapped its tail; its
+            // output is read only from here on.
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             // both query tiles (a tile past the end of the head reads other
             // rows or the fill value: its rows are computed, never written)
             att_expect_tx(&ctl->q_full, AQT * Lay::QB);
@@ -333,7 +360,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                 tc_wait_ld();
                 if (kvalid >= AKB) {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) mx = fmaxf(mx, fmaxf(__uint_as_float(va[i]), __uint_as_float(vb[i])));
+                    for (int i = 0; i < 32; ++i) mx = att_max3(mx, __uint_as_float(va[i]), __uint_as_float(vb[i]));
                 } else {
 #pragma unroll
                     for (int i = 0; i < 32; ++i) {
@@ -348,7 +375,9 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
             const float alpha = (j > 0 && grow) ? att_ex2(m - mu) : 1.f;
             // P = 2^(s - mu) as binary16 over the first 64 columns of S (keys
             // 64 cp .. 64 cp + 63 -> columns 32 cp .. 32 cp + 31, read before written)
-            float lsum = 0.f;
+            // (key pairs in packed f32x2 arithmetic: s - mu and the row sum)
+            const uint64_t negmu2 = att_pack2(-mu, -mu);
+            uint64_t lsum2 = att_pack2(0.f, 0.f);
 #pragma unroll
             for (int cp = 0; cp < AKB / 64; ++cp) {
                 uint32_t va[32], vb[32], w[32];
@@ -364,13 +393,18 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
                         if (cp * 64 + i >= kvalid) s0 = -INFINITY;
                         if (cp * 64 + i + 1 >= kvalid) s1 = -INFINITY;
                     }
-                    const float p0 = att_ex2(s0 - mu), p1 = att_ex2(s1 - mu);
-                    lsum += p0 + p1;
+                    float d0, d1;
+                    att_unpack2(att_add2(att_pack2(s0, s1), negmu2), d0, d1);
+                    const float p0 = att_ex2(d0), p1 = att_ex2(d1);
+                    lsum2 = att_add2(lsum2, att_pack2(p0, p1));
                     const __half2 hp = __floats2half2_rn(p0, p1);
                     w[e] = *reinterpret_cast<const uint32_t *>(&hp);
                 }
                 att_st32(ts + uint32_t(cp * 32), w);
             }
+            float lsum0, lsum1;
+            att_unpack2(lsum2, lsum0, lsum1);
+            const float lsum = lsum0 + lsum1;
             if (j > 0 && __any_sync(0xffffffffu, grow)) {
                 // rescale this row of O (rows that keep m scale by 1) once
                 // P V of block j - 1 has accumulated into it
@@ -436,64 +470,71 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
     }
 }
 
-// q, k [H][S][Din] -> binary16 [H][Sp][D] (blockIdx.y = 0: q times `qscale`;
-// 1: k), zero rows past S and zero features past Din; 8 elements per item.
+// The binary16 pre-pass in one launch, grid (nvt + nqk, H), head h = blockIdx.y:
+//  * blocks x < nvt (nvt = Sp/64 * D/64): v [H][S][Din] -> binary16 v^T
+//    [H][D][Sp], one 64-key x 64-feature tile through shared memory, 16-byte
+//    reads and writes;
+//  * the other blocks: q and k [H][S][Din] -> binary16 [H][Sp][D], 256 items of
+//    8 elements per block (q times `qscale`).
+// Keys past S and features past Din are zero.
 __global__ void __launch_bounds__(256)
-attn_prep_qk_kernel(const float *__restrict__ q, const float *__restrict__ k, __half *__restrict__ qh,
-                    __half *__restrict__ kh, int H, int S, int Sp, int D, int Din, float qscale) {
-    const float *src = blockIdx.y ? k : q;
-    __half *dst = blockIdx.y ? kh : qh;
-    const float scale = blockIdx.y ? 1.0f : qscale;
-    const int64_t items = int64_t(H) * Sp * (D / 8), stride = int64_t(gridDim.x) * blockDim.x;
-    for (int64_t it = int64_t(blockIdx.x) * blockDim.x + threadIdx.x; it < items; it += stride) {
-        const int64_t row = it / (D / 8);  // h * Sp + s
-        const int g = int(it % (D / 8));
-        const int h = int(row / Sp), s = int(row % Sp);
-        float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (s < S && g * 8 < Din) {
-            const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t(h) * S + s) * Din + g * 8);
-            const float4 a = __ldcs(p), c = __ldcs(p + 1);
-            f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
-        }
-        uint4 o;
-        __half2 t0 = __floats2half2_rn(f[0] * scale, f[1] * scale), t1 = __floats2half2_rn(f[2] * scale, f[3] * scale);
-        __half2 t2 = __floats2half2_rn(f[4] * scale, f[5] * scale), t3 = __floats2half2_rn(f[6] * scale, f[7] * scale);
-        o.x = *reinterpret_cast<uint32_t *>(&t0);
-        o.y = *reinterpret_cast<uint32_t *>(&t1);
-        o.z = *reinterpret_cast<uint32_t *>(&t2);
-        o.w = *reinterpret_cast<uint32_t *>(&t3);
-        *reinterpret_cast<uint4 *>(dst + row * D + g * 8) = o;
-    }
-}
-
-// v [H][S][Din] -> binary16 v^T [H][D][Sp], zero keys past S and features past
-// Din: 64 keys x 64 features per block through shared memory, 16-byte reads
-// and writes.
-__global__ void __launch_bounds__(256)
-attn_prep_vt_kernel(const float *__restrict__ v, __half *__restrict__ vt, int S, int Sp, int D, int Din) {
+attn_prep_kernel(const float *__restrict__ q, const float *__restrict__ k, const float *__restrict__ v,
+                 __half *__restrict__ qh, __half *__restrict__ kh, __half *__restrict__ vt, int S, int Sp, int D,
+                 int Din, float qscale) {
+    // the attention kernel behind this one may launch now: it waits for this
+    // kernel's completion before it reads any staged operand
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ __align__(16) __half tile[64][72];  // [feature][key], 8 halves of padding
-    const int s0 = blockIdx.x * 64, d0 = blockIdx.y * 64, h = blockIdx.z;
+    const int h = blockIdx.y;
+    const int nst = Sp / 64, nvt = nst * (D / 64);
     const int t = threadIdx.x;
+    if (int(blockIdx.x) < nvt) {
+        const int s0 = (int(blockIdx.x) % nst) * 64, d0 = (int(blockIdx.x) / nst) * 64;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int idx = t + 256 * i;           // 0..1023: key idx / 16, features 4 (idx % 16) .. +3
-        const int key = idx >> 4, f4 = idx & 15;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (s0 + key < S && d0 + 4 * f4 < Din)
-            x = __ldcs(reinterpret_cast<const float4 *>(v + (int64_t(h) * S + s0 + key) * Din + d0) + f4);
-        tile[4 * f4 + 0][key] = __float2half_rn(x.x);
-        tile[4 * f4 + 1][key] = __float2half_rn(x.y);
-        tile[4 * f4 + 2][key] = __float2half_rn(x.z);
-        tile[4 * f4 + 3][key] = __float2half_rn(x.w);
-    }
-    __syncthreads();
+        for (int i = 0; i < 4; ++i) {
+            const int idx = t + 256 * i;           // 0..1023: key idx / 16, features 4 (idx % 16) .. +3
+            const int key = idx >> 4, f4 = idx & 15;
+            float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (s0 + key < S && d0 + 4 * f4 < Din)
+                x = __ldcs(reinterpret_cast<const float4 *>(v + (int64_t(h) * S + s0 + key) * Din + d0) + f4);
+            tile[4 * f4 + 0][key] = __float2half_rn(x.x);
+            tile[4 * f4 + 1][key] = __float2half_rn(x.y);
+            tile[4 * f4 + 2][key] = __float2half_rn(x.z);
+            tile[4 * f4 + 3][key] = __float2half_rn(x.w);
+        }
+        __syncthreads();
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int idx = t + 256 * i;           // 0..511: feature idx / 8, keys 8 (idx % 8) .. +7
-        const int f = idx >> 3, c = idx & 7;
-        *reinterpret_cast<uint4 *>(vt + (int64_t(h) * D + d0 + f) * Sp + s0 + 8 * c) =
-            *reinterpret_cast<const uint4 *>(&tile[f][8 * c]);
+        for (int i = 0; i < 2; ++i) {
+            const int idx = t + 256 * i;           // 0..511: feature idx / 8, keys 8 (idx % 8) .. +7
+            const int f = idx >> 3, c = idx & 7;
+            *reinterpret_cast<uint4 *>(vt + (int64_t(h) * D + d0 + f) * Sp + s0 + 8 * c) =
+                *reinterpret_cast<const uint4 *>(&tile[f][8 * c]);
+        }
+        return;
     }
+    const int64_t per = int64_t(Sp) * (D / 8);  // items of q (or k) of one head
+    const int64_t it = int64_t(int(blockIdx.x) - nvt) * 256 + t;
+    if (it >= 2 * per) return;
+    const bool isk = it >= per;
+    const int64_t idx = isk ? it - per : it;
+    const int s = int(idx / (D / 8)), g = int(idx % (D / 8));
+    const float *src = isk ? k : q;
+    __half *dst = isk ? kh : qh;
+    const float scale = isk ? 1.0f : qscale;
+    float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (s < S && g * 8 < Din) {
+        const float4 *p = reinterpret_cast<const float4 *>(src + (int64_t(h) * S + s) * Din + g * 8);
+        const float4 a = __ldcs(p), c = __ldcs(p + 1);
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = c.x; f[5] = c.y; f[6] = c.z; f[7] = c.w;
+    }
+    uint4 o;
+    __half2 t0 = __floats2half2_rn(f[0] * scale, f[1] * scale), t1 = __floats2half2_rn(f[2] * scale, f[3] * scale);
+    __half2 t2 = __floats2half2_rn(f[4] * scale, f[5] * scale), t3 = __floats2half2_rn(f[6] * scale, f[7] * scale);
+    o.x = *reinterpret_cast<uint32_t *>(&t0);
+    o.y = *reinterpret_cast<uint32_t *>(&t1);
+    o.z = *reinterpret_cast<uint32_t *>(&t2);
+    o.w = *reinterpret_cast<uint32_t *>(&t3);
+    *reinterpret_cast<uint4 *>(dst + (int64_t(h) * Sp + s) * D + g * 8) = o;
 }
 
 // D: the kernel's head width (64 or 128); Din <= D the caller's (a multiple of 8)
@@ -506,12 +547,9 @@ cudaError_t launch_attention_d(const float *q, const float *k, const float *v, f
     __half *kh = qh + H * Sp * D;
     __half *vt = kh + H * Sp * D;
     const float qscale = 1.4426950408889634f / sqrtf(float(Din));  // log2(e) / sqrt(head dim)
-    const int64_t items = H * Sp * (D / 8);
-    const int64_t pgrid = std::min<int64_t>((items + 255) / 256, int64_t(ctx.num_sms) * 16);
-    attn_prep_qk_kernel<<<dim3(unsigned(pgrid), 2), 256, 0, ctx.stream>>>(q, k, qh, kh, int(H), int(S), int(Sp), D,
-                                                                          Din, qscale);
-    attn_prep_vt_kernel<<<dim3(unsigned(Sp / 64), unsigned(D / 64), unsigned(H)), 256, 0, ctx.stream>>>(
-        v, vt, int(S), int(Sp), D, Din);
+    const int64_t nvt = (Sp / 64) * (D / 64), nqk = (2 * Sp * (D / 8) + 255) / 256;  // blocks per head
+    attn_prep_kernel<<<dim3(unsigned(nvt + nqk), unsigned(H)), 256, 0, ctx.stream>>>(q, k, v, qh, kh, vt, int(S),
+                                                                                      int(Sp), D, Din, qscale);
     cudaError_t e = cudaPeekAtLastError();
     if (e != cudaSuccess) return e;
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
@@ -536,9 +574,19 @@ cudaError_t launch_attention_d(const float *q, const float *k, const float *v, f
         return cudaErrorInvalidValue;
     e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::BYTES);
     if (e != cudaSuccess) return e;
-    attn_fwd_kernel<D><<<dim3(unsigned((Sp / AQ + AQT - 1) / AQT), unsigned(H)), ATHREADS, Lay::BYTES,
-                         ctx.stream>>>(
-        qmap, kmap, vmap, out, int(H), int(S), int(Sp), Din, ctx.status, ctx.wait_ns);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(unsigned((Sp / AQ + AQT - 1) / AQT), unsigned(H));
+    cfg.blockDim = dim3(ATHREADS);
+    cfg.dynamicSmemBytes = Lay::BYTES;
+    cfg.stream = ctx.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, qmap, kmap, vmap, out, int(H), int(S), int(Sp), Din,
+                           ctx.status, ctx.wait_ns);
+    if (e != cudaSuccess) return e;
     return cudaPeekAtLastError();
 }
 
