@@ -655,12 +655,315 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     }
 }
 
+
+// ---------------------------------------------------------------------------
+// M = 1 decode GEMV with wide lanes (K a multiple of 2048, at most 8192).
+//
+// The same streaming and the same exact integer arithmetic as above, but lane
+// l of a chunk warp owns 64 weights, [2048 c + 64 l, +64) = half of 128-weight
+// block 32 c + l / 2.  A row then costs one 16-byte shared-memory read per
+// lane, and the per-row work outside the dot products (the address, the limb
+// combination, the butterfly) is spread over twice the weights.  The 48 limb
+// registers need up to 112 registers per thread: eight consumer warps (two
+// per scheduler) and the producer, two CTAs per SM.
+//
+// x arrives as two tensor copies of 128-byte rows: the first 32 elements of
+// every lane slice, then the last 32 (a 3-D view [K/64][2][32] of x), so that
+// lane l of chunk c reads row 32 c + l of each half.  With the 128-byte
+// swizzle the eight lanes of one shared-memory wavefront then hit eight
+// different 16-byte bank groups.
+constexpr int kGwLaneW = 64;               // weights per lane: half a 128-weight block
+constexpr int kGwChunk = 32 * kGwLaneW;    // weights per warp-chunk (2048)
+constexpr int kGwConsumers = 8;            // consumer warps (groups x chunks)
+constexpr int kGwMaxK = 4 * kGwChunk;      // at least two groups of chunk warps
+
+template <int RS, bool DBULK>
+__global__ void __launch_bounds__(32 * (kGwConsumers + 1), 2)
+gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__restrict__ qs,
+                 const __half *__restrict__ dpl, const float *residual, float *out, GvsParams P,
+                 unsigned int *status, uint64_t wait_ns) {
+    extern __shared__ __align__(128) uint8_t gvw_raw[];
+    uint8_t *gvs_smem = gvw_raw + ((1024u - (smem_u32(gvw_raw) & 1023u)) & 1023u);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = P.k, C = P.C;
+    const int64_t kq = k / 4, kb = k / kBlockW;
+    const int consumers = P.consumers;
+    const int pwarp = int(blockDim.x >> 5) - 1;
+    const int b = int(blockIdx.x);
+    const int R0 = b * P.rbase + min(b, P.rextra);
+    const int nf = P.rbase + (b < P.rextra ? 1 : 0);
+    const int rows = P.swiglu ? 2 * nf : nf;
+    auto real_row = [&](int i) { return (P.swiglu && i >= nf) ? P.f + R0 + (i - nf) : R0 + i; };
+    const int nstages = (rows + RS - 1) / RS;
+    constexpr bool dbulk = DBULK;
+    const uint32_t code_bytes = uint32_t(RS * kq);
+    const uint32_t stage_bytes = code_bytes + (dbulk ? uint32_t(RS * kb * 2) : 0u);
+    const int xr = k / kGwLaneW;  // 128-byte rows per half of the x tile
+
+    // shared memory: [x: two halves][ring][partials][barriers][abort flag]
+    const float *xs = reinterpret_cast<const float *>(gvs_smem);
+    uint8_t *ring = gvs_smem + P.off_ring;
+    float *partial = reinterpret_cast<float *>(gvs_smem + P.off_partial);
+    uint64_t *full = reinterpret_cast<uint64_t *>(gvs_smem + P.off_bar);
+    uint64_t *empty = full + P.ns;
+    uint64_t *xbar = empty + P.ns;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(xbar + 1);
+    const uint32_t ring_addr = smem_u32(ring);
+
+    if (warp == 0) {
+        for (int i = lane; i < P.ns; i += 32) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 32 * C);
+        }
+        if (lane == 0) {
+            mbar_init(xbar, 1);
+            *abort_flag = 0;
+        }
+        fence_proxy_async_smem();
+    }
+    __syncthreads();
+    const bool producer = warp == pwarp && lane == 0;
+    auto pieces = [&](int st, auto &&fn) {
+        const int lo = st * RS, hi = min(lo + RS, rows);
+        if (P.swiglu && lo < nf && hi > nf) {
+            fn(lo, nf - lo, 0);
+            fn(nf, hi - nf, nf - lo);
+        } else {
+            fn(lo, hi - lo, 0);
+        }
+    };
+    auto issue = [&](int st) {
+        const int slot = st % P.ns;
+        const int r = min(RS, rows - st * RS);
+        const uint32_t dst = ring_addr + uint32_t(slot) * stage_bytes;
+        mbar_expect_tx_gv(&full[slot], uint32_t(r) * (uint32_t(kq) + (dbulk ? uint32_t(kb * 2) : 0u)));
+        pieces(st, [&](int i0, int cnt, int off) {
+            const int64_t row = real_row(i0);
+            bulk_g2s_gv(dst + uint32_t(off) * uint32_t(kq), qs + row * kq, uint32_t(cnt * kq), &full[slot]);
+            if (dbulk)
+                bulk_g2s_gv(dst + code_bytes + uint32_t(off) * uint32_t(kb * 2), dpl + row * kb,
+                            uint32_t(cnt * kb * 2), &full[slot]);
+        });
+    };
+    // weights to L2 before the dependency wait (see gemv_stream_kernel)
+    if (warp == pwarp) {
+        for (int st = lane; st < nstages; st += 32) {
+            pieces(st, [&](int i0, int cnt, int) {
+                const int64_t row = real_row(i0);
+                bulk_prefetch_l2(qs + row * kq, uint32_t(cnt * kq));
+                if (dbulk) bulk_prefetch_l2(dpl + row * kb, uint32_t(cnt * kb * 2));
+            });
+        }
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (warp == pwarp) {
+        if (lane == 0) {
+            // half h: elements [64 j + 32 h, +32) of every j, as xr rows of 128 bytes
+            mbar_expect_tx_gv(xbar, uint32_t(2 * xr * 128));
+            for (int h = 0; h < 2; ++h)
+                asm volatile(
+                    "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes "
+                    "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(gvs_smem) + uint32_t(h * xr * 128)),
+                    "l"(reinterpret_cast<uint64_t>(&xmap)), "r"(0), "r"(h), "r"(0), "r"(smem_u32(xbar))
+                    : "memory");
+        }
+        const int first = min(nstages, P.ns);
+        for (int st = lane; st < first; st += 32) issue(st);
+        if (producer) {
+            for (int st = P.ns; st < nstages; ++st) {
+                const int slot = st % P.ns, u = st / P.ns;
+                if (!mbar_wait_spin(&empty[slot], (u - 1) & 1, wait_ns, status)) {
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                issue(st);
+            }
+            const uint64_t drain = wait_ns > 1000000000ull ? wait_ns : 1000000000ull;
+            for (int st = max(0, nstages - P.ns); st < nstages; ++st)
+                mbar_wait_spin(&full[st % P.ns], (st / P.ns) & 1, drain, status);
+        }
+    } else if (warp < consumers) {
+        const int g = warp / C, c = warp % C;
+        const int kw0 = c * kGwChunk + lane * kGwLaneW;
+        // ---- quantise this lane's 64 elements of x (one scale per 128-weight
+        // block, shared with the neighbouring lane) into three limbs.
+        // L[q][t][l] holds in byte i limb l of X[16q + t + 4i].
+        uint32_t L[4][4][3];
+        int sx;
+        float sc;
+        if (!mbar_wait_spin(xbar, 0, wait_ns, status)) *abort_flag = 1;
+        {
+            float xv[kGwLaneW];
+            const int xrow = c * 32 + lane;  // this lane's row in each half
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float4 v =
+                        *reinterpret_cast<const float4 *>(xs + (h * xr + xrow) * 32 + ((i ^ (xrow & 7)) << 2));
+                    xv[32 * h + 4 * i + 0] = v.x;
+                    xv[32 * h + 4 * i + 1] = v.y;
+                    xv[32 * h + 4 * i + 2] = v.z;
+                    xv[32 * h + 4 * i + 3] = v.w;
+                }
+            // max |x| as a balanced tree (short dependency chain)
+            float m[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) m[j] = fmaxf(fabsf(xv[2 * j]), fabsf(xv[2 * j + 1]));
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+            float s = fmaxf(m[0], __shfl_xor_sync(0xffffffffu, m[0], 1));  // the block's other half
+            // 2^22 / s (correctly rounded reciprocal, exact scaling)
+            const float inv = s > 0.f ? __frcp_rn(s) * 4194304.0f : 0.f;
+            // X = rint(x * inv) by one fused multiply-add onto 1.5 * 2^23 (|X| <= 2^22)
+            int X[kGwLaneW];
+#pragma unroll
+            for (int j = 0; j < kGwLaneW; ++j)
+                X[j] = __float_as_int(__fmaf_rn(xv[j], inv, 12582912.0f)) - 0x4B400000;
+            int ps[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) ps[j] = (X[4 * j] + X[4 * j + 1]) + (X[4 * j + 2] + X[4 * j + 3]);
+#pragma unroll
+            for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
+            sx = -ps[0];  // the first accumulator of every row starts at -sum X
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const uint32_t x0 = uint32_t(X[16 * q + t]), x1 = uint32_t(X[16 * q + t + 4]);
+                    const uint32_t x2 = uint32_t(X[16 * q + t + 8]), x3 = uint32_t(X[16 * q + t + 12]);
+                    const uint32_t p01 = __byte_perm(x0, x1, 0x5140);
+                    const uint32_t p23 = __byte_perm(x2, x3, 0x5140);
+                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);
+                    L[q][t][1] = __byte_perm(p01, p23, 0x7632);
+                    const uint32_t h01 = __byte_perm(x0, x1, 0x0062);
+                    const uint32_t h23 = __byte_perm(x2, x3, 0x0062);
+                    L[q][t][2] = __byte_perm(h01, h23, 0x5410);
+                }
+            sc = s * (1.0f / 4194304.0f);
+        }
+        const uint32_t kq32 = uint32_t(kq), kb2 = uint32_t(kb) * 2;
+        const uint32_t code_off = uint32_t(kw0 / 4);
+        const uint32_t d_off = code_bytes + uint32_t(kw0 / kBlockW) * 2;
+        const int64_t dcol = kw0 / kBlockW;
+        int slot = g, ph = 0;
+        for (int st = g; st < nstages; st += P.groups) {
+            if (!mbar_wait_spin(&full[slot], uint32_t(ph), wait_ns, status)) {
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            const int r0 = st * RS;
+            const int nv = min(RS, rows - r0);
+            const uint8_t *sb = ring + uint32_t(slot) * stage_bytes;
+            // one 16-byte read per row and lane (a warp reads 512 contiguous bytes)
+            uint4 cw[RS];
+#pragma unroll
+            for (int uu = 0; uu < RS; ++uu)
+                cw[uu] = *reinterpret_cast<const uint4 *>(sb + code_off + uint32_t(uu) * kq32);
+            if (!dbulk) mbar_arrive(&empty[slot]);
+            constexpr int V = RS <= 2 ? 2 : RS <= 4 ? 4 : 8;
+            int tv[V];
+#pragma unroll
+            for (int uu = 0; uu < V; ++uu) tv[uu] = 0;
+#pragma unroll
+            for (int uu = 0; uu < RS; ++uu) {
+                int a0 = sx, a1 = 0, a2 = 0;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t wq = q == 0 ? cw[uu].x : q == 1 ? cw[uu].y : q == 2 ? cw[uu].z : cw[uu].w;
+#pragma unroll
+                    for (int t = 0; t < 4; ++t) {
+                        const uint32_t cv = (wq >> (2 * t)) & 0x03030303u;
+                        a0 = dp4a_uu(cv, L[q][t][0], a0);
+                        a1 = dp4a_uu(cv, L[q][t][1], a1);
+                        a2 = dp4a_us(cv, L[q][t][2], a2);
+                    }
+                }
+                tv[uu] = a0 + (a1 << 8) + (a2 << 16);  // |T| <= 64 * 2^22
+            }
+            // butterfly level 1 (lanes 2j, 2j+1: one block, one x scale):
+            // exact integer adds (|sum| <= 2^29)
+            constexpr int VH = V / 2;
+            {
+                const bool upper = (lane & 1) != 0;
+#pragma unroll
+                for (int i = 0; i < VH; ++i) {
+                    const int give = upper ? tv[i] : tv[i + VH];
+                    const int keep = upper ? tv[i + VH] : tv[i];
+                    tv[i] = keep + __shfl_xor_sync(0xffffffffu, give, 1);
+                }
+            }
+            const int sel = lane & 1;
+            float fv[VH];
+#pragma unroll
+            for (int i = 0; i < VH; ++i) {
+                const int uu = sel * VH + i;
+                float dd = 0.f;
+                if (uu < nv)
+                    dd = dbulk ? __half2float(*reinterpret_cast<const __half *>(sb + d_off + uint32_t(uu) * kb2))
+                               : __half2float(__ushort_as_half(ldg_u16(dpl + int64_t(real_row(r0 + uu)) * kb + dcol)));
+                fv[i] = float(tv[i]) * (sc * dd);
+            }
+            if (dbulk) mbar_arrive(&empty[slot]);
+            // float halving levels at offsets 2, 4, ... until one value is left
+#pragma unroll
+            for (int lv = 0; (VH >> lv) > 1; ++lv) {
+                const int o = 2 << lv, half = VH >> (lv + 1);
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < VH / 2; ++i)
+                    if (i < half) {
+                        const float give = upper ? fv[i] : fv[i + half];
+                        const float keep = upper ? fv[i + half] : fv[i];
+                        fv[i] = keep + __shfl_xor_sync(0xffffffffu, give, o);
+                    }
+            }
+            constexpr int LV = V == 8 ? 3 : V == 4 ? 2 : 1;
+#pragma unroll
+            for (int o = 1 << LV; o < 32; o <<= 1) fv[0] += __shfl_xor_sync(0xffffffffu, fv[0], o);
+            if (lane < V) {
+                const int uu = V == 8 ? ((lane & 1) << 2) | (((lane >> 1) & 1) << 1) | ((lane >> 2) & 1)
+                                      : V == 4 ? ((lane & 1) << 1) | ((lane >> 1) & 1) : (lane & 1);
+                if (uu < RS && uu < nv) partial[(r0 + uu) * C + c] = fv[0];
+            }
+            slot += P.groups;
+            if (slot >= P.ns) slot -= P.ns, ph ^= 1;
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) return;
+    if (P.swiglu) {
+        for (int i = threadIdx.x; i < nf; i += blockDim.x) {
+            float g = 0.f, u = 0.f;
+            for (int cc = 0; cc < C; ++cc) g += partial[i * C + cc];
+            for (int cc = 0; cc < C; ++cc) u += partial[(nf + i) * C + cc];
+            out[R0 + i] = g / (1.0f + expf(-g)) * u;
+        }
+        return;
+    }
+    for (int i = threadIdx.x; i < rows; i += blockDim.x) {
+        float sum = 0.f;
+        for (int cc = 0; cc < C; ++cc) sum += partial[i * C + cc];
+        if (residual) sum += residual[R0 + i];
+        out[R0 + i] = sum;
+    }
+}
+
 }  // namespace
 
 // swiglu: n = 2f weight rows (gate then up), out has f elements, no residual.
 cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *residual,
                                float *out, int64_t n, int64_t k, bool swiglu, const LaunchCtx &ctx) {
-    const int C = int((k + kGvChunk - 1) / kGvChunk);
+    // wide lanes (64 weights) where K splits into at most four 2048-weight chunks
+    const bool wide = k % kGwChunk == 0 && k <= kGwMaxK;
+    const int C = wide ? int(k / kGwChunk) : int((k + kGvChunk - 1) / kGvChunk);
     const int64_t kq = k / 4, kb = k / kBlockW;
     if (C > kGvMaxConsumers) return cudaErrorNotSupported;
     GvsParams P;
@@ -669,7 +972,7 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.C = C;
     P.swiglu = swiglu ? 1 : 0;
     P.f = int(n / 2);
-    P.groups = std::max(1, kGvMaxConsumers / C);  // groups of C warps (one per chunk)
+    P.groups = std::max(1, (wide ? kGwConsumers : kGvMaxConsumers) / C);  // groups of C warps (one per chunk)
     // the CTAs split the rows (with swiglu: the features, two rows each)
     const int64_t units = swiglu ? n / 2 : n;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(ctx.num_sms, (n + 7) / 8));
@@ -693,10 +996,11 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     const size_t stage_bytes = size_t(P.rs) * kq + (dbulk ? size_t(P.rs) * kb * 2 : 0);
     const size_t partial_bytes = size_t((P.rows_cta * C + 1) & ~1) * 4;
     // x as a tensor of K/32 rows of 128 bytes, in boxes of at most 256 rows
-    // (a multiple of 8 rows: every box starts on a 1024-byte swizzle atom)
+    // (a multiple of 8 rows: every box starts on a 1024-byte swizzle atom);
+    // wide lanes: two halves of K/64 rows (K/64 <= 128, a multiple of 32)
     const int xrows = int(k / kGvLaneW);
-    P.nxbox = (xrows + 255) / 256;
-    P.xbox_rows = (((xrows + P.nxbox - 1) / P.nxbox) + 7) & ~7;
+    P.nxbox = wide ? 2 : (xrows + 255) / 256;
+    P.xbox_rows = wide ? int(k / kGwLaneW) : (((xrows + P.nxbox - 1) / P.nxbox) + 7) & ~7;
     const size_t x_bytes = size_t(P.nxbox) * P.xbox_rows * 128;
     // two CTAs per SM: 2 * (this + 1 KB reserved per CTA) within 228 KB
     const size_t budget = 112 * 1024;
@@ -721,7 +1025,17 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return cudaErrorNotSupported;
     CUtensorMap xmap;
-    {
+    if (wide) {
+        // [K/64][2][32] view of x: element (e, h, j) = x[64 j + 32 h + e]
+        const cuuint64_t gdim[3] = {32, 2, cuuint64_t(k / kGwLaneW)};
+        const cuuint64_t gstride[2] = {128, 256};
+        const cuuint32_t box[3] = {32, 1, cuuint32_t(k / kGwLaneW)};
+        const cuuint32_t estride[3] = {1, 1, 1};
+        if (enc(&xmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float *>(x), gdim, gstride, box,
+                estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    } else {
         const cuuint64_t gdim[2] = {cuuint64_t(kGvLaneW), cuuint64_t(xrows)};
         const cuuint64_t gstride[1] = {cuuint64_t(kGvLaneW) * 4};
         const cuuint32_t box[2] = {cuuint32_t(kGvLaneW), cuuint32_t(P.xbox_rows)};
@@ -735,7 +1049,8 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     void (*kern)(const CUtensorMap, const uint8_t *, const __half *, const float *, float *, GvsParams,
                  unsigned int *, uint64_t) = nullptr;
 #define TQ2_GV_KERN(RSV)                                                                                    \
-    kern = dbulk ? gemv_stream_kernel<RSV, true, kGvMaxConsumers> : gemv_stream_kernel<RSV, false, kGvMaxConsumers>
+    kern = wide ? (dbulk ? gemv_wide_kernel<RSV, true> : gemv_wide_kernel<RSV, false>)                      \
+                : (dbulk ? gemv_stream_kernel<RSV, true, kGvMaxConsumers> : gemv_stream_kernel<RSV, false, kGvMaxConsumers>)
     switch (P.rs) {
         case 2: TQ2_GV_KERN(2); break;
         case 3: TQ2_GV_KERN(3); break;

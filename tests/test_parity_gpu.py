@@ -129,7 +129,9 @@ def test_gemv_down_residual_full(tq2):
 
 
 @pytest.mark.parametrize("n,k", [(1, 128), (129, 128), (7, 1152), (300, 3072), (33, 20480),
-                                 (5, 65536), (30400, 4096), (250000, 512), (2000, 16384)])
+                                 (5, 65536), (30400, 4096), (250000, 512), (2000, 16384),
+                                 # 64-weight lanes: one to four 2048-weight chunks
+                                 (1, 2048), (77, 2048), (3, 6144), (1000, 8192), (153, 4096)])
 def test_gemv_edge_shapes(tq2, n, k):
     p = tq2_synth.make_problem(1, n, k, seed=n * 7 + k, residual=(n % 2 == 1))
     w = upload(tq2, p)
