@@ -42,7 +42,8 @@ KERNEL_NAMES = {0: "auto", 1: "gemv", 2: "skinny", 3: "tc", 4: "f32ref", 5: "tc_
 
 # Every symbol include/tq2.h declares.
 EXPORTS = (
-    "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemm",
+    "tq2_soa_bytes", "tq2_status_string", "tq2_reformat_aos_to_soa", "tq2_gemv", "tq2_gemv_resident",
+    "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
     "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu", "tq2_act16_from_f32",
@@ -69,8 +70,10 @@ def _load():
     L.tq2_status_string.argtypes = [i32]
     L.tq2_reformat_aos_to_soa.restype = i32
     L.tq2_reformat_aos_to_soa.argtypes = [vp, vp, i64, i64, vp]
-    L.tq2_gemv.restype = i32
-    L.tq2_gemv.argtypes = [vp, vp, vp, vp, i64, i64, vp]
+    for name in ("tq2_gemv", "tq2_gemv_resident"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [vp, vp, vp, vp, i64, i64, vp]
     for name in ("tq2_gemm", "tq2_gemm_f32ref"):
         f = getattr(L, name)
         f.restype = i32
@@ -199,6 +202,11 @@ def tq2_gate_up_swiglu(w_soa, x, out, m: int, f: int, k: int, stream=None) -> No
 def tq2_gemv(w_soa, x, residual, out, n: int, k: int, stream=None) -> None:
     _check(lib.tq2_gemv(_ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), n, k, _stream(stream)),
            "tq2_gemv")
+
+
+def tq2_gemv_resident(w_soa, x, residual, out, n: int, k: int, stream=None) -> None:
+    _check(lib.tq2_gemv_resident(_ptr(w_soa), _ptr(x), _ptr(residual), _ptr(out), n, k,
+                                 _stream(stream)), "tq2_gemv_resident")
 
 
 def tq2_gemm(w_soa, x, residual, out, m: int, n: int, k: int, stream=None) -> None:

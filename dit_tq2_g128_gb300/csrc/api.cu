@@ -430,6 +430,17 @@ int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *ou
     return tq2_gemm_with(TQ2_KERNEL_GEMV, w_soa, x, residual, out, 1, n, k, stream);
 }
 
+int tq2_gemv_resident(const void *w_soa, const float *x, const float *residual, float *out,
+                      int64_t n, int64_t k, void *stream) {
+    bool noop = false;
+    int st = check_matmul(w_soa, x, residual, out, 1, n, k, &noop);
+    if (st != TQ2_OK || noop) return st;
+    tq2::LaunchCtx ctx;
+    st = prepare(stream, &ctx, {w_soa, x, residual, out});
+    if (st != TQ2_OK) return st;
+    return finish(tq2::launch_gemv(w_soa, x, residual, out, n, k, ctx, true));
+}
+
 int tq2_gemm_f32ref(const void *w_soa, const float *x, const float *residual, float *out,
                     int64_t m, int64_t n, int64_t k, void *stream) {
     return tq2_gemm_with(TQ2_KERNEL_F32REF, w_soa, x, residual, out, m, n, k, stream);

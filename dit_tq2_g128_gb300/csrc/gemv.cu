@@ -326,6 +326,8 @@ struct GvsParams {
     int consumers;     // consumer warps = groups * C
     int groups;        // consumer warp groups; group g owns the ring slots s with s % groups == g
     int rows_cta;      // max rows of a CTA (partial buffer size)
+    int early;         // resident weights: the first ring of stages is copied before the
+                       // dependency wait (no kernel still running can write the weights)
 };
 
 // RS: rows per stage; DBULK: the rows' block scales travel with their stage in
@@ -408,8 +410,14 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     // The weights go to L2 before waiting for the preceding kernel.  A
     // prefetch cannot leave stale data behind (L2 is the point of coherence,
     // and the copies below read through it after the wait).
+    // With resident weights the first ring of stages goes straight to shared
+    // memory here, during the preceding kernel; only the stages beyond the
+    // ring are prefetched into L2.
+    const int first = min(nstages, P.ns);
     if (warp == pwarp) {
-        for (int st = lane; st < nstages; st += 32) {
+        if (P.early)
+            for (int st = lane; st < first; st += 32) issue(st);
+        for (int st = (P.early ? first : 0) + lane; st < nstages; st += 32) {
             pieces(st, [&](int i0, int cnt, int) {
                 const int64_t row = real_row(i0);
                 bulk_prefetch_l2(qs + row * kq, uint32_t(cnt * kq));
@@ -440,8 +448,8 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         // the first ring-full of stages needs no slot to free up: the 32 lanes
         // issue those copies in parallel; lane 0 then refills slots as the
         // consumers release them
-        const int first = min(nstages, P.ns);
-        for (int st = lane; st < first; st += 32) issue(st);
+        if (!P.early)
+            for (int st = lane; st < first; st += 32) issue(st);
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
@@ -746,8 +754,14 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
         });
     };
     // weights to L2 before the dependency wait (see gemv_stream_kernel)
+    // With resident weights the first ring of stages goes straight to shared
+    // memory here, during the preceding kernel; only the stages beyond the
+    // ring are prefetched into L2.
+    const int first = min(nstages, P.ns);
     if (warp == pwarp) {
-        for (int st = lane; st < nstages; st += 32) {
+        if (P.early)
+            for (int st = lane; st < first; st += 32) issue(st);
+        for (int st = (P.early ? first : 0) + lane; st < nstages; st += 32) {
             pieces(st, [&](int i0, int cnt, int) {
                 const int64_t row = real_row(i0);
                 bulk_prefetch_l2(qs + row * kq, uint32_t(cnt * kq));
@@ -768,8 +782,8 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
                     "l"(reinterpret_cast<uint64_t>(&xmap)), "r"(0), "r"(h), "r"(0), "r"(smem_u32(xbar))
                     : "memory");
         }
-        const int first = min(nstages, P.ns);
-        for (int st = lane; st < first; st += 32) issue(st);
+        if (!P.early)
+            for (int st = lane; st < first; st += 32) issue(st);
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
@@ -960,7 +974,8 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
 
 // swiglu: n = 2f weight rows (gate then up), out has f elements, no residual.
 cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *residual,
-                               float *out, int64_t n, int64_t k, bool swiglu, const LaunchCtx &ctx) {
+                               float *out, int64_t n, int64_t k, bool swiglu, bool resident,
+                               const LaunchCtx &ctx) {
     // wide lanes (64 weights) where K splits into at most four 2048-weight chunks
     const bool wide = k % kGwChunk == 0 && k <= kGwMaxK;
     const int C = wide ? int(k / kGwChunk) : int((k + kGvChunk - 1) / kGvChunk);
@@ -971,6 +986,9 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.k = int(k);
     P.C = C;
     P.swiglu = swiglu ? 1 : 0;
+    // (the 32-weight-lane kernel measured slower with early copies: 6.50 against
+    // 6.21 us at K=12288, N=4096, its ring holding only part of a CTA's stages)
+    P.early = resident && wide ? 1 : 0;
     P.f = int(n / 2);
     P.groups = std::max(1, (wide ? kGwConsumers : kGvMaxConsumers) / C);  // groups of C warps (one per chunk)
     // the CTAs split the rows (with swiglu: the features, two rows each)
@@ -1087,13 +1105,13 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
 cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,
                                const LaunchCtx &ctx) {
     if (k > int64_t(kGvMaxConsumers) * kGvChunk || 2 * f > INT32_MAX) return cudaErrorNotSupported;
-    return launch_gemv_stream(w_soa, x, nullptr, out, 2 * f, k, true, ctx);
+    return launch_gemv_stream(w_soa, x, nullptr, out, 2 * f, k, true, false, ctx);
 }
 
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
-                        int64_t n, int64_t k, const LaunchCtx &ctx) {
+                        int64_t n, int64_t k, const LaunchCtx &ctx, bool resident) {
     if (k <= int64_t(kGvMaxConsumers) * kGvChunk && n <= INT32_MAX) {
-        cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, false, ctx);
+        cudaError_t e = launch_gemv_stream(w_soa, x, residual, out, n, k, false, resident, ctx);
         if (e != cudaErrorNotSupported) return e;
         (void)cudaGetLastError();
     }

@@ -42,8 +42,11 @@ inline SoaView soa_view(const void *w_soa, int64_t n, int64_t k) {
 cudaError_t launch_quantize(const float *w, void *w_aos, int64_t n, int64_t k, const LaunchCtx &ctx);
 cudaError_t launch_reformat(const void *w_aos, void *w_soa, int64_t n, int64_t k,
                             const LaunchCtx &ctx);
+// resident: the weights are written by no work still unfinished when the call
+// is enqueued, so their copies into shared memory may precede the dependency
+// wait (same arithmetic and result either way).
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,
-                        int64_t n, int64_t k, const LaunchCtx &ctx);
+                        int64_t n, int64_t k, const LaunchCtx &ctx, bool resident = false);
 // Fused gate/up + SwiGLU (weight rows [0, f) gate, [f, 2f) up; out [m, f]).
 // cudaErrorNotSupported: shape outside the fused kernels (the caller falls back).
 cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,

@@ -148,6 +148,18 @@ int tq2_quantize_f32(const float *w, void *w_aos, int64_t n, int64_t k, void *st
 int tq2_gemv(const void *w_soa, const float *x, const float *residual, float *out,
              int64_t n, int64_t k, void *stream);
 
+/* tq2_gemv for weights that stay resident across calls (decoding with a
+ * weight set uploaded once): the same arguments, arithmetic and result, bit
+ * for bit.  Contract: no work that is still unfinished when this call is
+ * enqueued writes w_soa (write the weights, then synchronise the stream or the
+ * device before the decode loop).  Under it the call copies its weight rows
+ * into shared memory before it waits for the preceding kernel of the stream,
+ * i.e. while that kernel runs; x, residual and out are still read and written
+ * only after that kernel has finished.  Breaking the contract gives results
+ * from stale weights (no fault).  Errors as tq2_gemv. */
+int tq2_gemv_resident(const void *w_soa, const float *x, const float *residual, float *out,
+                      int64_t n, int64_t k, void *stream);
+
 /* Any-M matmul with optional residual epilogue, dispatching on M (and N, K)
  * between the GEMV (m = 1), the one-launch skinny tensor-core kernel
  * (2 <= m <= 32, TQ2_KERNEL_SKINNY_MMA below) and the tcgen05 tensor-core

@@ -138,6 +138,53 @@ def test_gemv_edge_shapes(tq2, n, k):
     check(run(tq2, tq2.TQ2_KERNEL_GEMV, w, p), p, TOL_F32, what=f"gemv n={n} k={k}")
 
 
+@pytest.mark.parametrize("n,k", [(12288, 4096), (4096, 12288), (153, 4096), (1, 2048), (3, 6144),
+                                 (7, 1152), (33, 20480), (30400, 4096)])
+def test_gemv_resident_equals_gemv_bit_for_bit(tq2, n, k):
+    # the resident-weights entry only moves the weight copies before the
+    # dependency wait: the same arithmetic, so the same bits as tq2_gemv
+    p = tq2_synth.make_problem(1, n, k, seed=n * 3 + k, residual=(n % 2 == 0))
+    w = upload(tq2, p)
+    torch.cuda.synchronize()  # the contract: the weights are complete before the call
+    x = torch.from_numpy(p.x[0]).cuda()
+    r = None if p.residual is None else torch.from_numpy(p.residual[0]).cuda()
+    a = torch.full((n,), float("nan"), device="cuda")
+    b = torch.full((n,), float("nan"), device="cuda")
+    tq2.tq2_gemv(w, x, r, a, n, k)
+    tq2.tq2_gemv_resident(w, x, r, b, n, k)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    check(b.cpu().numpy(), p, TOL_F32, what=f"gemv resident n={n} k={k}")
+
+
+@pytest.mark.parametrize("k", [4096, 3072])
+def test_gemv_resident_chain_reads_x_after_the_previous_call(tq2, k):
+    # a chain of dependent calls with no synchronisation in between: call i+1
+    # reads the x that call i writes (and adds the residual call i-1 wrote), so
+    # reading x or the residual before the dependency wait would show up as a
+    # difference from the same chain through tq2_gemv
+    n = k
+    ws = []
+    for i in range(3):
+        p = tq2_synth.make_problem(1, n, k, seed=500 + i + k)
+        ws.append(upload(tq2, p))
+    torch.cuda.synchronize()
+    x0 = torch.from_numpy(tq2_synth.make_problem(1, n, k, seed=600 + k).x[0]).cuda()
+
+    def chain(fn):
+        bufs = [x0.clone()] + [torch.full((n,), float("nan"), device="cuda") for _ in range(12)]
+        for i in range(12):
+            res = bufs[i - 1] if i >= 1 else None
+            fn(ws[i % 3], bufs[i], res, bufs[i + 1], n, k)
+        torch.cuda.synchronize()
+        return torch.stack(bufs[1:])
+
+    a = chain(tq2.tq2_gemv)
+    b = chain(tq2.tq2_gemv_resident)
+    assert torch.isfinite(a).all()
+    assert torch.equal(a, b)
+
+
 def test_gemv_quantisation_bound_with_wide_dynamic_range(tq2):
     # one huge activation per 64 elements next to tiny ones: the GEMV's
     # documented bound (2^-22 * max|x_block| * sum_block |w| per 128-weight
