@@ -74,6 +74,7 @@ def test_argument_errors_are_returned_before_any_launch(tq2):
     for k in (0, -128, 64, 130):
         assert rc_gemm(tq2, W, X, None, O, 4, 4, k) == tq2.TQ2_ERR_BAD_K
         assert tq2.lib.tq2_gemv(W, X, None, O, 4, k, None) == tq2.TQ2_ERR_BAD_K
+        assert tq2.lib.tq2_gemv_resident(W, X, None, O, 4, k, None) == tq2.TQ2_ERR_BAD_K
         assert tq2.lib.tq2_reformat_aos_to_soa(W, O, 4, k, None) == tq2.TQ2_ERR_BAD_K
     # negative sizes
     assert rc_gemm(tq2, W, X, None, O, -1, 4, 128) == tq2.TQ2_ERR_INVALID_ARG

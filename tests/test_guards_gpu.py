@@ -60,7 +60,7 @@ def finish(tq2, g):
     assert g.written(), "the output was not written in full"
 
 
-MATMUL_SHAPES = [(1, 1, 128), (1, 257, 640), (1, 12288, 4096), (1, 4096, 12288), (2, 300, 384),
+MATMUL_SHAPES = [(1, 1, 128), (1, 257, 640), (1, 12288, 4096), (1, 4096, 12288), (1, 153, 2048), (2, 300, 384),
                  (3, 7, 128), (8, 1024, 1024), (16, 129, 256), (17, 257, 384), (129, 300, 640),
                  (300, 1028, 256), (1536, 3072, 3072)]
 
@@ -112,9 +112,11 @@ def test_matmul_guard_bands(tq2, m, n, k, res):
                 tq2.tq2_gemm_noalloc(w, x, rr, g.view, m, n, k)
             finish(tq2, g)
     if m == 1:
-        g = Guarded(n)
-        tq2.tq2_gemv(w, x[0], None if r is None else r[0], g.view, n, k)
-        finish(tq2, g)
+        for fn in (tq2.tq2_gemv, tq2.tq2_gemv_resident):
+            g = Guarded(n)
+            torch.cuda.synchronize()
+            fn(w, x[0], None if r is None else r[0], g.view, n, k)
+            finish(tq2, g)
 
 
 @pytest.mark.parametrize("m,f,k", [(1, 48, 256), (1, 6144, 4096), (2, 64, 256), (8, 100, 384),
@@ -199,8 +201,11 @@ def test_operands_not_on_this_device_are_refused(tq2):
         # element-wise converter first (a plain-load kernel), then every other entry point
         assert L.tq2_act16_from_f32(hp, x16.data_ptr(), m, k, stream) == bad, label
         assert L.tq2_act16_to_f32(o16.data_ptr(), hp, m, n, stream) == bad, label
-        assert L.tq2_gemv(w.data_ptr(), hp, None, out.data_ptr(), n, k, stream) == bad, label
-        assert L.tq2_gemv(hp, x.data_ptr(), None, out.data_ptr(), n, k, stream) == bad, label
+        for gv in (L.tq2_gemv, L.tq2_gemv_resident):
+            assert gv(w.data_ptr(), hp, None, out.data_ptr(), n, k, stream) == bad, label
+            assert gv(hp, x.data_ptr(), None, out.data_ptr(), n, k, stream) == bad, label
+            assert gv(w.data_ptr(), x.data_ptr(), hp, out.data_ptr(), n, k, stream) == bad, label
+            assert gv(w.data_ptr(), x.data_ptr(), None, hp, n, k, stream) == bad, label
         for kern in (0, 1, 2, 3, 4, 5, 6):
             mm = 1 if kern == 1 else m
             for args in ((hp, x.data_ptr(), None, out.data_ptr()), (w.data_ptr(), hp, None, out.data_ptr()),
