@@ -326,8 +326,8 @@ struct GvsParams {
     int consumers;     // consumer warps = groups * C
     int groups;        // consumer warp groups; group g owns the ring slots s with s % groups == g
     int rows_cta;      // max rows of a CTA (partial buffer size)
-    int early;         // resident weights: the first ring of stages is copied before the
-                       // dependency wait (no kernel still running can write the weights)
+    int early;         // resident weights (wide-lane kernel): the first ring of stages is
+                       // copied before the dependency wait (no unfinished work writes them)
 };
 
 // RS: rows per stage; DBULK: the rows' block scales travel with their stage in
@@ -410,14 +410,8 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     // The weights go to L2 before waiting for the preceding kernel.  A
     // prefetch cannot leave stale data behind (L2 is the point of coherence,
     // and the copies below read through it after the wait).
-    // With resident weights the first ring of stages goes straight to shared
-    // memory here, during the preceding kernel; only the stages beyond the
-    // ring are prefetched into L2.
-    const int first = min(nstages, P.ns);
     if (warp == pwarp) {
-        if (P.early)
-            for (int st = lane; st < first; st += 32) issue(st);
-        for (int st = (P.early ? first : 0) + lane; st < nstages; st += 32) {
+        for (int st = lane; st < nstages; st += 32) {
             pieces(st, [&](int i0, int cnt, int) {
                 const int64_t row = real_row(i0);
                 bulk_prefetch_l2(qs + row * kq, uint32_t(cnt * kq));
@@ -448,8 +442,8 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         // the first ring-full of stages needs no slot to free up: the 32 lanes
         // issue those copies in parallel; lane 0 then refills slots as the
         // consumers release them
-        if (!P.early)
-            for (int st = lane; st < first; st += 32) issue(st);
+        const int first = min(nstages, P.ns);
+        for (int st = lane; st < first; st += 32) issue(st);
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
