@@ -272,7 +272,7 @@ attn_fwd_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant_
         const uint64_t dk0 = att_desc(sK), dk1 = att_desc(sK + Lay::KB);
         const uint64_t dv0 = att_desc(sV), dv1 = att_desc(sV + Lay::VB);
         const bool leader = lane == 0;
-        // waits by the whole warp, with one verdict for all lanes
+        // waits by the whole warp, with one outcome for all lanes
         auto wait_all = [&](uint64_t *bar, uint32_t parity) {
             const bool got = mbar_wait_spin(bar, parity, wait_ns, status);
             return __all_sync(0xffffffffu, got && *abort_flag == 0);
