@@ -535,7 +535,10 @@ def check_swiglu(got, p, f, rel, *, rows=None, cos=False, what=""):
 
 
 @pytest.mark.parametrize("f,k", [(6144, 4096), (1, 128), (7, 1152), (100, 3072), (2048, 12288),
-                                 (33, 16384)])
+                                 (33, 16384),
+                                 # 64-weight lanes; odd feature counts put a stage across the
+                                 # gate / up boundary of a CTA's rows
+                                 (7, 2048), (153, 4096), (1001, 8192)])
 def test_swiglu_decode(tq2, f, k):
     # m = 1: fused into the GEMV for k <= 12288 (the 6144 x 4096 case is the
     # decode fused gate/up shape, 2f = 12288 rows); k = 16384 takes the
