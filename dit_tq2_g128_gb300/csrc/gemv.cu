@@ -764,7 +764,11 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
         }
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // The next kernel of the stream may launch once every thread has passed
+    // this point: at once with resident weights (its early weight copies need
+    // the time), else after this CTA's x has been issued and quantised, so that
+    // the next call's set-up and prefetch do not compete with this call's x.
+    if (P.early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == pwarp) {
         if (lane == 0) {
             // half h: elements [64 j + 32 h, +32) of every j, as xr rows of 128 bytes
@@ -776,8 +780,10 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
                     "l"(reinterpret_cast<uint64_t>(&xmap)), "r"(0), "r"(h), "r"(0), "r"(smem_u32(xbar))
                     : "memory");
         }
-        if (!P.early)
+        if (!P.early) {
             for (int st = lane; st < first; st += 32) issue(st);
+            asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+        }
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
@@ -828,34 +834,39 @@ gemv_wide_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__rest
             // 2^22 / s (correctly rounded reciprocal, exact scaling)
             const float inv = s > 0.f ? __frcp_rn(s) * 4194304.0f : 0.f;
             // X = rint(x * inv) by one fused multiply-add onto 1.5 * 2^23 (|X| <= 2^22)
-            int X[kGwLaneW];
+            // B = the bits of that sum = 0x4B400000 + X.  Bytes 0 and 1 of B are
+            // those of X (the offset's low half is zero); byte 2 of X is byte 2
+            // of B minus 0x40, subtracted for two values at once with byte 3
+            // (0x4B) of each absorbing the borrow; sum X = sum B - 64 * 0x4B400000.
+            uint32_t B[kGwLaneW];
 #pragma unroll
-            for (int j = 0; j < kGwLaneW; ++j)
-                X[j] = __float_as_int(__fmaf_rn(xv[j], inv, 12582912.0f)) - 0x4B400000;
-            int ps[16];
+            for (int j = 0; j < kGwLaneW; ++j) B[j] = __float_as_uint(__fmaf_rn(xv[j], inv, 12582912.0f));
+            uint32_t ps[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) ps[j] = (X[4 * j] + X[4 * j + 1]) + (X[4 * j + 2] + X[4 * j + 3]);
+            for (int j = 0; j < 16; ++j) ps[j] = (B[4 * j] + B[4 * j + 1]) + (B[4 * j + 2] + B[4 * j + 3]);
 #pragma unroll
             for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
                 for (int j = 0; j < w; ++j) ps[j] += ps[j + w];
-            sx = -ps[0];  // the first accumulator of every row starts at -sum X
+            // the first accumulator of every row starts at -sum X (|sum X| <= 2^28: exact mod 2^32)
+            sx = -int(ps[0] - 64u * 0x4B400000u);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t x0 = uint32_t(X[16 * q + t]), x1 = uint32_t(X[16 * q + t + 4]);
-                    const uint32_t x2 = uint32_t(X[16 * q + t + 8]), x3 = uint32_t(X[16 * q + t + 12]);
-                    const uint32_t p01 = __byte_perm(x0, x1, 0x5140);
+                    const uint32_t x0 = B[16 * q + t], x1 = B[16 * q + t + 4];
+                    const uint32_t x2 = B[16 * q + t + 8], x3 = B[16 * q + t + 12];
+                    const uint32_t p01 = __byte_perm(x0, x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1
                     const uint32_t p23 = __byte_perm(x2, x3, 0x5140);
-                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);
-                    L[q][t][1] = __byte_perm(p01, p23, 0x7632);
-                    const uint32_t h01 = __byte_perm(x0, x1, 0x0062);
-                    const uint32_t h23 = __byte_perm(x2, x3, 0x0062);
-                    L[q][t][2] = __byte_perm(h01, h23, 0x5410);
+                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);        // byte 0 of X0..X3
+                    L[q][t][1] = __byte_perm(p01, p23, 0x7632);        // byte 1
+                    const uint32_t h01 = __byte_perm(x0, x1, 0x7632) - 0x00400040u;  // x0.b2 x0.b3 x1.b2 x1.b3
+                    const uint32_t h23 = __byte_perm(x2, x3, 0x7632) - 0x00400040u;
+                    L[q][t][2] = __byte_perm(h01, h23, 0x6420);        // byte 2 of X0..X3 (signed)
                 }
             sc = s * (1.0f / 4194304.0f);
         }
+        if (!P.early) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         const uint32_t kq32 = uint32_t(kq), kb2 = uint32_t(kb) * 2;
         const uint32_t code_off = uint32_t(kw0 / 4);
         const uint32_t d_off = code_bytes + uint32_t(kw0 / kBlockW) * 2;
