@@ -991,9 +991,7 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     P.k = int(k);
     P.C = C;
     P.swiglu = swiglu ? 1 : 0;
-    // (the 32-weight-lane kernel measured slower with early copies: 6.50 against
-    // 6.21 us at K=12288, N=4096, its ring holding only part of a CTA's stages)
-    P.early = resident && wide ? 1 : 0;
+    P.early = 0;  // set below, once the ring size is known
     P.f = int(n / 2);
     P.groups = std::max(1, (wide ? kGwConsumers : kGvMaxConsumers) / C);  // groups of C warps (one per chunk)
     // the CTAs split the rows (with swiglu: the features, two rows each)
@@ -1041,6 +1039,10 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
     }
     P.ns = ns;
     P.consumers = P.groups * C;
+    // Resident weights: copy early only when the ring holds all of a CTA's
+    // stages (measured slower otherwise: 7.6 against 6.9 us at K=N=8192, and
+    // 6.50 against 6.21 us with the 32-weight lanes at K=12288, N=4096).
+    P.early = resident && wide && ns >= nst ? 1 : 0;
     P.off_ring = uint32_t(x_bytes);
     P.off_partial = uint32_t(x_bytes + size_t(ns) * stage_bytes);
     P.off_bar = uint32_t((P.off_partial + partial_bytes + 7) & ~size_t(7));
