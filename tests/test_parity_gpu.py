@@ -482,6 +482,30 @@ def test_quantize_special_blocks(tq2):
     assert np.array_equal(_encode(tq2, w, n, k), oracle.quantize(w, n, k))
 
 
+def test_quantize_exponent_spans(tq2):
+    # blocks around the exact-integer route's limit (magnitudes spanning 22
+    # binades are summed as integers, 23 and more in double in index order),
+    # subnormals next to normals, and block means at the binary16 overflow edge
+    rng = np.random.default_rng(3)
+    blocks = []
+    for span in (0, 1, 21, 22, 23, 24, 40, 100):
+        b = rng.uniform(1.0, 2.0, 128) * np.where(rng.random(128) < 0.5, -1.0, 1.0)
+        b[rng.integers(0, 128, 3)] *= 2.0 ** -span
+        blocks.append(b)
+    blocks.append(np.r_[np.full(64, 1e-40), np.full(64, 1e-38)])          # subnormal + normal
+    blocks.append(np.r_[np.full(127, 1.4e-45), np.full(1, 1.0)])          # smallest subnormal
+    blocks.append(np.full(128, 65504.0))                                  # d = 65504
+    blocks.append(np.full(128, 65519.0))                                  # rounds down to 65504
+    blocks.append(np.full(128, 65520.0))                                  # rounds up to Inf: codes 1
+    blocks.append(np.full(128, 2.0 ** -25))                               # d below the half grid
+    blocks.append(np.full(128, 3.0 * 2.0 ** -26))                         # d rounds to the grid
+    for _ in range(24):
+        blocks.append(rng.standard_normal(128) * np.exp2(rng.uniform(-30, 30, 128)))
+    w = np.stack(blocks).astype(np.float32).reshape(1, -1)
+    n, k = 1, w.size
+    assert np.array_equal(_encode(tq2, w, n, k), oracle.quantize(w, n, k))
+
+
 def test_quantize_then_matmul(tq2):
     rng = np.random.default_rng(21)
     m, n, k = 64, 300, 1024
