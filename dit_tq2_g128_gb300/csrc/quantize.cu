@@ -55,33 +55,31 @@ __device__ __forceinline__ uint16_t to_half_rne(double v) {
     return uint16_t(sign | uint16_t((e + 15) << 10) | uint16_t(r - 1024.0));
 }
 
-// binary16 bits of S * 2^E, round to nearest even (S < 2^53): overflow to Inf
-// from 65520 up, subnormals on the 2^-24 grid (1024 carries into the exponent).
+// binary16 bits of S * 2^E, round to nearest even (S < 2^53): S is first
+// rounded to 24 bits with round-to-odd (the truncation's lost bits folded into
+// the last bit), which the binary16 conversion's round-to-nearest then rounds
+// exactly as it would round S itself (the intermediate keeps at least two more
+// bits than binary16 has, also on the subnormal grid); the power-of-two scale
+// is exact wherever the result can be nonzero.
 __device__ __forceinline__ uint16_t half_of_scaled(uint64_t S, int E) {
-    if (S == 0) return 0;
-    const int p = 63 - __clzll(static_cast<long long>(S));  // leading bit
-    int e = p + E;                                          // unbiased exponent of the value
-    // bits to drop: to 11 significant bits (normal) or to the 2^-24 grid (subnormal)
-    const int shift = e >= -14 ? p - 10 : -(E + 24);
-    uint64_t m;
-    if (shift <= 0) {
-        m = S << (-shift);
-    } else if (shift >= 64) {
-        m = 0;  // below half of the smallest subnormal
+    if (S == 0 || E < -126) return 0;  // S * 2^E < 2^-73: rounds to zero
+    const int p = 63 - __clzll(static_cast<long long>(S));
+    uint32_t m;
+    int k = E;
+    if (p > 23) {
+        const int sh = p - 23;
+        m = uint32_t(S >> sh) | uint32_t((S & ((uint64_t(1) << sh) - 1)) != 0);
+        k += sh;  // <= 97 + 29: a finite power of two
     } else {
-        m = S >> shift;
-        const uint64_t rem = S & ((uint64_t(1) << shift) - 1), half = uint64_t(1) << (shift - 1);
-        if (rem > half || (rem == half && (m & 1))) ++m;
+        m = uint32_t(S);
     }
-    if (e < -14) return uint16_t(m);  // subnormal (m == 1024 is the smallest normal's encoding)
-    if (m == 2048) m = 1024, ++e;
-    if (e > 15) return 0x7c00;
-    return uint16_t(((e + 15) << 10) | int(m - 1024));
+    const float y = float(m) * __int_as_float((k + 127) << 23);  // m < 2^24: exact conversion
+    return __half_as_ushort(__float2half_rn(y));
 }
 
 constexpr int kQWarps = kQThreads / 32;
 
-__global__ void __launch_bounds__(kQThreads)
+__global__ void __launch_bounds__(kQThreads, 5)
 quantize_kernel(const float *__restrict__ w, uint8_t *__restrict__ aos, int64_t nblk) {
     __shared__ float fb[kQWarps][kBlockW];  // the literal route's staging, per warp
     const int lane = threadIdx.x & 31, wi = threadIdx.x >> 5;
@@ -89,37 +87,36 @@ quantize_kernel(const float *__restrict__ w, uint8_t *__restrict__ aos, int64_t 
     auto one = [&](int64_t b, const float4 v) {
         const float x[4] = {v.x, v.y, v.z, v.w};
         uint32_t a[4];
-        int ex_lo = 255, ex_hi = 0;
-        bool wide = false;
 #pragma unroll
-        for (int f = 0; f < 4; ++f) {
-            a[f] = __float_as_uint(x[f]) & 0x7fffffffu;
-            const int E = int(a[f] >> 23);
-            wide |= E == 255;  // Inf or NaN
-            if (a[f] != 0) {
-                const int ex = E > 0 ? E : 1;
-                ex_lo = min(ex_lo, ex);
-                ex_hi = max(ex_hi, ex);
-            }
-        }
-        const int emin = int(__reduce_min_sync(0xffffffffu, uint32_t(ex_lo)));
-        const int emax = int(__reduce_max_sync(0xffffffffu, uint32_t(ex_hi)));
-        wide = __any_sync(0xffffffffu, wide) || (emax >= emin && emax - emin > 22);
+        for (int f = 0; f < 4; ++f) a[f] = __float_as_uint(x[f]) & 0x7fffffffu;
+        // largest magnitude, and smallest nonzero one (a - 1 wraps zero to the top)
+        const uint32_t amax = __reduce_max_sync(0xffffffffu, max(max(a[0], a[1]), max(a[2], a[3])));
+        const uint32_t amin1 =
+            __reduce_min_sync(0xffffffffu, min(min(a[0] - 1u, a[1] - 1u), min(a[2] - 1u, a[3] - 1u)));
+        const int emax = int(amax >> 23), emin = int((amin1 + 1u) >> 23);
+        // integer route: finite, every nonzero magnitude at least 2^-104 and
+        // within 22 binades of the largest (or all zero)
+        const bool fast = amax < 0x7f800000u && (amax == 0 || (emin >= 23 && emax - emin <= 22));
         uint16_t dh;
-        if (!wide) {
-            uint64_t t = 0;
-            if (emax >= emin) {  // some nonzero weight
+        if (fast) {
+            // v = |w| * 2^(150 - emin): an integer below 2^46, exact in binary32,
+            // split as vh * 2^23 + vl with both parts below 2^23, each read off
+            // the bits of a sum onto 2^23 (vh by a round-down add): FP32 and
+            // integer pipes only.  Per lane the biased bits add without overflow.
+            const float scale = __int_as_float((150 - emin + 127) << 23);
+            uint32_t hs = 0, ls = 0;
 #pragma unroll
-                for (int f = 0; f < 4; ++f)
-                    if (a[f] != 0) {
-                        const int E = int(a[f] >> 23);
-                        const uint64_t mant = (a[f] & 0x7fffffu) | (E > 0 ? 0x800000u : 0u);
-                        t += mant << ((E > 0 ? E : 1) - emin);
-                    }
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+            for (int f = 0; f < 4; ++f) {
+                const float v = __uint_as_float(a[f]) * scale;
+                const float rh = __fadd_rd(v * 1.1920928955078125e-7f, 8388608.0f);  // 2^23 + floor(v / 2^23)
+                const float vl = __fmaf_rn(rh - 8388608.0f, -8388608.0f, v);         // v mod 2^23, exact
+                hs += __float_as_uint(rh);
+                ls += __float_as_uint(vl + 8388608.0f);
             }
-            dh = half_of_scaled(t, emin - 157);  // (sum / 128) = t * 2^(emin - 150 - 7)
+            const uint32_t hi = __reduce_add_sync(0xffffffffu, hs - 4u * 0x4B000000u);  // < 2^30
+            const uint32_t lo = __reduce_add_sync(0xffffffffu, ls - 4u * 0x4B000000u);
+            const uint64_t S = (uint64_t(hi) << 23) + uint64_t(lo);
+            dh = half_of_scaled(S, emin - 157);  // (sum / 128) = S * 2^(emin - 150 - 7)
         } else {
 #pragma unroll
             for (int f = 0; f < 4; ++f) fb[wi][4 * lane + f] = x[f];
@@ -133,33 +130,41 @@ quantize_kernel(const float *__restrict__ w, uint8_t *__restrict__ aos, int64_t 
             dh = uint16_t(__shfl_sync(0xffffffffu, d32, 0));
             __syncwarp();
         }
+        // code: rint(w / d) in binary32 is >= 1 in magnitude exactly when the
+        // rounded quotient exceeds 1/2, i.e. when |w| / d > 1/2 + 2^-25 (a tie
+        // goes to the even 1/2), i.e. when |w| exceeds T, the largest binary32 not
+        // above d/2 + d * 2^-25: one round-toward-zero FMA per block, then an
+        // integer comparison of magnitudes per weight (no division).
         const float df = __half2float(__ushort_as_half(dh));
         const bool live = df > 0.f && isfinite(df);
+        const uint32_t tb = live ? __float_as_uint(__fmaf_rz(df, 2.98023223876953125e-8f, 0.5f * df)) : 0xffffffffu;
         uint32_t byte = 0;
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
-            int c = 1;
-            if (live) {
-                const float q = rintf(__fdiv_rn(x[f], df));
-                c = q >= 1.f ? 2 : (q <= -1.f ? 0 : 1);
-            }
-            byte |= uint32_t(c) << (2 * f);
+            const uint32_t c = a[f] > tb ? 2u - ((__float_as_uint(x[f]) >> 30) & 2u) : 1u;  // 2, or 0 if negative
+            byte |= c << (2 * f);
         }
         // qs[l] is this lane's byte: lanes 2i and 2i+1 store one 16-bit word
         // (a block starts on an even byte); lane 0 also stores d
-        const uint32_t hi = __shfl_down_sync(0xffffffffu, byte, 1);
+        const uint32_t hi8 = __shfl_down_sync(0xffffffffu, byte, 1);
         uint8_t *ob = aos + b * kBlockBytes;
-        if ((lane & 1) == 0) *reinterpret_cast<uint16_t *>(ob + lane) = uint16_t(byte | (hi << 8));
+        if ((lane & 1) == 0) *reinterpret_cast<uint16_t *>(ob + lane) = uint16_t(byte | (hi8 << 8));
         if (lane == 0) *reinterpret_cast<uint16_t *>(ob + 32) = dh;
     };
-    // grid-stride over blocks, two loads in flight per warp
-    for (int64_t b = int64_t(blockIdx.x) * kQWarps + wi; b < nblk; b += 2 * nw) {
-        const float4 v0 = __ldcs(reinterpret_cast<const float4 *>(w + b * kBlockW) + lane);
-        const bool two = b + nw < nblk;
-        float4 v1 = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (two) v1 = __ldcs(reinterpret_cast<const float4 *>(w + (b + nw) * kBlockW) + lane);
+    // grid-stride over blocks, two at a time; the next two blocks' loads are
+    // issued before the current two are encoded (four per warp in flight)
+    auto load = [&](int64_t blk) {
+        return blk < nblk ? __ldcs(reinterpret_cast<const float4 *>(w + blk * kBlockW) + lane)
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+    };
+    int64_t b = int64_t(blockIdx.x) * kQWarps + wi;
+    float4 n0 = load(b), n1 = load(b + nw);
+    for (; b < nblk; b += 2 * nw) {
+        const float4 v0 = n0, v1 = n1;
+        n0 = load(b + 2 * nw);
+        n1 = load(b + 3 * nw);
         one(b, v0);
-        if (two) one(b + nw, v1);
+        if (b + nw < nblk) one(b + nw, v1);
     }
 }
 
@@ -169,7 +174,7 @@ cudaError_t launch_quantize(const float *w, void *w_aos, int64_t n, int64_t k, c
     const int64_t nblk = n * (k / kBlockW);
     if (nblk == 0) return cudaSuccess;
     // resident CTAs, a grid-stride loop over the blocks
-    const int64_t grid = std::min<int64_t>((nblk + kQWarps - 1) / kQWarps, int64_t(ctx.num_sms) * 4);
+    const int64_t grid = std::min<int64_t>((nblk + kQWarps - 1) / kQWarps, int64_t(ctx.num_sms) * 5);
     quantize_kernel<<<unsigned(grid), kQThreads, 0, ctx.stream>>>(w, static_cast<uint8_t *>(w_aos), nblk);
     return cudaPeekAtLastError();
 }
