@@ -16,12 +16,13 @@
 // every partial sum fits a double's 53-bit significand: with the nonzero
 // magnitudes m_j * 2^(e_j - 150) (24-bit m_j) and e_max - e_min <= 22 the total
 // is below 2^53 units of 2^(e_min - 150), so the sequential sum equals the exact
-// one, which the warp forms in any order as a 64-bit integer of aligned
-// significands, and d is that integer times 2^(e_min - 157) rounded to binary16
-// with integer operations.  Blocks with a wider exponent span, or with an Inf
-// or NaN, take the literal route: lane 0 adds the 128 magnitudes in double in
-// index order.  Both give the same bytes; the FP64 pipe, a small fraction of
-// the FP32 one on this part, is used only for the rare wide blocks.
+// one, which the warp forms in any order as an integer of aligned significands
+// (FP32 and integer instructions only), and d is that integer times
+// 2^(e_min - 157) rounded to binary16.  Blocks with a wider exponent span,
+// magnitudes below 2^-104, or an Inf or NaN take the literal route: lane 0
+// adds the 128 magnitudes in double in index order.  Both give the same bytes;
+// the FP64 pipe, a small fraction of the FP32 one on this part, is used only
+// for those blocks.  The codes need no division (see the code step below).
 #include <algorithm>
 
 #include <cuda_fp16.h>
