@@ -423,11 +423,13 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
     // the residual) is touched only after this.
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // Programmatic dependent launch: the next kernel of the stream may start
-    // launching now.  Two CTAs of this kernel fit on one SM, so the next
-    // call's set-up and weight prefetch overlap this call's arithmetic (which
-    // needs no memory bandwidth); the next call reads nothing a predecessor
-    // may write before its own griddepcontrol.wait.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // launching once every thread of this CTA has passed its trigger below
+    // (the producer after issuing x and the first stages, consumers after
+    // quantising x, idle warps at once).  Two CTAs of this kernel fit on one
+    // SM, so the next call's set-up and weight prefetch overlap this call's
+    // arithmetic without competing with this call's x; the next call reads
+    // nothing a predecessor may write before its own griddepcontrol.wait.
+    if (warp != pwarp && warp >= consumers) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     if (warp == pwarp) {
         // x first: one tensor copy per box of 128-byte rows (32 elements), each
         // row's 16-byte pieces permuted by the 128-byte swizzle (piece i of row
@@ -444,6 +446,7 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
         // consumers release them
         const int first = min(nstages, P.ns);
         for (int st = lane; st < first; st += 32) issue(st);
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         if (producer) {
             for (int st = P.ns; st < nstages; ++st) {
                 const int slot = st % P.ns, u = st / P.ns;
@@ -502,29 +505,35 @@ gemv_stream_kernel(const __grid_constant__ CUtensorMap xmap, const uint8_t *__re
             // where the binary32 spacing is 1, so the low mantissa bits hold
             // X + 2^22.  |x * inv| <= 2^22 + 2^-2 (the reciprocal is within half
             // an ulp), so |X| <= 2^22 without a clamp.
-            int X[kGvLaneW];
+            // B = the bits of that sum = 0x4B400000 + X: bytes 0 and 1 are those
+            // of X, byte 2 of X is byte 2 of B minus 0x40 (two values per
+            // subtraction, byte 3 = 0x4B absorbing the borrow), and
+            // sum X = sum B - 32 * 0x4B400000 (mod 2^32; |sum X| <= 2^27)
+            uint32_t B[kGvLaneW];
+            uint32_t bs = 0;
 #pragma unroll
             for (int j = 0; j < kGvLaneW; ++j) {
-                X[j] = __float_as_int(__fmaf_rn(xv[j], inv, 12582912.0f)) - 0x4B400000;
-                sx += X[j];
+                B[j] = __float_as_uint(__fmaf_rn(xv[j], inv, 12582912.0f));
+                bs += B[j];
             }
-            sx = -sx;  // the first accumulator of every row starts at -sum X (the "- 1" of c - 1)
+            sx = -int(bs - 32u * 0x4B400000u);  // the first accumulator of every row starts at -sum X
 #pragma unroll
             for (int q = 0; q < 2; ++q)
 #pragma unroll
                 for (int t = 0; t < 4; ++t) {
-                    const uint32_t x0 = uint32_t(X[16 * q + t]), x1 = uint32_t(X[16 * q + t + 4]);
-                    const uint32_t x2 = uint32_t(X[16 * q + t + 8]), x3 = uint32_t(X[16 * q + t + 12]);
+                    const uint32_t x0 = B[16 * q + t], x1 = B[16 * q + t + 4];
+                    const uint32_t x2 = B[16 * q + t + 8], x3 = B[16 * q + t + 12];
                     const uint32_t p01 = __byte_perm(x0, x1, 0x5140);  // x0.b0 x1.b0 x0.b1 x1.b1
                     const uint32_t p23 = __byte_perm(x2, x3, 0x5140);
-                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);        // byte 0 of x0..x3
+                    L[q][t][0] = __byte_perm(p01, p23, 0x5410);        // byte 0 of X0..X3
                     L[q][t][1] = __byte_perm(p01, p23, 0x7632);        // byte 1
-                    const uint32_t h01 = __byte_perm(x0, x1, 0x0062);  // x0.b2 x1.b2
-                    const uint32_t h23 = __byte_perm(x2, x3, 0x0062);
-                    L[q][t][2] = __byte_perm(h01, h23, 0x5410);        // byte 2 (signed)
+                    const uint32_t h01 = __byte_perm(x0, x1, 0x7632) - 0x00400040u;
+                    const uint32_t h23 = __byte_perm(x2, x3, 0x7632) - 0x00400040u;
+                    L[q][t][2] = __byte_perm(h01, h23, 0x6420);        // byte 2 of X0..X3 (signed)
                 }
             sc = s * (1.0f / 4194304.0f);  // s * 2^-22
         }
+        asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
         // loop-invariant 32-bit shared-memory offsets of this lane's data in a
         // slot: code bytes of row u at code_off + u * kq, the row's block scale
         // at d_off + u * kb * 2
