@@ -68,6 +68,8 @@ def parse():
                     help="instead of the bench line: tq2_gemm at the skinny-sweep shape (M rows, K=N=4096) "
                          "alone, `--steps` calls after `--warmup` on rotating weight copies, one JSON line "
                          "with the time per call (for profiling that path)")
+    ap.add_argument("--encoder", action="store_true",
+                    help="only tq2_quantize_f32 at 12288 x 3072 (the encoder's ncu workload)")
     ap.add_argument("--attention", action="store_true",
                     help="instead of the bench line: the DiT joint attention alone (24 heads x 4096 "
                          "tokens x 128, seeded N(0,1) inputs), `--steps` calls after `--warmup`, "
@@ -464,6 +466,35 @@ def run_attention_only(args):
             "us_per_call": round(t * 1e6, 2), "TFLOPs": round(4.0 * h * s * s * d / t / 1e12, 2)}
 
 
+def run_encoder_only(args):
+    """tq2_quantize_f32 on the largest DiT weight (12288 x 3072, N(0, 0.02)
+    weights as in the suite), nothing else: the workload of the encoder's ncu
+    summary.  The calls are captured in one CUDA graph."""
+    import torch
+    import dit_tq2_g128_gb300 as tq2
+
+    n, k = 12288, 3072
+    wf = torch.randn((n, k), device="cuda", generator=torch.Generator(device="cuda").manual_seed(12)) * 0.02
+    aos = torch.empty(tq2.tq2_soa_bytes(n, k), dtype=torch.uint8, device="cuda")
+
+    def step(i):
+        tq2.tq2_quantize_f32(wf, aos, n, k)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    steps = max(args.steps, 1)
+    g = graph_of(step, steps, torch)
+    g.replay()
+    torch.cuda.synchronize()
+    t = statistics.median(time_graph(g, torch, reps=3)) / steps
+    assert tq2.tq2_device_status() == tq2.TQ2_OK
+    return {"workload": "encoder_f32_to_blocks_12288x3072", "steps": args.steps, "warmup": args.warmup,
+            "us_per_call": round(t * 1e6, 2), "f32_GBps": round(n * k * 4 / t / 1e9, 1),
+            "bytes_GBps": round((n * k * 4 + tq2.tq2_soa_bytes(n, k)) / t / 1e9, 1),
+            "method": "steps captured in one CUDA graph, median of 3 replays"}
+
+
 def run_skinny_only(args):
     """tq2_gemm at M = args.skinny rows, K = N = 4096 (the skinny sweep's shape),
     nothing else: the workload of the skinny kernel's ncu summary."""
@@ -857,6 +888,9 @@ def main():
         return
     if args.skinny:
         print(json.dumps(run_skinny_only(args)), flush=True)
+        return
+    if args.encoder:
+        print(json.dumps(run_encoder_only(args)), flush=True)
         return
     if args.cpu_configs:
         print(json.dumps(run_cpu_configs()), flush=True)
