@@ -134,17 +134,24 @@ quantize_kernel(const float *__restrict__ w, uint8_t *__restrict__ aos, int64_t 
         // code: rint(w / d) in binary32 is >= 1 in magnitude exactly when the
         // rounded quotient exceeds 1/2, i.e. when |w| / d > 1/2 + 2^-25 (a tie
         // goes to the even 1/2), i.e. when |w| exceeds T, the largest binary32 not
-        // above d/2 + d * 2^-25: one round-toward-zero FMA per block, then an
-        // integer comparison of magnitudes per weight (no division).
+        // above d/2 + d * 2^-25: one round-toward-zero FMA per block (T = +Inf
+        // when d is zero or not finite: every code 1).  Per weight, on the FP32
+        // pipe: g = saturate((|w| - T) * 2^127) is exactly 1 when |w| > T (the
+        // smallest positive difference, 2^-48 or more, times 2^127 exceeds 1) and
+        // 0 otherwise (NaN saturates to 0), the code is g * sign(w) + 1, and its
+        // bits are read off a sum onto 2^23.  No division.
         const float df = __half2float(__ushort_as_half(dh));
         const bool live = df > 0.f && isfinite(df);
-        const uint32_t tb = live ? __float_as_uint(__fmaf_rz(df, 2.98023223876953125e-8f, 0.5f * df)) : 0xffffffffu;
-        uint32_t byte = 0;
+        const float tf = live ? __fmaf_rz(df, 2.98023223876953125e-8f, 0.5f * df) : __int_as_float(0x7f800000);
+        uint32_t cb[4];
 #pragma unroll
         for (int f = 0; f < 4; ++f) {
-            const uint32_t c = a[f] > tb ? 2u - ((__float_as_uint(x[f]) >> 30) & 2u) : 1u;  // 2, or 0 if negative
-            byte |= c << (2 * f);
+            const float g = __saturatef((__uint_as_float(a[f]) - tf) * 1.7014118346046923e38f);  // 2^127
+            const float sgn = __uint_as_float((__float_as_uint(x[f]) & 0x80000000u) | 0x3f800000u);  // +-1
+            cb[f] = __float_as_uint(__fmaf_rn(g, sgn, 1.0f) + 8388608.0f);  // 0x4B000000 + code
         }
+        // the offsets of the four sums vanish from the low byte after the shifts
+        const uint32_t byte = (cb[0] + (cb[1] << 2) + (cb[2] << 4) + (cb[3] << 6)) & 0xffu;
         // qs[l] is this lane's byte: lanes 2i and 2i+1 store one 16-bit word
         // (a block starts on an even byte); lane 0 also stores d
         const uint32_t hi8 = __shfl_down_sync(0xffffffffu, byte, 1);
