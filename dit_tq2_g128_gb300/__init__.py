@@ -46,7 +46,8 @@ EXPORTS = (
     "tq2_gemm",
     "tq2_gemm_f32ref", "tq2_gemm_with", "tq2_select_kernel", "tq2_set_wait_timeout_ns",
     "tq2_device_status", "tq2_version", "tq2_gemm_workspace_bytes", "tq2_gemm_ws",
-    "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu", "tq2_act16_from_f32",
+    "tq2_gemm_noalloc", "tq2_quantize_f32", "tq2_gate_up_swiglu", "tq2_gate_up_swiglu_resident",
+    "tq2_act16_from_f32",
     "tq2_act16_to_f32", "tq2_gemm_act16", "tq2_attention_f32",
 )
 
@@ -102,8 +103,10 @@ def _load():
     L.tq2_gemm_act16.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     L.tq2_attention_f32.restype = i32
     L.tq2_attention_f32.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
-    L.tq2_gate_up_swiglu.restype = i32
-    L.tq2_gate_up_swiglu.argtypes = [vp, vp, vp, i64, i64, i64, vp]
+    for name in ("tq2_gate_up_swiglu", "tq2_gate_up_swiglu_resident"):
+        f = getattr(L, name)
+        f.restype = i32
+        f.argtypes = [vp, vp, vp, i64, i64, i64, vp]
     L.tq2_gemm_noalloc.restype = i32
     L.tq2_gemm_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i64, vp]
     return L
@@ -197,6 +200,11 @@ def tq2_attention_f32(q, k, v, out, heads: int, seq: int, dim: int, stream=None)
 def tq2_gate_up_swiglu(w_soa, x, out, m: int, f: int, k: int, stream=None) -> None:
     _check(lib.tq2_gate_up_swiglu(_ptr(w_soa), _ptr(x), _ptr(out), m, f, k, _stream(stream)),
            "tq2_gate_up_swiglu")
+
+
+def tq2_gate_up_swiglu_resident(w_soa, x, out, m: int, f: int, k: int, stream=None) -> None:
+    _check(lib.tq2_gate_up_swiglu_resident(_ptr(w_soa), _ptr(x), _ptr(out), m, f, k, _stream(stream)),
+           "tq2_gate_up_swiglu_resident")
 
 
 def tq2_gemv(w_soa, x, residual, out, n: int, k: int, stream=None) -> None:

@@ -302,8 +302,8 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
     return tq2_gemm_with(TQ2_KERNEL_AUTO, w_soa, x, residual, out, m, n, k, stream);
 }
 
-int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
-                       int64_t k, void *stream) {
+static int gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                          int64_t k, void *stream, bool resident) {
     if (k <= 0 || k % tq2::kBlockW) return TQ2_ERR_BAD_K;
     if (f < 0 || f > (int64_t(1) << 39)) return TQ2_ERR_INVALID_ARG;
     bool noop = false;
@@ -319,7 +319,7 @@ int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m,
     if (st != TQ2_OK) return st;
     cudaError_t e = cudaErrorNotSupported;
     if (m == 1) {
-        e = tq2::launch_gemv_swiglu(w_soa, x, out, f, k, ctx);
+        e = tq2::launch_gemv_swiglu(w_soa, x, out, f, k, ctx, resident);
     } else if (f % 16 == 0) {
         void *ws = nullptr;
         if (cudaMallocAsync(&ws, tq2::tc_swiglu_ws_bytes(m, k), ctx.stream) != cudaSuccess) {
@@ -343,6 +343,16 @@ int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m,
     if (st == TQ2_OK) st = finish(tq2::launch_swiglu_rows(static_cast<const float *>(gu), out, m, f, ctx));
     const cudaError_t fr = cudaFreeAsync(gu, ctx.stream);
     return st != TQ2_OK ? st : finish(fr);
+}
+
+int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                       int64_t k, void *stream) {
+    return gate_up_swiglu(w_soa, x, out, m, f, k, stream, false);
+}
+
+int tq2_gate_up_swiglu_resident(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                                int64_t k, void *stream) {
+    return gate_up_swiglu(w_soa, x, out, m, f, k, stream, true);
 }
 
 int tq2_act16_from_f32(const float *x, void *x16, int64_t m, int64_t k, void *stream) {

@@ -1119,9 +1119,9 @@ cudaError_t launch_gemv_stream(const void *w_soa, const float *x, const float *r
 }
 
 cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,
-                               const LaunchCtx &ctx) {
+                               const LaunchCtx &ctx, bool resident) {
     if (k > int64_t(kGvMaxConsumers) * kGvChunk || 2 * f > INT32_MAX) return cudaErrorNotSupported;
-    return launch_gemv_stream(w_soa, x, nullptr, out, 2 * f, k, true, false, ctx);
+    return launch_gemv_stream(w_soa, x, nullptr, out, 2 * f, k, true, resident, ctx);
 }
 
 cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual, float *out,

@@ -50,7 +50,7 @@ cudaError_t launch_gemv(const void *w_soa, const float *x, const float *residual
 // Fused gate/up + SwiGLU (weight rows [0, f) gate, [f, 2f) up; out [m, f]).
 // cudaErrorNotSupported: shape outside the fused kernels (the caller falls back).
 cudaError_t launch_gemv_swiglu(const void *w_soa, const float *x, float *out, int64_t f, int64_t k,
-                               const LaunchCtx &ctx);
+                               const LaunchCtx &ctx, bool resident = false);
 cudaError_t launch_tc_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
                              int64_t k, void *ws, const LaunchCtx &ctx);
 size_t tc_swiglu_ws_bytes(int64_t m, int64_t k);

@@ -214,6 +214,16 @@ int tq2_gemm(const void *w_soa, const float *x, const float *residual, float *ou
 int tq2_gate_up_swiglu(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
                        int64_t k, void *stream);
 
+/* tq2_gate_up_swiglu for weights that stay resident across calls: the same
+ * arguments, arithmetic and result, bit for bit.  Contract (as
+ * tq2_gemv_resident): no work that is still unfinished when this call is
+ * enqueued writes w_soa.  At m = 1 the call may then copy its weight rows into
+ * shared memory before it waits for the preceding kernel of the stream;
+ * other m are computed exactly as tq2_gate_up_swiglu.  Errors as
+ * tq2_gate_up_swiglu. */
+int tq2_gate_up_swiglu_resident(const void *w_soa, const float *x, float *out, int64_t m, int64_t f,
+                                int64_t k, void *stream);
+
 /* Binary16 activation layout (activation-resident chaining of layers): a
  * row-major [m][k] array of binary16 in which element i (0..15) of every
  * 16-element group of a row is stored at position 2i for i < 8 and 2(i-8)+1

@@ -572,6 +572,24 @@ def test_swiglu_decode(tq2, f, k):
     check_swiglu(run_swiglu(tq2, w, p, f), p, f, TOL_F32, what=f"swiglu m=1 f={f} k={k}")
 
 
+@pytest.mark.parametrize("m,f,k", [(1, 6144, 4096), (1, 7, 2048), (1, 153, 4096), (1, 100, 3072),
+                                   (1, 33, 16384), (2, 64, 256), (8, 100, 384)])
+def test_swiglu_resident_equals_swiglu_bit_for_bit(tq2, m, f, k):
+    # resident weights change only when the weight copies are issued (m = 1,
+    # 64-weight lanes); every other shape runs the same code as tq2_gate_up_swiglu
+    p = tq2_synth.make_problem(m, 2 * f, k, seed=m * 13 + f + k)
+    w = upload(tq2, p)
+    torch.cuda.synchronize()
+    x = torch.from_numpy(p.x).cuda()
+    a = torch.full((m, f), float("nan"), device="cuda")
+    b = torch.full((m, f), float("nan"), device="cuda")
+    tq2.tq2_gate_up_swiglu(w, x, a, m, f, k)
+    tq2.tq2_gate_up_swiglu_resident(w, x, b, m, f, k)
+    torch.cuda.synchronize()
+    assert torch.isfinite(a).all()
+    assert torch.equal(a, b)
+
+
 @pytest.mark.parametrize("m,f,k", [(8, 512, 1024), (2, 64, 256), (129, 48, 640), (300, 1024, 3072),
                                    (64, 6144, 4096), (5, 40, 384), (20, 1000, 1152), (3, 7, 128)])
 def test_swiglu_batched(tq2, m, f, k):
